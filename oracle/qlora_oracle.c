@@ -1,0 +1,367 @@
+/*
+ * qlora_oracle.c -- the plain, slow CPU oracle for the NF4 + double-quantized
+ * LoRA linear layer.
+ *
+ * THIS IS TEST INFRASTRUCTURE. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load it. The GPU library shares no code, no
+ * header and no constant with this file, and must never call it.
+ *
+ * Sources (web pages on QLoRA; cited by page title and section):
+ *  [QL-note]  inquiringlines.com, "Can we finetune huge language models on a
+ *             single GPU?" -- the paragraph on the mechanism (NF4 bins hold an
+ *             equal share of a zero-centred normal; double quantization
+ *             quantizes the quantization constants; gradients flow through the
+ *             frozen 4-bit weights into LoRA adapters).
+ *  [QL-70B]   ashishsrivastav.com, "QLoRA: Fine-Tuning a 70B on One GPU" --
+ *             sections "NF4 Quantization: Beyond Standard INT4" (16 levels from
+ *             the normal CDF, each weight mapped to the closest level, done once
+ *             before training) and "Double Quantization: Squeezing the
+ *             Constants" (constants stored as INT8; dequantization on the fly
+ *             to the compute type).
+ *  [QL-host]  serverroom.net, "Fine-tuning an LLM on a GPU: memory requirements
+ *             for LoRA and QLoRA" -- section "What LoRA and QLoRA change in
+ *             memory" (nf4, double quant, bf16 compute; dropout 0, no bias in
+ *             the adapter setup listing).
+ *  [QL-mem]   xingyuzhitong.com, "Fine-Tuning Memory Requirements: Full
+ *             Training vs LoRA vs QLoRA" -- sections "LoRA: freeze the base,
+ *             train small adapters" (r x (d_in + d_out) adapter parameters) and
+ *             "QLoRA: quantize the frozen base to 4 bits" (dequantize on the fly).
+ *
+ * Precision: the codec takes every decision that yields an integer (a 4-bit
+ * code, an int8 absmax code) in fp32, the precision the GPU kernels use, and
+ * spells out each fp32 rounding. The linear algebra accumulates in fp64.
+ * Compile with -ffp-contract=off: no fused multiply-add anywhere.
+ *
+ * Layout conventions shared with the library's C-ABI (a data format, not code):
+ * W is [rows=N out, cols=K in] row-major bf16; blocks of 64 run along the
+ * flattened row-major order; byte i of the packed codes holds element 2i in
+ * its high nibble and element 2i+1 in its low nibble; absmax codes are int8,
+ * one per block; one fp32 scale per group of 256 blocks; one fp32 mean.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define NF4_BLOCK 64
+#define DQ_GROUP 256
+
+/* ------------------------------------------------------------------------ */
+/* bf16 <-> fp32 (bit-level; bf16 is the upper half of an IEEE binary32).    */
+/* ------------------------------------------------------------------------ */
+static float bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Round-to-nearest-even from binary32 to bfloat16, for finite inputs. */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+float oracle_bf16_to_f32(uint16_t h) { return bf16_to_f32(h); }
+
+/* ------------------------------------------------------------------------ */
+/* NF4 code table [QL-note mechanism; QL-70B "NF4 Quantization"].            */
+/* ------------------------------------------------------------------------ */
+
+/* Standard normal CDF through the complementary error function. */
+static double std_normal_cdf(double x) { return 0.5 * erfc(-x / sqrt(2.0)); }
+
+/* Inverse standard normal CDF by bisection until the bracket cannot shrink
+ * further in double precision. Slow and obviously monotone. */
+double oracle_norm_ppf(double p) {
+    double lo = -40.0, hi = 40.0;
+    for (int it = 0; it < 4000; ++it) {
+        double mid = 0.5 * (lo + hi);
+        if (mid <= lo || mid >= hi) break;
+        if (std_normal_cdf(mid) < p) lo = mid; else hi = mid;
+    }
+    /* return the bracket end whose CDF is closer to p */
+    return (fabs(std_normal_cdf(lo) - p) <= fabs(std_normal_cdf(hi) - p)) ? lo : hi;
+}
+
+double oracle_norm_cdf(double x) { return std_normal_cdf(x); }
+
+/* Outermost probability used for the table. With 16 equal-mass bins the
+ * centre of the outermost bin sits at 1 - 1/32; with 15 bins at 1 - 1/30.
+ * The table is built from an 8-level half and a 7-level half, so the reading
+ * taken here is the average of the two. */
+double oracle_nf4_delta(void) { return 0.5 * (31.0 / 32.0 + 29.0 / 30.0); }
+
+/* Probability of level j on a half with n levels: equal steps from 1/2 to
+ * delta (j = 1..n). */
+double oracle_nf4_prob(int j, int n) {
+    double d = oracle_nf4_delta();
+    return 0.5 + (d - 0.5) * ((double)j / (double)n);
+}
+
+/* Fills L[0..15]: 7 negative levels, an exact zero at code 7, 8 positive
+ * levels; each half is divided by its own outermost quantile so that
+ * L[0] = -1 and L[15] = +1 exactly. Rounded once from double to fp32. */
+void oracle_nf4_table(float L[16]) {
+    double pos[9], neg[8];
+    for (int j = 1; j <= 8; ++j) pos[j] = oracle_norm_ppf(oracle_nf4_prob(j, 8));
+    for (int j = 1; j <= 7; ++j) neg[j] = -oracle_norm_ppf(oracle_nf4_prob(j, 7));
+    for (int j = 1; j <= 7; ++j) L[7 - j] = (float)(neg[j] / fabs(neg[7]));
+    L[7] = 0.0f;
+    for (int j = 1; j <= 8; ++j) L[7 + j] = (float)(pos[j] / pos[8]);
+}
+
+/* Nearest level to x (fp32). Distances are compared in double; ties go to
+ * the lower code because only a strictly smaller distance moves the choice. */
+int oracle_nf4_nearest(float x, const float L[16]) {
+    int best = 0;
+    double bd = fabs((double)x - (double)L[0]);
+    for (int i = 1; i < 16; ++i) {
+        double d = fabs((double)x - (double)L[i]);
+        if (d < bd) { bd = d; best = i; }
+    }
+    return best;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Blockwise absmax + NF4 encode + packing [QL-70B "NF4 Quantization"].     */
+/* ------------------------------------------------------------------------ */
+
+/* Encodes n = rows*cols bf16 weights (n % 64 == 0). Writes the packed codes
+ * (n/2 bytes) and the exact per-block absmax (n/64 floats). The codes use the
+ * exact absmax: the weights are quantized first, then the constants. */
+void oracle_nf4_encode(const uint16_t *W, int64_t n, uint8_t *codes, float *absmax) {
+    float L[16];
+    oracle_nf4_table(L);
+    int64_t nb = n / NF4_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint16_t *w = W + b * NF4_BLOCK;
+        float a = 0.0f;
+        for (int i = 0; i < NF4_BLOCK; ++i) {
+            float v = fabsf(bf16_to_f32(w[i]));
+            if (v > a) a = v;
+        }
+        absmax[b] = a;
+        int c[NF4_BLOCK];
+        for (int i = 0; i < NF4_BLOCK; ++i) {
+            if (a == 0.0f) {
+                c[i] = 7; /* the exact-zero level */
+            } else {
+                float x = bf16_to_f32(w[i]) / a; /* fp32, round to nearest */
+                c[i] = oracle_nf4_nearest(x, L);
+            }
+        }
+        for (int i = 0; i < NF4_BLOCK / 2; ++i)
+            codes[b * (NF4_BLOCK / 2) + i] = (uint8_t)((c[2 * i] << 4) | c[2 * i + 1]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Double quantization of the absmax [QL-note; QL-70B "Double Quantization"] */
+/* ------------------------------------------------------------------------ */
+
+/* Pairwise (balanced binary tree) sum in double: the leaves, in order, padded
+ * with zeros to a power of two; each level adds neighbours (2i, 2i+1). */
+double oracle_pairwise_sum(const float *v, int64_t n) {
+    if (n <= 0) return 0.0;
+    int64_t p = 1;
+    while (p < n) p <<= 1;
+    double *t = (double *)calloc((size_t)p, sizeof(double));
+    for (int64_t i = 0; i < n; ++i) t[i] = (double)v[i];
+    while (p > 1) {
+        for (int64_t i = 0; i < p / 2; ++i) t[i] = t[2 * i] + t[2 * i + 1];
+        p /= 2;
+    }
+    double s = t[0];
+    free(t);
+    return s;
+}
+
+/* Second-level quantization of the nb block absmax values:
+ *   mean  = fp32( S / nb ),  S the pairwise double sum above;
+ *   per group g of 256 blocks (the last may be partial):
+ *     c_b = fp32(a_b - mean)
+ *     s2_g = fp32( max_b |c_b| / 127 )
+ *     q_b  = 0 if s2_g == 0, else clamp(rint(fp32(c_b / s2_g)), -127, 127)
+ *   with rint rounding half to even. */
+void oracle_dq_encode(const float *absmax, int64_t nb, int8_t *q, float *scale, float *mean_out) {
+    double S = oracle_pairwise_sum(absmax, nb);
+    float mean = (float)(S / (double)nb);
+    *mean_out = mean;
+    int64_t ng = (nb + DQ_GROUP - 1) / DQ_GROUP;
+    for (int64_t g = 0; g < ng; ++g) {
+        int64_t b0 = g * DQ_GROUP, b1 = b0 + DQ_GROUP;
+        if (b1 > nb) b1 = nb;
+        float m = 0.0f;
+        for (int64_t b = b0; b < b1; ++b) {
+            float c = absmax[b] - mean;
+            if (fabsf(c) > m) m = fabsf(c);
+        }
+        float s2 = m / 127.0f;
+        scale[g] = s2;
+        for (int64_t b = b0; b < b1; ++b) {
+            float c = absmax[b] - mean;
+            if (s2 == 0.0f) {
+                q[b] = 0;
+            } else {
+                float r = rintf(c / s2);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                q[b] = (int8_t)r;
+            }
+        }
+    }
+}
+
+/* Whole quantizer: encode, then double-quantize the absmax. absmax_exact may
+ * be NULL; when given it receives the first-level absmax (n/64 floats). */
+void oracle_nf4_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8_t *codes,
+                         int8_t *q, float *scale, float *mean, float *absmax_exact) {
+    int64_t n = rows * cols, nb = n / NF4_BLOCK;
+    float *a = absmax_exact ? absmax_exact : (float *)malloc((size_t)nb * sizeof(float));
+    oracle_nf4_encode(W, n, codes, a);
+    oracle_dq_encode(a, nb, q, scale, mean);
+    if (!absmax_exact) free(a);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode [QL-70B "Double Quantization": dequantize on the fly to the        */
+/* compute type; QL-host: the compute type is bf16].                         */
+/* ------------------------------------------------------------------------ */
+
+/* Reconstructed absmax of block b: fp32(q) * s2 rounded, then + mean rounded
+ * (two separate fp32 operations, never fused). */
+float oracle_dq_decode(int8_t qb, float s2, float mean) {
+    float t = (float)qb * s2;
+    return t + mean;
+}
+
+/* W'[i] = bf16_rne( fp32( L[code_i] * a'_b ) ) for all n elements. */
+void oracle_nf4_dequantize(const uint8_t *codes, const int8_t *q, const float *scale, float mean,
+                           int64_t rows, int64_t cols, uint16_t *out) {
+    float L[16];
+    oracle_nf4_table(L);
+    int64_t n = rows * cols, nb = n / NF4_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nb; ++b) {
+        float a = oracle_dq_decode(q[b], scale[b / DQ_GROUP], mean);
+        for (int i = 0; i < NF4_BLOCK; ++i) {
+            uint8_t byte = codes[b * (NF4_BLOCK / 2) + i / 2];
+            int c = (i % 2 == 0) ? (byte >> 4) : (byte & 15);
+            float v = L[c] * a;
+            out[b * NF4_BLOCK + i] = f32_to_bf16_rne(v);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Linear layer with LoRA, forward and backward, in fp64 on the dequantized  */
+/* bf16 weights [QL-note: gradients flow through the frozen 4-bit weights    */
+/* into the adapters; QL-mem "LoRA": A is r x d_in, B is d_out x r].         */
+/* s is the LoRA scale (alpha / r); adapter dropout is 0 and there is no     */
+/* bias [QL-host adapter setup].                                             */
+/* ------------------------------------------------------------------------ */
+
+/* U[m, j] = sum_k X[m,k] A[j,k]   for all m (U: M x r, double). */
+void oracle_lora_down(const uint16_t *X, int64_t M, int64_t K, const uint16_t *A, int r, double *U) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)bf16_to_f32(X[m * K + k]) * (double)bf16_to_f32(A[(int64_t)j * K + k]);
+            U[m * r + j] = acc;
+        }
+}
+
+/* V[m, j] = sum_n dY[m,n] B[n,j]   for all m (V: M x r, double). */
+void oracle_lora_up_t(const uint16_t *dY, int64_t M, int64_t N, const uint16_t *B, int r, double *V) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                acc += (double)bf16_to_f32(dY[m * N + n]) * (double)bf16_to_f32(B[n * r + j]);
+            V[m * r + j] = acc;
+        }
+}
+
+/* Forward: Y[m, n] = sum_k X[m,k] W'[n,k] + s * sum_j U[m,j] B[n,j].
+ * rows: the nr row indices m to compute (NULL: all M rows, nr = M);
+ * Y is nr x N in the order of rows. U is the full M x r down-projection. */
+void oracle_linear_fwd(const uint16_t *X, int64_t M, const uint16_t *Wdq, int64_t N, int64_t K,
+                       const uint16_t *A, const uint16_t *B, int r, float scale,
+                       const int64_t *rows, int64_t nr, double *Y, double *U) {
+    oracle_lora_down(X, M, K, A, r, U);
+    if (!rows) nr = M;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nr; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        for (int64_t n = 0; n < N; ++n) {
+            double base = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                base += (double)bf16_to_f32(X[m * K + k]) * (double)bf16_to_f32(Wdq[n * K + k]);
+            double lora = 0.0;
+            for (int j = 0; j < r; ++j) lora += U[m * r + j] * (double)bf16_to_f32(B[n * r + j]);
+            Y[i * N + n] = base + (double)scale * lora;
+        }
+    }
+}
+
+/* Backward, with V = dY B and U = X A^T recomputed in fp64:
+ *   dX[m, k] = sum_n dY[m,n] W'[n,k] + s * sum_j V[m,j] A[j,k]   (rows m listed)
+ *   dB[n, j] = s * sum_m dY[m,n] U[m,j]                          (rows n listed)
+ *   dA[j, k] = s * sum_m V[m,j] X[m,k]                           (columns k listed)
+ * No gradient for the frozen W. A NULL list means every index (and its count
+ * is then M, N or K); outputs are packed in list order: dX is nr x K, dB is
+ * nn x r, dA is r x nk. */
+void oracle_linear_bwd(const uint16_t *dY, const uint16_t *X, int64_t M, const uint16_t *Wdq,
+                       int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, int r,
+                       float scale, const int64_t *rows, int64_t nr, const int64_t *ncols,
+                       int64_t nn, const int64_t *kcols, int64_t nk, double *dX, double *dA,
+                       double *dB) {
+    double *U = (double *)malloc((size_t)(M * r) * sizeof(double));
+    double *V = (double *)malloc((size_t)(M * r) * sizeof(double));
+    oracle_lora_down(X, M, K, A, r, U);
+    oracle_lora_up_t(dY, M, N, B, r, V);
+    if (!rows) nr = M;
+    if (!ncols) nn = N;
+    if (!kcols) nk = K;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nr; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        for (int64_t k = 0; k < K; ++k) {
+            double base = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                base += (double)bf16_to_f32(dY[m * N + n]) * (double)bf16_to_f32(Wdq[n * K + k]);
+            double lora = 0.0;
+            for (int j = 0; j < r; ++j) lora += V[m * r + j] * (double)bf16_to_f32(A[(int64_t)j * K + k]);
+            dX[i * K + k] = base + (double)scale * lora;
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nn; ++i) {
+        int64_t n = ncols ? ncols[i] : i;
+        for (int j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += (double)bf16_to_f32(dY[m * N + n]) * U[m * r + j];
+            dB[i * r + j] = (double)scale * acc;
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nk; ++i) {
+        int64_t k = kcols ? kcols[i] : i;
+        for (int j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += V[m * r + j] * (double)bf16_to_f32(X[m * K + k]);
+            dA[(int64_t)j * nk + i] = (double)scale * acc;
+        }
+    }
+    free(U);
+    free(V);
+}
