@@ -1,0 +1,323 @@
+// lora_simt.cuh -- CUDA-core kernels of the LoRA linear layer:
+//   k_lora_down     U = P Q^T for a skinny Q (U = X A^T, V = dY B via B^T),
+//                   writes bf16 U and bf16 (s * U)
+//   k_transpose     B [N, r] -> B^T [r8, N] (zero rows beyond r)
+//   k_lora_grad     split-M partial sums of out[j, c] = sum_m P[m, j] Q[m, c]
+//   k_grad_reduce   sums the partials in a fixed order, applies s, stores
+//                   dA [r, K] or dB [N, r]
+//   k_fwd_simt      Y = X W'^T + (sU) B^T, NF4 decoded in the K loop
+//   k_dx_simt       dX = dY W' + (sV) A, NF4 decoded in the N loop
+// The tiled GEMMs here serve small M (and any shape, as a reference path on
+// the device); large M runs on the tcgen05 kernels.
+// Sources: xingyuzhitong.com "Fine-Tuning Memory Requirements", sections "LoRA:
+// freeze the base, train small adapters" and "QLoRA: quantize the frozen base
+// to 4 bits"; inquiringlines.com note, mechanism paragraph.
+#pragma once
+
+#include "common.cuh"
+
+namespace qlora {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// U[m, j] = sum_k P[m, k] Q[j, k] (fp32), j < r. One warp per 2 rows m,
+// 16 values of j per pass; lanes stride over K in 8-element chunks.
+// Writes U (bf16, stride ldu, may be null) and sU = bf16(s * U) (stride lds,
+// zero for r <= j < lds).
+__global__ void __launch_bounds__(256) k_lora_down(const uint16_t *__restrict__ P, int64_t M, int64_t K,
+                                                   const uint16_t *__restrict__ Q, int r, float s,
+                                                   uint16_t *__restrict__ U, int ldu, uint16_t *__restrict__ sU,
+                                                   int lds) {
+    const int lane = threadIdx.x & 31;
+    const int64_t m0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * 2;
+    if (m0 >= M) return;
+    const bool has1 = m0 + 1 < M;
+    const int64_t nch = K / 8;
+    for (int j0 = 0; j0 < r; j0 += 16) {
+        float acc0[16], acc1[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc0[j] = acc1[j] = 0.0f;
+        for (int64_t c = lane; c < nch; c += 32) {
+            const uint4 x0 = reinterpret_cast<const uint4 *>(P + m0 * K)[c];
+            const uint4 x1 = has1 ? reinterpret_cast<const uint4 *>(P + (m0 + 1) * K)[c] : make_uint4(0, 0, 0, 0);
+            const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (j0 + j < r) {
+                    const uint4 qv = reinterpret_cast<const uint4 *>(Q + (int64_t)(j0 + j) * K)[c];
+                    const uint32_t b[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float bl = bf16lo_to_f32(b[e]), bh = bf16hi_to_f32(b[e]);
+                        acc0[j] = fmaf(bf16lo_to_f32(a0[e]), bl, acc0[j]);
+                        acc0[j] = fmaf(bf16hi_to_f32(a0[e]), bh, acc0[j]);
+                        acc1[j] = fmaf(bf16lo_to_f32(a1[e]), bl, acc1[j]);
+                        acc1[j] = fmaf(bf16hi_to_f32(a1[e]), bh, acc1[j]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float u0 = warp_sum(acc0[j]), u1 = warp_sum(acc1[j]);
+            if (lane == j) {
+                const int jj = j0 + j;
+                if (jj < r) {
+                    if (U) {
+                        U[m0 * ldu + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(u0));
+                        if (has1) U[(m0 + 1) * ldu + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(u1));
+                    }
+                    sU[m0 * lds + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, u0)));
+                    if (has1) sU[(m0 + 1) * lds + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, u1)));
+                }
+            }
+        }
+    }
+    // zero the padding columns of sU
+    for (int jj = r + lane; jj < lds; jj += 32) {
+        sU[m0 * lds + jj] = 0;
+        if (has1) sU[(m0 + 1) * lds + jj] = 0;
+    }
+}
+
+// out[j, n] = in[n, j] for j < r, 0 for r <= j < r8.
+__global__ void k_transpose(const uint16_t *__restrict__ in, int64_t N, int r, int r8, uint16_t *__restrict__ out) {
+    const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    for (int j = 0; j < r8; ++j) out[(int64_t)j * N + n] = j < r ? in[n * r + j] : (uint16_t)0;
+}
+
+// Partial sums over one chunk of rows: part[chunk][j][c] = sum_{m in chunk}
+// P[m, j] Q[m, c] for c in a 64-column tile, j < r. P is bf16 [M, ldp],
+// Q is bf16 [M, C]. Thread layout: 64 columns x 4 j-groups.
+__global__ void __launch_bounds__(256) k_lora_grad(const uint16_t *__restrict__ P, int ldp,
+                                                   const uint16_t *__restrict__ Q, int64_t M, int64_t C, int r,
+                                                   int64_t rows_per_chunk, float *__restrict__ part) {
+    __shared__ float sP[64][129];
+    const int tc = threadIdx.x & 63, tj = threadIdx.x >> 6;
+    const int64_t c = (int64_t)blockIdx.x * 64 + tc;
+    const int64_t mbeg = (int64_t)blockIdx.y * rows_per_chunk;
+    const int64_t mend = min(M, mbeg + rows_per_chunk);
+    const int jper = (r + 3) / 4;
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+    for (int64_t mb = mbeg; mb < mend; mb += 64) {
+        const int nm = (int)min((int64_t)64, mend - mb);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nm * r; i += 256) {
+            const int mm = i / r, j = i % r;
+            sP[mm][j] = bf16lo_to_f32(P[(mb + mm) * ldp + j]);
+        }
+        __syncthreads();
+        for (int mm = 0; mm < nm; ++mm) {
+            const float qv = c < C ? bf16lo_to_f32(Q[(mb + mm) * C + c]) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int j = tj * jper + i;
+                if (i < jper && j < r) acc[i] = fmaf(sP[mm][j], qv, acc[i]);
+            }
+        }
+    }
+    if (c < C) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int j = tj * jper + i;
+            if (i < jper && j < r) part[((int64_t)blockIdx.y * r + j) * C + c] = acc[i];
+        }
+    }
+}
+
+// out = s * sum over chunks (in chunk order) of part[chunk][j][c];
+// transposed == 0: out[j * C + c] (dA [r, K]); 1: out[c * r + j] (dB [N, r]).
+__global__ void k_grad_reduce(const float *__restrict__ part, int nchunks, int r, int64_t C, float s,
+                              int transposed, float *__restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)r * C) return;
+    const int64_t j = i / C, c = i % C;
+    float acc = 0.0f;
+    for (int k = 0; k < nchunks; ++k) acc += part[(int64_t)k * r * C + i];
+    const float v = __fmul_rn(s, acc);
+    if (transposed) out[c * r + j] = v; else out[i] = v;
+}
+
+// ---- tiled SIMT GEMMs with NF4 decode (64 x 64 tiles, 4 x 4 per thread) ---
+constexpr int kSt = 64;
+
+// Decodes the 64 codes of block b (row n, columns k0..k0+63 of W') as fp32.
+// Thread `half` (0/1) decodes codes 32*half .. 32*half+31.
+__device__ __forceinline__ void decode_half_block(const uint8_t *__restrict__ codes, const int8_t *__restrict__ q,
+                                                  const float *__restrict__ s2, float mean, int64_t b, int half,
+                                                  float (&f)[32]) {
+    const float a = dq_absmax(q[b], s2[b / kGroup], mean);
+    const Nf4Table tab = make_table(a);
+    const uint4 cw = reinterpret_cast<const uint4 *>(codes + b * 32)[half];
+    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t o[4];
+        decode8(tab, w[i], o);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[8 * i + 2 * e] = bf16lo_to_f32(o[e]);
+            f[8 * i + 2 * e + 1] = bf16hi_to_f32(o[e]);
+        }
+    }
+}
+
+// Y[m, n] = sum_k X[m, k] W'[n, k] + sum_j sU[m, j] B[n, j]
+__global__ void __launch_bounds__(256) k_fwd_simt(const uint16_t *__restrict__ X, int64_t M, int64_t K,
+                                                  const uint8_t *__restrict__ codes, const int8_t *__restrict__ q,
+                                                  const float *__restrict__ s2, const float *__restrict__ mean_p,
+                                                  int64_t N, const uint16_t *__restrict__ sU, int ldu,
+                                                  const uint16_t *__restrict__ B, int r, uint16_t *__restrict__ Y) {
+    __shared__ float Xs[kSt][kSt + 1];  // [m][k]
+    __shared__ float Ws[kSt][kSt + 1];  // [k][n]
+    const int tid = threadIdx.x, tm = tid & 15, tn = tid >> 4;
+    const int64_t m0 = (int64_t)blockIdx.y * kSt, n0 = (int64_t)blockIdx.x * kSt;
+    const float mean = *mean_p;
+    float acc[4][4] = {};
+    for (int64_t k0 = 0; k0 < K; k0 += kSt) {
+        for (int i = tid; i < kSt * 8; i += 256) {
+            const int row = i >> 3, kc = i & 7;
+            const int64_t m = m0 + row;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (m < M) v = *reinterpret_cast<const uint4 *>(X + m * K + k0 + kc * 8);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                Xs[row][kc * 8 + 2 * e] = bf16lo_to_f32(u[e]);
+                Xs[row][kc * 8 + 2 * e + 1] = bf16hi_to_f32(u[e]);
+            }
+        }
+        if (tid < 128) {
+            const int row = tid >> 1, half = tid & 1;
+            const int64_t n = n0 + row;
+            float f[32];
+            if (n < N) {
+                decode_half_block(codes, q, s2, mean, (n * K + k0) / kBlock, half, f);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) Ws[half * 32 + e][row] = f[e];
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < kSt; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = Xs[tm * 4 + i][kk];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Ws[kk][tn * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    for (int j = 0; j < r; ++j) {
+        float u[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t m = m0 + tm * 4 + i;
+            u[i] = m < M ? bf16lo_to_f32(sU[m * ldu + j]) : 0.0f;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int64_t n = n0 + tn * 4 + jj;
+            b[jj] = n < N ? bf16lo_to_f32(B[n * r + j]) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(u[i], b[jj], acc[i][jj]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + tm * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int64_t n = n0 + tn * 4 + jj;
+            if (n < N) Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i][jj]));
+        }
+    }
+}
+
+// dX[m, k] = sum_n dY[m, n] W'[n, k] + sum_j sV[m, j] A[j, k]
+__global__ void __launch_bounds__(256) k_dx_simt(const uint16_t *__restrict__ dY, int64_t M, int64_t N,
+                                                 const uint8_t *__restrict__ codes, const int8_t *__restrict__ q,
+                                                 const float *__restrict__ s2, const float *__restrict__ mean_p,
+                                                 int64_t K, const uint16_t *__restrict__ sV, int ldv,
+                                                 const uint16_t *__restrict__ A, int r, uint16_t *__restrict__ dX) {
+    __shared__ float Ds[kSt][kSt + 1];  // [m][n]
+    __shared__ float Ws[kSt][kSt + 1];  // [n][k]
+    const int tid = threadIdx.x, tm = tid & 15, tk = tid >> 4;
+    const int64_t m0 = (int64_t)blockIdx.y * kSt, k0 = (int64_t)blockIdx.x * kSt;
+    const float mean = *mean_p;
+    float acc[4][4] = {};
+    for (int64_t n0 = 0; n0 < N; n0 += kSt) {
+        for (int i = tid; i < kSt * kSt; i += 256) {
+            const int row = i >> 6, nn = i & 63;
+            const int64_t m = m0 + row, n = n0 + nn;
+            Ds[row][nn] = (m < M && n < N) ? bf16lo_to_f32(dY[m * N + n]) : 0.0f;
+        }
+        if (tid < 128) {
+            const int row = tid >> 1, half = tid & 1;
+            const int64_t n = n0 + row;
+            float f[32];
+            if (n < N) {
+                decode_half_block(codes, q, s2, mean, (n * K + k0) / kBlock, half, f);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) Ws[row][half * 32 + e] = f[e];
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int nn = 0; nn < kSt; ++nn) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = Ds[tm * 4 + i][nn];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Ws[nn][tk * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    for (int j = 0; j < r; ++j) {
+        float v[4], a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t m = m0 + tm * 4 + i;
+            v[i] = m < M ? bf16lo_to_f32(sV[m * ldv + j]) : 0.0f;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) a[jj] = bf16lo_to_f32(A[(int64_t)j * K + k0 + tk * 4 + jj]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(v[i], a[jj], acc[i][jj]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + tm * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) dX[m * K + k0 + tk * 4 + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i][jj]));
+    }
+}
+
+}  // namespace qlora

@@ -1,0 +1,461 @@
+// qlora_lib.cu -- the C ABI (include/qlora.h): argument validation, workspace
+// layout and kernel launches. All kernels are compiled in this one
+// translation unit so they share the device error word.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+#include <algorithm>
+
+#include "qlora.h"
+
+#include "common.cuh"
+#include "codec.cuh"
+#include "lora_simt.cuh"
+
+using namespace qlora;
+
+namespace {
+
+thread_local std::string t_last_error;
+int64_t g_wait_limit = 0;  // 0: default
+
+qlora_status fail(qlora_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+qlora_status ok() {
+    t_last_error.clear();
+    return QLORA_OK;
+}
+
+inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;
+
+// ---- optional profiling of our own launches (qlora_profile_start/stop) ----
+struct ProfRec {
+    cudaEvent_t a, b;
+    int kind;
+};
+std::vector<ProfRec> g_prof;
+bool g_prof_on = false;
+int g_prof_count[QLORA_KERNEL_KINDS];
+
+struct ProfScope {
+    int kind;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr;
+    ProfScope(int k, cudaStream_t st) : kind(k), s(st) {
+        if (!g_prof_on) return;
+        g_prof_count[k]++;
+        if (cudaEventCreate(&a) == cudaSuccess) cudaEventRecord(a, s);
+    }
+    ~ProfScope() {
+        if (!g_prof_on || !a) return;
+        cudaEvent_t b;
+        if (cudaEventCreate(&b) == cudaSuccess) {
+            cudaEventRecord(b, s);
+            g_prof.push_back({a, b, kind});
+        }
+    }
+};
+
+qlora_status launch_check(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    return QLORA_OK;
+}
+
+bool valid_dims(int64_t rows, int64_t cols) {
+    return rows >= 0 && cols > 0 && cols % kBlock == 0 && rows < kMaxDim && cols < kMaxDim;
+}
+
+qlora_status check_weight(const qlora_nf4_weight *w, bool need_rows) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    if (!valid_dims(w->rows, w->cols))
+        return fail(QLORA_ERR_SHAPE, "weight shape [%lld, %lld]: need rows >= 0, cols > 0, cols %% 64 == 0",
+                    (long long)w->rows, (long long)w->cols);
+    if (need_rows && w->rows == 0) return fail(QLORA_ERR_SHAPE, "weight has 0 rows");
+    if (!w->codes || !w->absmax_q || !w->absmax_scale || !w->absmax_mean)
+        return fail(QLORA_ERR_NULL, "weight descriptor has a NULL array");
+    if (!al16(w->codes) || !al16(w->absmax_q) || !al16(w->absmax_scale) || !al16(w->absmax_mean))
+        return fail(QLORA_ERR_ALIGN, "weight arrays must be 16-byte aligned");
+    return QLORA_OK;
+}
+
+// Workspace carving helper: 256-byte aligned slices.
+struct Carve {
+    char *base;
+    size_t off = 0;
+    explicit Carve(void *b) : base(static_cast<char *>(b)) {}
+    template <class T>
+    T *take(size_t count) {
+        T *p = reinterpret_cast<T *>(base ? base + off : nullptr);
+        off = up(off + count * sizeof(T), 256);
+        return p;
+    }
+};
+
+// ---- quantize workspace: absmax fp32 [nb], group sums fp64 [ng], two
+// ping-pong fp64 buffers of ceil(ng / 256) for the upper tree levels.
+size_t quantize_ws(int64_t rows, int64_t cols, float **absmax, double **gsum, double **buf0, double **buf1,
+                   void *ws) {
+    const int64_t nb = rows * cols / kBlock, ng = cdiv(nb, kGroup), nl = cdiv(ng, 256) + 1;
+    Carve c(ws);
+    float *a = c.take<float>(nb);
+    double *g = c.take<double>(ng);
+    double *b0 = c.take<double>(nl);
+    double *b1 = c.take<double>(nl);
+    if (absmax) *absmax = a;
+    if (gsum) *gsum = g;
+    if (buf0) *buf0 = b0;
+    if (buf1) *buf1 = b1;
+    return c.off;
+}
+
+// ---- linear workspaces
+struct FwdWs {
+    uint16_t *sU;
+};
+size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
+    (void)N;
+    (void)K;
+    const int r8 = (int)up(r, 8);
+    Carve c(ws);
+    uint16_t *sU = c.take<uint16_t>((size_t)M * r8);
+    if (out) out->sU = sU;
+    return c.off;
+}
+
+struct GradSplit {
+    int64_t rows_per_chunk, nchunks;
+};
+GradSplit grad_split(int64_t M, int64_t C) {
+    const int64_t tiles = cdiv(C, 64);
+    int64_t s = cdiv(2 * 148, tiles);
+    s = s < 1 ? 1 : s;
+    const int64_t maxs = cdiv(M, 64) < 1 ? 1 : cdiv(M, 64);
+    s = s > maxs ? maxs : s;
+    int64_t rows = up((size_t)cdiv(M, s), 64);
+    if (rows < 64) rows = 64;
+    return {rows, M > 0 ? cdiv(M, rows) : 1};
+}
+
+struct BwdWs {
+    uint16_t *Bt, *sV, *U;
+    float *part;
+};
+size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, BwdWs *out) {
+    const int r8 = (int)up(r, 8);
+    const GradSplit ga = grad_split(M, K), gb = grad_split(M, N);
+    const size_t part = (size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N);
+    Carve c(ws);
+    uint16_t *Bt = c.take<uint16_t>((size_t)r8 * N);
+    uint16_t *sV = c.take<uint16_t>((size_t)M * r8);
+    uint16_t *U = c.take<uint16_t>((size_t)M * r8);
+    float *p = c.take<float>(part);
+    if (out) *out = BwdWs{Bt, sV, U, p};
+    return c.off;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qlora_version(void) { return "qlora-b300 0.1 (sm_103a)"; }
+
+const char *qlora_last_error(void) { return t_last_error.c_str(); }
+
+void qlora_set_wait_limit(int64_t spins) { g_wait_limit = spins > 0 ? spins : 0; }
+
+void qlora_nf4_table(float levels[16]) {
+    static const float L[16] = QLORA_NF4_LEVELS;
+    if (levels) memcpy(levels, L, sizeof L);
+}
+
+size_t qlora_nf4_codes_bytes(int64_t rows, int64_t cols) {
+    return valid_dims(rows, cols) ? (size_t)(rows * cols / 2) : 0;
+}
+size_t qlora_nf4_absmax_count(int64_t rows, int64_t cols) {
+    return valid_dims(rows, cols) ? (size_t)(rows * cols / kBlock) : 0;
+}
+size_t qlora_nf4_scale_count(int64_t rows, int64_t cols) {
+    return valid_dims(rows, cols) ? (size_t)cdiv(rows * cols / kBlock, kGroup) : 0;
+}
+size_t qlora_nf4_storage_bytes(int64_t rows, int64_t cols) {
+    if (!valid_dims(rows, cols)) return 0;
+    return up(qlora_nf4_codes_bytes(rows, cols), 16) + up(qlora_nf4_absmax_count(rows, cols), 16) +
+           up(qlora_nf4_scale_count(rows, cols) * 4, 16) + 16;
+}
+size_t qlora_nf4_quantize_workspace(int64_t rows, int64_t cols) {
+    if (!valid_dims(rows, cols)) return 0;
+    return quantize_ws(rows, cols, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, size_t ws_bytes,
+                                qlora_stream_t stream) {
+    qlora_status st = check_weight(out, false);
+    if (st) return st;
+    if (!W) return fail(QLORA_ERR_NULL, "W is NULL");
+    if (!al16(W)) return fail(QLORA_ERR_ALIGN, "W must be 16-byte aligned");
+    const int64_t rows = out->rows, cols = out->cols;
+    if (rows == 0) return ok();
+    if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
+    if (!al16(ws)) return fail(QLORA_ERR_ALIGN, "workspace must be 16-byte aligned");
+    float *absmax;
+    double *gsum, *b0, *b1;
+    const size_t need = quantize_ws(rows, cols, &absmax, &gsum, &b0, &b1, ws);
+    if (ws_bytes < need)
+        return fail(QLORA_ERR_WORKSPACE, "quantize workspace %zu < %zu bytes", ws_bytes, need);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t nb = rows * cols / kBlock, ng = cdiv(nb, kGroup);
+    {
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_nf4_encode<<<(unsigned)ng, 256, 0, s>>>(static_cast<const uint4 *>(W), nb,
+                                                 reinterpret_cast<uint32_t *>(out->codes), absmax, gsum);
+    }
+    if ((st = launch_check("k_nf4_encode"))) return st;
+    // continue the pairwise tree over the group sums, 256 per warp
+    const double *cur = gsum;
+    int64_t n = ng;
+    double *bufs[2] = {b0, b1};
+    int flip = 0;
+    while (n > 256) {
+        const int64_t chunks = cdiv(n, 256);
+        {
+            ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+            k_pairwise_reduce<<<(unsigned)cdiv(chunks, 8), 256, 0, s>>>(cur, n, bufs[flip], nullptr, nb);
+        }
+        if ((st = launch_check("k_pairwise_reduce"))) return st;
+        cur = bufs[flip];
+        flip ^= 1;
+        n = chunks;
+    }
+    {
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_pairwise_reduce<<<1, 256, 0, s>>>(cur, n, nullptr, out->absmax_mean, nb);
+    }
+    if ((st = launch_check("k_pairwise_reduce(mean)"))) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_dq_encode<<<(unsigned)cdiv(ng, 8), 256, 0, s>>>(absmax, nb, out->absmax_mean, out->absmax_q,
+                                                          out->absmax_scale);
+    }
+    if ((st = launch_check("k_dq_encode"))) return st;
+    return ok();
+}
+
+qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream) {
+    qlora_status st = check_weight(w, false);
+    if (st) return st;
+    if (!out) return fail(QLORA_ERR_NULL, "output is NULL");
+    if (!al16(out)) return fail(QLORA_ERR_ALIGN, "output must be 16-byte aligned");
+    if (w->rows == 0) return ok();
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t nhalf = w->rows * w->cols / 32;
+    {
+        ProfScope ps(QLORA_KERNEL_DEQUANT, s);
+        k_nf4_dequant<<<(unsigned)cdiv(nhalf, 256), 256, 0, s>>>(reinterpret_cast<const uint4 *>(w->codes),
+                                                                 w->absmax_q, w->absmax_scale, w->absmax_mean,
+                                                                 nhalf, static_cast<uint4 *>(out));
+    }
+    if ((st = launch_check("k_nf4_dequant"))) return st;
+    return ok();
+}
+
+size_t qlora_linear_fwd_workspace(int64_t M, const qlora_nf4_weight *w, int r) {
+    if (!w || !valid_dims(w->rows, w->cols) || M < 0 || r < 1 || r > 128) return 0;
+    return fwd_ws(M, w->rows, w->cols, r, nullptr, nullptr);
+}
+
+size_t qlora_linear_bwd_workspace(int64_t M, const qlora_nf4_weight *w, int r) {
+    if (!w || !valid_dims(w->rows, w->cols) || M < 0 || r < 1 || r > 128) return 0;
+    return bwd_ws(M, w->rows, w->cols, r, nullptr, nullptr);
+}
+
+static qlora_status check_linear_common(int64_t M, const qlora_nf4_weight *w, const void *A, const void *B, int r,
+                                        void *ws) {
+    qlora_status st = check_weight(w, true);
+    if (st) return st;
+    if (M < 0 || M >= kMaxDim) return fail(QLORA_ERR_SHAPE, "M = %lld out of range", (long long)M);
+    if (r < 1 || r > 128) return fail(QLORA_ERR_RANK, "LoRA rank r = %d outside [1, 128]", r);
+    if (!A || !B) return fail(QLORA_ERR_NULL, "LoRA A or B is NULL");
+    if (!al16(A) || !al16(B)) return fail(QLORA_ERR_ALIGN, "LoRA A and B must be 16-byte aligned");
+    if (ws && !al16(ws)) return fail(QLORA_ERR_ALIGN, "workspace must be 16-byte aligned");
+    return QLORA_OK;
+}
+
+qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *w, const void *A, const void *B,
+                              int r, float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
+                              qlora_stream_t stream) {
+    qlora_status st = check_linear_common(M, w, A, B, r, ws);
+    if (st) return st;
+    if (M > 0 && (!X || !Y)) return fail(QLORA_ERR_NULL, "X or Y is NULL");
+    if ((X && !al16(X)) || (Y && !al16(Y)) || (U_save && !al16(U_save)))
+        return fail(QLORA_ERR_ALIGN, "X, Y and U_save must be 16-byte aligned");
+    if (M == 0) return ok();
+    const int64_t N = w->rows, K = w->cols;
+    FwdWs f;
+    const size_t need = fwd_ws(M, N, K, r, ws, &f);
+    if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
+    if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "forward workspace %zu < %zu bytes", ws_bytes, need);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int r8 = (int)up(r, 8);
+    {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(static_cast<const uint16_t *>(X), M, K,
+                                                          static_cast<const uint16_t *>(A), r, scale,
+                                                          static_cast<uint16_t *>(U_save), r, f.sU, r8);
+    }
+    if ((st = launch_check("k_lora_down"))) return st;
+    dim3 grid((unsigned)cdiv(N, kSt), (unsigned)cdiv(M, kSt));
+    {
+        ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
+        k_fwd_simt<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(X), M, K, w->codes, w->absmax_q,
+                                        w->absmax_scale, w->absmax_mean, N, f.sU, r8,
+                                        static_cast<const uint16_t *>(B), r, static_cast<uint16_t *>(Y));
+    }
+    if ((st = launch_check("k_fwd_simt"))) return st;
+    return ok();
+}
+
+qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
+                              const qlora_nf4_weight *w, const void *A, const void *B, int r, float scale, void *dX,
+                              float *dA, float *dB, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    qlora_status st = check_linear_common(M, w, A, B, r, ws);
+    if (st) return st;
+    if (!dA || !dB) return fail(QLORA_ERR_NULL, "dA or dB is NULL");
+    if (M > 0 && (!dY || !X || !dX)) return fail(QLORA_ERR_NULL, "dY, X or dX is NULL");
+    if ((dY && !al16(dY)) || (X && !al16(X)) || (dX && !al16(dX)) || !al16(dA) || !al16(dB) ||
+        (U_saved && !al16(U_saved)))
+        return fail(QLORA_ERR_ALIGN, "dY, X, U_saved, dX, dA and dB must be 16-byte aligned");
+    const int64_t N = w->rows, K = w->cols;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (M == 0) {
+        if (cudaMemsetAsync(dA, 0, sizeof(float) * r * K, s) != cudaSuccess ||
+            cudaMemsetAsync(dB, 0, sizeof(float) * r * N, s) != cudaSuccess)
+            return fail(QLORA_ERR_CUDA, "memset of dA/dB failed");
+        return ok();
+    }
+    BwdWs b;
+    const size_t need = bwd_ws(M, N, K, r, ws, &b);
+    if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
+    if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "backward workspace %zu < %zu bytes", ws_bytes, need);
+    const int r8 = (int)up(r, 8);
+    const uint16_t *dY16 = static_cast<const uint16_t *>(dY), *X16 = static_cast<const uint16_t *>(X);
+    {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_transpose<<<(unsigned)cdiv(N, 256), 256, 0, s>>>(static_cast<const uint16_t *>(B), N, r, r8, b.Bt);
+    }
+    if ((st = launch_check("k_transpose"))) return st;
+    // sV = bf16(s * dY B)
+    {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, r8);
+    }
+    if ((st = launch_check("k_lora_down(V)"))) return st;
+    const uint16_t *U = static_cast<const uint16_t *>(U_saved);
+    int ldu = r;
+    if (!U) {
+        {
+            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+            k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, 1.0f,
+                                                              nullptr, 0, b.U, r8);
+        }
+        if ((st = launch_check("k_lora_down(U)"))) return st;
+        U = b.U;
+        ldu = r8;
+    }
+    dim3 grid((unsigned)cdiv(K, kSt), (unsigned)cdiv(M, kSt));
+    {
+        ProfScope ps(QLORA_KERNEL_DX_SIMT, s);
+        k_dx_simt<<<grid, 256, 0, s>>>(dY16, M, N, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, K, b.sV,
+                                       r8, static_cast<const uint16_t *>(A), r, static_cast<uint16_t *>(dX));
+    }
+    if ((st = launch_check("k_dx_simt"))) return st;
+    // dA = (sV)^T X
+    GradSplit ga = grad_split(M, K);
+    {
+        ProfScope ps(QLORA_KERNEL_GRADS, s);
+        k_lora_grad<<<dim3((unsigned)cdiv(K, 64), (unsigned)ga.nchunks), 256, 0, s>>>(b.sV, r8, X16, M, K, r,
+                                                                                   ga.rows_per_chunk, b.part);
+    }
+    if ((st = launch_check("k_lora_grad(dA)"))) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_GRADS, s);
+        k_grad_reduce<<<(unsigned)cdiv((int64_t)r * K, 256), 256, 0, s>>>(b.part, (int)ga.nchunks, r, K, 1.0f, 0,
+                                                                          dA);
+    }
+    if ((st = launch_check("k_grad_reduce(dA)"))) return st;
+    // dB = s * dY^T U
+    GradSplit gb = grad_split(M, N);
+    {
+        ProfScope ps(QLORA_KERNEL_GRADS, s);
+        k_lora_grad<<<dim3((unsigned)cdiv(N, 64), (unsigned)gb.nchunks), 256, 0, s>>>(U, ldu, dY16, M, N, r,
+                                                                                   gb.rows_per_chunk, b.part);
+    }
+    if ((st = launch_check("k_lora_grad(dB)"))) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_GRADS, s);
+        k_grad_reduce<<<(unsigned)cdiv((int64_t)r * N, 256), 256, 0, s>>>(b.part, (int)gb.nchunks, r, N, scale, 1,
+                                                                          dB);
+    }
+    if ((st = launch_check("k_grad_reduce(dB)"))) return st;
+    return ok();
+}
+
+void qlora_profile_start(void) {
+    for (auto &p : g_prof) {
+        cudaEventDestroy(p.a);
+        cudaEventDestroy(p.b);
+    }
+    g_prof.clear();
+    for (int k = 0; k < QLORA_KERNEL_KINDS; ++k) g_prof_count[k] = 0;
+    g_prof_on = true;
+}
+
+int qlora_profile_stop(double ms_per_kind[QLORA_KERNEL_KINDS], int launches_per_kind[QLORA_KERNEL_KINDS]) {
+    g_prof_on = false;
+    int total = 0, bad = 0;
+    for (int k = 0; k < QLORA_KERNEL_KINDS; ++k) {
+        if (ms_per_kind) ms_per_kind[k] = 0.0;
+        if (launches_per_kind) launches_per_kind[k] = g_prof_count[k];
+        total += g_prof_count[k];
+    }
+    for (auto &p : g_prof) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess) bad = 1;
+        if (ms_per_kind) ms_per_kind[p.kind] += ms;
+        cudaEventDestroy(p.a);
+        cudaEventDestroy(p.b);
+    }
+    g_prof.clear();
+    return bad ? -1 : total;
+}
+
+qlora_status qlora_check_device_status(qlora_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof word);
+    if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+    if (word) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero);
+        return fail(QLORA_ERR_TIMEOUT, "bounded wait ran out: kernel %u, site %u", word >> 16, word & 0xFFFFu);
+    }
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,235 @@
+"""Thin Python binding of the C ABI in include/qlora.h (ctypes).
+
+The functions carry the C names and only marshal arguments: tensors become
+device pointers, the stream defaults to torch's current stream, a non-zero
+status raises QloraError with the library's message. Every step of the
+computation runs in the library's CUDA kernels. PyTorch supplies device
+memory and streams.
+
+The library must be built first (``python -m bit_quantized_lora_double_b300._build``
+or ``__graft_entry__.build()``); importing this module without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqlora_b300.so")
+_lib = None
+
+STATUS = {0: "QLORA_OK", 1: "QLORA_ERR_NULL", 2: "QLORA_ERR_SHAPE", 3: "QLORA_ERR_ALIGN",
+          4: "QLORA_ERR_WORKSPACE", 5: "QLORA_ERR_RANK", 6: "QLORA_ERR_CUDA", 7: "QLORA_ERR_TIMEOUT",
+          8: "QLORA_ERR_UNSUPPORTED"}
+
+EXPORTS = [
+    "qlora_nf4_codes_bytes", "qlora_nf4_absmax_count", "qlora_nf4_scale_count", "qlora_nf4_storage_bytes",
+    "qlora_nf4_quantize_workspace", "qlora_nf4_table", "qlora_nf4_quantize", "qlora_nf4_dequantize",
+    "qlora_linear_fwd_workspace", "qlora_linear_bwd_workspace", "qlora_linear_fwd", "qlora_linear_bwd",
+    "qlora_last_error", "qlora_check_device_status", "qlora_set_wait_limit", "qlora_version",
+    "qlora_profile_start", "qlora_profile_stop",
+]
+
+KERNEL_KINDS = ["quantize", "dequant", "lora_pre", "fwd_gemm", "fwd_simt", "dx_gemm", "dx_simt", "grads"]
+
+
+class QloraError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Nf4WeightDesc(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("codes", ctypes.c_void_p),
+                ("absmax_q", ctypes.c_void_p), ("absmax_scale", ctypes.c_void_p),
+                ("absmax_mean", ctypes.c_void_p)]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {_LIB_PATH} is missing "
+                               "(run python -m bit_quantized_lora_double_b300._build)")
+        L = ctypes.CDLL(_LIB_PATH)
+        i64, sz, vp, i32, f32 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        W = ctypes.POINTER(Nf4WeightDesc)
+        for n in ("qlora_nf4_codes_bytes", "qlora_nf4_absmax_count", "qlora_nf4_scale_count",
+                  "qlora_nf4_storage_bytes", "qlora_nf4_quantize_workspace"):
+            getattr(L, n).restype = sz
+            getattr(L, n).argtypes = [i64, i64]
+        L.qlora_nf4_table.restype = None
+        L.qlora_nf4_table.argtypes = [vp]
+        L.qlora_nf4_quantize.restype = i32
+        L.qlora_nf4_quantize.argtypes = [vp, W, vp, sz, vp]
+        L.qlora_nf4_dequantize.restype = i32
+        L.qlora_nf4_dequantize.argtypes = [W, vp, vp]
+        L.qlora_linear_fwd_workspace.restype = sz
+        L.qlora_linear_fwd_workspace.argtypes = [i64, W, i32]
+        L.qlora_linear_bwd_workspace.restype = sz
+        L.qlora_linear_bwd_workspace.argtypes = [i64, W, i32]
+        L.qlora_linear_fwd.restype = i32
+        L.qlora_linear_fwd.argtypes = [vp, i64, W, vp, vp, i32, f32, vp, vp, vp, sz, vp]
+        L.qlora_linear_bwd.restype = i32
+        L.qlora_linear_bwd.argtypes = [vp, vp, vp, i64, W, vp, vp, i32, f32, vp, vp, vp, vp, sz, vp]
+        L.qlora_last_error.restype = ctypes.c_char_p
+        L.qlora_last_error.argtypes = []
+        L.qlora_check_device_status.restype = i32
+        L.qlora_check_device_status.argtypes = [vp]
+        L.qlora_set_wait_limit.restype = None
+        L.qlora_set_wait_limit.argtypes = [i64]
+        L.qlora_version.restype = ctypes.c_char_p
+        L.qlora_version.argtypes = []
+        L.qlora_profile_start.restype = None
+        L.qlora_profile_start.argtypes = []
+        L.qlora_profile_stop.restype = i32
+        L.qlora_profile_stop.argtypes = [vp, vp]
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise QloraError(status, lib().qlora_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    h = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(h)
+
+
+@dataclass
+class Nf4Weight:
+    """A quantized weight: device arrays (torch-owned) plus the C descriptor."""
+    rows: int
+    cols: int
+    codes: torch.Tensor
+    absmax_q: torch.Tensor
+    absmax_scale: torch.Tensor
+    absmax_mean: torch.Tensor
+
+    @property
+    def desc(self) -> Nf4WeightDesc:
+        return Nf4WeightDesc(self.rows, self.cols, self.codes.data_ptr(), self.absmax_q.data_ptr(),
+                             self.absmax_scale.data_ptr(), self.absmax_mean.data_ptr())
+
+
+# ---- sizes -----------------------------------------------------------------
+
+def qlora_nf4_codes_bytes(rows, cols):
+    return lib().qlora_nf4_codes_bytes(rows, cols)
+
+
+def qlora_nf4_absmax_count(rows, cols):
+    return lib().qlora_nf4_absmax_count(rows, cols)
+
+
+def qlora_nf4_scale_count(rows, cols):
+    return lib().qlora_nf4_scale_count(rows, cols)
+
+
+def qlora_nf4_storage_bytes(rows, cols):
+    return lib().qlora_nf4_storage_bytes(rows, cols)
+
+
+def qlora_nf4_quantize_workspace(rows, cols):
+    return lib().qlora_nf4_quantize_workspace(rows, cols)
+
+
+def qlora_nf4_table():
+    import numpy as np
+    out = np.zeros(16, np.float32)
+    lib().qlora_nf4_table(out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def qlora_linear_fwd_workspace(M, w: Nf4Weight, r):
+    d = w.desc
+    return lib().qlora_linear_fwd_workspace(M, ctypes.byref(d), r)
+
+
+def qlora_linear_bwd_workspace(M, w: Nf4Weight, r):
+    d = w.desc
+    return lib().qlora_linear_bwd_workspace(M, ctypes.byref(d), r)
+
+
+def alloc_nf4_weight(rows: int, cols: int, device="cuda") -> Nf4Weight:
+    """Allocates the device arrays of a quantized weight (torch tensors)."""
+    nb = qlora_nf4_absmax_count(rows, cols)
+    if qlora_nf4_codes_bytes(rows, cols) == 0 and rows != 0:
+        raise QloraError(2, f"invalid weight shape [{rows}, {cols}]")
+    return Nf4Weight(rows, cols,
+                     torch.empty(rows * cols // 2, dtype=torch.uint8, device=device),
+                     torch.empty(nb, dtype=torch.int8, device=device),
+                     torch.empty(qlora_nf4_scale_count(rows, cols), dtype=torch.float32, device=device),
+                     torch.empty(4, dtype=torch.float32, device=device))
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+# ---- calls -----------------------------------------------------------------
+
+def qlora_nf4_quantize(W: torch.Tensor, out: Nf4Weight, ws: torch.Tensor, stream=None):
+    d = out.desc
+    _check(lib().qlora_nf4_quantize(_ptr(W), ctypes.byref(d), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream)))
+
+
+def qlora_nf4_dequantize(w: Nf4Weight, out: torch.Tensor, stream=None):
+    d = w.desc
+    _check(lib().qlora_nf4_dequantize(ctypes.byref(d), _ptr(out), _stream(stream)))
+
+
+def qlora_linear_fwd(X, M, w: Nf4Weight, A, B, r, scale, Y, U_save, ws, stream=None):
+    d = w.desc
+    _check(lib().qlora_linear_fwd(_ptr(X), M, ctypes.byref(d), _ptr(A), _ptr(B), r, float(scale), _ptr(Y),
+                                  _ptr(U_save), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                  _stream(stream)))
+
+
+def qlora_linear_bwd(dY, X, U_saved, M, w: Nf4Weight, A, B, r, scale, dX, dA, dB, ws, stream=None):
+    d = w.desc
+    _check(lib().qlora_linear_bwd(_ptr(dY), _ptr(X), _ptr(U_saved), M, ctypes.byref(d), _ptr(A), _ptr(B), r,
+                                  float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qlora_last_error() -> str:
+    return lib().qlora_last_error().decode()
+
+
+def qlora_check_device_status(stream=None):
+    _check(lib().qlora_check_device_status(_stream(stream)))
+
+
+def qlora_set_wait_limit(spins: int):
+    lib().qlora_set_wait_limit(int(spins))
+
+
+def qlora_version() -> str:
+    return lib().qlora_version().decode()
+
+
+def qlora_profile_start():
+    lib().qlora_profile_start()
+
+
+def qlora_profile_stop():
+    """Returns ({kind: summed ms}, {kind: launches}, total launches)."""
+    import numpy as np
+    ms = np.zeros(len(KERNEL_KINDS), np.float64)
+    n = np.zeros(len(KERNEL_KINDS), np.int32)
+    total = lib().qlora_profile_stop(ms.ctypes.data_as(ctypes.c_void_p), n.ctypes.data_as(ctypes.c_void_p))
+    if total < 0:
+        raise QloraError(6, "profiling events failed")
+    return dict(zip(KERNEL_KINDS, ms.tolist())), dict(zip(KERNEL_KINDS, n.tolist())), int(total)

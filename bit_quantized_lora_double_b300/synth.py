@@ -4,9 +4,10 @@ This module holds no arithmetic of the method: it only draws Gaussian numbers
 and rounds them to bf16 bit patterns, so the GPU path and the CPU oracle can be
 fed the same bytes.
 
-Recipe: numpy ``Generator(PCG64(seed))`` draws float64 N(0, std^2); the values
-are rounded to float32 (numpy, round to nearest) and then to bf16 with
-round-to-nearest-even on the bit pattern. Seeds are
+Recipe: numpy ``Generator(PCG64(seed))`` draws float32 standard normals
+(``standard_normal(dtype=float32)``), multiplies them by the float32 std
+(round to nearest) and rounds the products to bf16 with round-to-nearest-even
+on the bit pattern. Seeds are
 ``20261202 + 100 * workload + tensor`` with tensor X=0, W=1, A=2, B=3, dY=4;
 projection p of a multi-projection workload adds ``10 * p``.
 """
@@ -24,9 +25,13 @@ def seed_for(workload: int, tensor: str, projection: int = 0) -> int:
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns (uint16), round to nearest even (finite inputs)."""
-    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
-    u = u + 0x7FFF + ((u >> 16) & 1)
-    return (u >> 16).astype(np.uint16)
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    # finite inputs stay below 0xFF800000 + 0x8000, so uint32 does not wrap
+    r = (u >> 16) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
@@ -40,7 +45,7 @@ def gaussian_bf16(shape, std: float, seed: int, chunk: int = 1 << 24) -> np.ndar
     out = np.empty(n, np.uint16)
     for i in range(0, n, chunk):
         m = min(chunk, n - i)
-        out[i:i + m] = f32_to_bf16_bits((rng.standard_normal(m) * std).astype(np.float32))
+        out[i:i + m] = f32_to_bf16_bits(rng.standard_normal(m, dtype=np.float32) * np.float32(std))
     return out.reshape(shape)
 
 

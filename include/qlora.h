@@ -1,0 +1,219 @@
+/*
+ * qlora.h -- C ABI of the NF4 + double-quantized LoRA linear layer on B300
+ * (sm_103a).
+ *
+ * What the calls compute (sources are web pages on QLoRA, cited by title and
+ * section):
+ *  - The frozen base weight W [N out, K in] is stored as 4-bit NormalFloat
+ *    codes: 16 levels taken from the quantiles of a standard normal, each bin
+ *    holding an equal share of the distribution, with an exact zero
+ *    (inquiringlines.com "Can we finetune huge language models on a single
+ *    GPU?", mechanism paragraph; ashishsrivastav.com "QLoRA: Fine-Tuning a 70B
+ *    on One GPU", section "NF4 Quantization: Beyond Standard INT4"). Each weight
+ *    maps to the closest level of its block, once, before training (same
+ *    section).
+ *  - The per-block scaling constants are themselves quantized to INT8 ("double
+ *    quantization"; same page, section "Double Quantization: Squeezing the
+ *    Constants"; inquiringlines.com, same paragraph: about 0.37 bit per
+ *    parameter saved).
+ *  - Dequantization to the bf16 compute type happens on the fly inside the
+ *    forward and backward passes (ashishsrivastav.com, same section;
+ *    serverroom.net "Fine-tuning an LLM on a GPU: memory requirements for LoRA
+ *    and QLoRA", section "What LoRA and QLoRA change in memory": compute dtype
+ *    bf16).
+ *  - Gradients flow through the frozen 4-bit weights into low-rank adapters A
+ *    [r, K] and B [N, r]; only the adapters get gradients
+ *    (inquiringlines.com, same paragraph; xingyuzhitong.com "Fine-Tuning Memory
+ *    Requirements: Full Training vs LoRA vs QLoRA", sections "LoRA: freeze the
+ *    base, train small adapters" and "QLoRA: quantize the frozen base to 4
+ *    bits"). Adapter dropout is 0 and there is no bias (serverroom.net, adapter
+ *    setup listing).
+ *
+ * Fixed format (readings where the pages are silent):
+ *  - blocks of 64 consecutive weights in row-major order (cols % 64 == 0), so
+ *    a block never crosses a row;
+ *  - codes: byte i holds element 2i in its high nibble, element 2i+1 in its
+ *    low nibble;
+ *  - absmax_q: one int8 per block, symmetric, in [-127, 127];
+ *  - absmax_scale: one fp32 per group of 256 consecutive blocks (the last
+ *    group may be partial);
+ *  - absmax_mean: one fp32 for the whole tensor, subtracted before the int8
+ *    step;
+ *  - reconstructed absmax a' = fp32(q) * scale + mean (two rounded fp32
+ *    operations, no fused multiply-add); dequantized weight
+ *    w' = bf16_rne(fp32(L[code] * a')).
+ *  - LoRA: Y = X W'^T + s (X A^T) B^T with s = alpha / r passed as `scale`.
+ *
+ * Conventions for every call:
+ *  - All tensors are row-major and contiguous; bf16 tensors are passed as
+ *    void pointers to 2-byte elements.
+ *  - Pointers are DEVICE pointers unless a comment says otherwise. The caller
+ *    owns every buffer; the library never allocates, frees or synchronizes,
+ *    and enqueues all work on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).
+ *  - Every argument is validated on the host before anything is launched. On
+ *    an error, nothing is launched, outputs are untouched, the status is
+ *    returned and qlora_last_error() describes it.
+ *  - A launch failure returns QLORA_ERR_CUDA. Faults inside kernels surface at
+ *    the caller's next synchronization. Pipelined kernels bound every wait;
+ *    a wait that runs out sets a device error word, which
+ *    qlora_check_device_status() reports as QLORA_ERR_TIMEOUT.
+ *  - The calls keep no state between calls and may run concurrently on
+ *    different streams when their buffers do not overlap.
+ *  - Alignment: every device pointer must be 16-byte aligned.
+ */
+#ifndef QLORA_B300_H
+#define QLORA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qlora_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    QLORA_OK = 0,
+    QLORA_ERR_NULL = 1,        /* a required pointer is NULL */
+    QLORA_ERR_SHAPE = 2,       /* a size is out of range (e.g. cols % 64 != 0, M < 0) */
+    QLORA_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
+    QLORA_ERR_WORKSPACE = 4,   /* workspace smaller than the size query returns */
+    QLORA_ERR_RANK = 5,        /* LoRA rank outside [1, 128] */
+    QLORA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+    QLORA_ERR_TIMEOUT = 7,     /* a bounded wait inside a kernel ran out */
+    QLORA_ERR_UNSUPPORTED = 8  /* device is not sm_103 / needed driver entry point missing */
+} qlora_status;
+
+/* A quantized weight: all pointers are device pointers owned by the caller. */
+typedef struct {
+    int64_t rows;           /* N: output features */
+    int64_t cols;           /* K: input features, cols % 64 == 0 */
+    uint8_t *codes;         /* rows*cols/2 bytes, layout above */
+    int8_t *absmax_q;       /* nb = rows*cols/64 int8 codes */
+    float *absmax_scale;    /* ng = ceil(nb/256) fp32 scales */
+    float *absmax_mean;     /* 1 fp32 */
+} qlora_nf4_weight;
+
+/* ---- sizes (host-only, no GPU needed) --------------------------------- */
+
+/* Bytes of packed codes: rows*cols/2. Returns 0 for invalid sizes. */
+size_t qlora_nf4_codes_bytes(int64_t rows, int64_t cols);
+/* Number of blocks (int8 absmax codes): rows*cols/64. */
+size_t qlora_nf4_absmax_count(int64_t rows, int64_t cols);
+/* Number of fp32 second-level scales: ceil(blocks / 256). */
+size_t qlora_nf4_scale_count(int64_t rows, int64_t cols);
+/* Total bytes of one quantized weight (codes + int8 codes + scales + mean),
+ * each array padded to 16 bytes as the library requires. */
+size_t qlora_nf4_storage_bytes(int64_t rows, int64_t cols);
+/* Workspace bytes qlora_nf4_quantize needs. */
+size_t qlora_nf4_quantize_workspace(int64_t rows, int64_t cols);
+
+/* Host copy of the 16 fp32 NF4 levels the kernels use (ascending; code 7 is
+ * the exact zero). */
+void qlora_nf4_table(float levels[16]);
+
+/* ---- codec ------------------------------------------------------------- */
+
+/* Quantizes a bf16 weight W [rows, cols] (device) into `out`, whose rows/cols
+ * must be set and whose arrays must be allocated (sizes above). Encodes each
+ * block of 64 with its exact absmax (nearest level, ties to the lower code),
+ * then double-quantizes the absmax: mean = fp32(S / nb) with S the pairwise
+ * (balanced binary tree, zero-padded to a power of two, leaves in block
+ * order) fp64 sum of the absmax values; per group g of 256 blocks,
+ * c = fp32(a - mean), scale_g = fp32(max|c| / 127), q = clamp(rint(fp32(c /
+ * scale_g)), -127, 127) (q = 0 when scale_g == 0). Inputs must be finite.
+ * `ws` is a device workspace of at least qlora_nf4_quantize_workspace bytes.
+ * Sources: ashishsrivastav.com, sections "NF4 Quantization" and "Double
+ * Quantization"; inquiringlines.com, mechanism paragraph. */
+qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, size_t ws_bytes,
+                                qlora_stream_t stream);
+
+/* Writes the dequantized bf16 weight W' [rows, cols] (device) to `out`:
+ * w' = bf16_rne(fp32(L[code] * a')) with a' = fp32(q)*scale + mean.
+ * Source: ashishsrivastav.com, section "Double Quantization" (dequantize on
+ * the fly to the compute type). */
+qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream);
+
+/* ---- linear layer with LoRA ------------------------------------------- */
+
+/* Workspace bytes for qlora_linear_fwd / qlora_linear_bwd at these sizes. */
+size_t qlora_linear_fwd_workspace(int64_t M, const qlora_nf4_weight *w, int r);
+size_t qlora_linear_bwd_workspace(int64_t M, const qlora_nf4_weight *w, int r);
+
+/* Forward:  Y = X W'^T + scale * (X A^T) B^T.
+ *   X      bf16 [M, K]        input activations (K = w->cols)
+ *   w      quantized W [N, K] (N = w->rows)
+ *   A      bf16 [r, K]        LoRA down-projection
+ *   B      bf16 [N, r]        LoRA up-projection
+ *   scale  LoRA scale s (alpha / r)
+ *   Y      bf16 [M, N]        output (overwritten)
+ *   U_save bf16 [M, r] or NULL: receives U = X A^T (rounded to bf16) for the
+ *          backward pass
+ *   ws     device workspace of qlora_linear_fwd_workspace bytes
+ * M may be 0 (nothing is launched). 1 <= r <= 128.
+ * Accumulation is fp32 over bf16 operands; the LoRA term enters as extra
+ * contraction steps over (s*U rounded to bf16) and B. */
+qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *w, const void *A,
+                              const void *B, int r, float scale, void *Y, void *U_save, void *ws,
+                              size_t ws_bytes, qlora_stream_t stream);
+
+/* Backward (no gradient for the frozen W):
+ *   V  = dY B                                    [M, r]
+ *   dX = dY W' + scale * V A                     bf16 [M, K]  (overwritten)
+ *   dB = scale * dY^T U                          fp32 [N, r]  (overwritten)
+ *   dA = scale * V^T X                           fp32 [r, K]  (overwritten)
+ *   dY bf16 [M, N]; X bf16 [M, K]; U_saved bf16 [M, r] from the forward, or
+ *   NULL to recompute U = X A^T. dA and dB are complete sums over the M rows
+ *   given (a data-parallel caller all-reduces them across replicas). */
+qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
+                              const qlora_nf4_weight *w, const void *A, const void *B, int r,
+                              float scale, void *dX, float *dA, float *dB, void *ws,
+                              size_t ws_bytes, qlora_stream_t stream);
+
+/* ---- diagnostics ------------------------------------------------------- */
+
+/* Message for the last error on the calling thread ("" if none). */
+const char *qlora_last_error(void);
+
+/* Synchronizes `stream`, then reads and clears the device error word set by
+ * bounded waits that ran out. Returns QLORA_OK, QLORA_ERR_TIMEOUT (message
+ * names the kernel and wait) or QLORA_ERR_CUDA. */
+qlora_status qlora_check_device_status(qlora_stream_t stream);
+
+/* Test hook: sets the iteration limit of the bounded waits in pipelined
+ * kernels (0 restores the default). A limit of 1 makes any wait that is not
+ * already satisfied run out at once. Host-side setting, applies to later
+ * launches on all streams. */
+void qlora_set_wait_limit(int64_t spins);
+
+/* Profiling of the library's own kernels, for benchmarks. Between
+ * qlora_profile_start() and qlora_profile_stop(), every kernel launch is
+ * counted by kind and bracketed by a pair of CUDA events recorded on its
+ * launch stream (the library creates and destroys these events; nothing else
+ * changes). qlora_profile_stop() waits for the recorded events and fills, per
+ * kind, the summed device time in ms and the number of launches; it returns
+ * the total number of launches, or -1 on a CUDA error. Not thread-safe: one
+ * profiling session at a time. */
+enum {
+    QLORA_KERNEL_QUANTIZE = 0,   /* encode + tree sum + double quantization */
+    QLORA_KERNEL_DEQUANT = 1,    /* standalone dequantize */
+    QLORA_KERNEL_LORA_PRE = 2,   /* U = X A^T, V = dY B, B^T */
+    QLORA_KERNEL_FWD_GEMM = 3,   /* fused dequant + tcgen05 forward GEMM */
+    QLORA_KERNEL_FWD_SIMT = 4,   /* small-M / CUDA-core forward */
+    QLORA_KERNEL_DX_GEMM = 5,    /* fused dequant + tcgen05 dX GEMM */
+    QLORA_KERNEL_DX_SIMT = 6,    /* small-M / CUDA-core dX */
+    QLORA_KERNEL_GRADS = 7,      /* dA, dB reductions */
+    QLORA_KERNEL_KINDS = 8
+};
+void qlora_profile_start(void);
+int qlora_profile_stop(double ms_per_kind[QLORA_KERNEL_KINDS], int launches_per_kind[QLORA_KERNEL_KINDS]);
+
+/* Library version string. */
+const char *qlora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLORA_B300_H */
