@@ -32,7 +32,7 @@ from bit_quantized_lora_double_b300 import synth  # noqa: E402
 
 WORKLOAD = 1          # Llama-3.1-8B-shaped layer, M = 2048, r = 16
 CODEC_WORKLOAD = 2    # 14336 x 4096 codec
-CPU_SAMPLE_TOKENS = 16
+CPU_SAMPLE_TOKENS = 96
 METRIC = "QLoRA linear fwd+bwd TFLOP/s and % bf16 peak; NF4 dequant GB/s and % HBM"
 
 

@@ -91,6 +91,22 @@ __global__ void k_transpose(const uint16_t *__restrict__ in, int64_t N, int r, i
     for (int j = 0; j < r8; ++j) out[(int64_t)j * N + n] = j < r ? in[n * r + j] : (uint16_t)0;
 }
 
+// out[n, j] = in[n, j] for j < r, 0 for r <= j < rp (zero-padded copy, rows of rp).
+__global__ void k_pad_cols(const uint16_t *__restrict__ in, int64_t N, int r, int rp, uint16_t *__restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= N * rp) return;
+    const int64_t n = i / rp;
+    const int j = (int)(i % rp);
+    out[i] = j < r ? in[n * r + j] : (uint16_t)0;
+}
+
+// out [rp, K] = in [r, K] followed by rp - r zero rows.
+__global__ void k_pad_rows(const uint16_t *__restrict__ in, int r, int rp, int64_t K, uint16_t *__restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)rp * K) return;
+    out[i] = i < (int64_t)r * K ? in[i] : (uint16_t)0;
+}
+
 // Partial sums over one chunk of rows: part[chunk][j][c] = sum_{m in chunk}
 // P[m, j] Q[m, c] for c in a 64-column tile, j < r. P is bf16 [M, ldp],
 // Q is bf16 [M, C]. Thread layout: 64 columns x 4 j-groups.

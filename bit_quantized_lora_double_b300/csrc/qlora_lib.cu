@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "codec.cuh"
 #include "lora_simt.cuh"
+#include "gemm_tc.cuh"
 
 using namespace qlora;
 
@@ -125,16 +126,20 @@ size_t quantize_ws(int64_t rows, int64_t cols, float **absmax, double **gsum, do
 }
 
 // ---- linear workspaces
+// The LoRA operands of the tensor-core path are zero-padded to rp = 64 *
+// ceil(r / 64) columns so every TMA box lies inside its tensor.
+inline int lora_pad(int r) { return (int)up((size_t)r, 64); }
+
 struct FwdWs {
-    uint16_t *sU;
+    uint16_t *sU, *Bp;
 };
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
-    (void)N;
     (void)K;
-    const int r8 = (int)up(r, 8);
+    const int rp = lora_pad(r);
     Carve c(ws);
-    uint16_t *sU = c.take<uint16_t>((size_t)M * r8);
-    if (out) out->sU = sU;
+    uint16_t *sU = c.take<uint16_t>((size_t)M * rp);
+    uint16_t *Bp = c.take<uint16_t>((size_t)N * rp);
+    if (out) *out = FwdWs{sU, Bp};
     return c.off;
 }
 
@@ -153,21 +158,86 @@ GradSplit grad_split(int64_t M, int64_t C) {
 }
 
 struct BwdWs {
-    uint16_t *Bt, *sV, *U;
+    uint16_t *Bt, *sV, *U, *Ap;
     float *part;
 };
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, BwdWs *out) {
-    const int r8 = (int)up(r, 8);
+    const int r8 = (int)up(r, 8), rp = lora_pad(r);
     const GradSplit ga = grad_split(M, K), gb = grad_split(M, N);
     const size_t part = (size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N);
     Carve c(ws);
     uint16_t *Bt = c.take<uint16_t>((size_t)r8 * N);
-    uint16_t *sV = c.take<uint16_t>((size_t)M * r8);
+    uint16_t *sV = c.take<uint16_t>((size_t)M * rp);
     uint16_t *U = c.take<uint16_t>((size_t)M * r8);
+    uint16_t *Ap = c.take<uint16_t>((size_t)rp * K);
     float *p = c.take<float>(part);
-    if (out) *out = BwdWs{Bt, sV, U, p};
+    if (out) *out = BwdWs{Bt, sV, U, Ap, p};
     return c.off;
 }
+
+// ---- tensor maps (driver entry point fetched through the runtime) ----------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// 2-D tiled map over a row-major [outer, inner] array (inner contiguous).
+qlora_status make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
+                      const char *what) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(QLORA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QLORA_ERR_CUDA, "tensor map for %s: error %d", what, (int)r);
+    return QLORA_OK;
+}
+
+// Device check for the tcgen05 kernels (compiled for sm_103a only).
+qlora_status tc_device_ok() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return fail(QLORA_ERR_CUDA, "cannot query the current device");
+    if (major != 10 || minor != 3)
+        return fail(QLORA_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a", major, minor);
+    return QLORA_OK;
+}
+
+template <int MODE>
+qlora_status tc_setup() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(k_gemm_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM_BYTES);
+    });
+    if (err != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(err));
+    return QLORA_OK;
+}
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per bounded wait
+uint64_t wait_ns() { return g_wait_limit > 0 ? (uint64_t)g_wait_limit * 1000ull : kDefaultWaitNs; }
+
+// Tokens at or above which the tensor-core path runs.
+constexpr int64_t kTcMinM = 64;
 
 }  // namespace
 
@@ -177,7 +247,7 @@ const char *qlora_version(void) { return "qlora-b300 0.1 (sm_103a)"; }
 
 const char *qlora_last_error(void) { return t_last_error.c_str(); }
 
-void qlora_set_wait_limit(int64_t spins) { g_wait_limit = spins > 0 ? spins : 0; }
+void qlora_set_wait_limit(int64_t microseconds) { g_wait_limit = microseconds > 0 ? microseconds : 0; }
 
 void qlora_nf4_table(float levels[16]) {
     static const float L[16] = QLORA_NF4_LEVELS;
@@ -311,22 +381,62 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
     if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "forward workspace %zu < %zu bytes", ws_bytes, need);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int r8 = (int)up(r, 8);
+    const int rp = lora_pad(r);
+    const uint16_t *X16 = static_cast<const uint16_t *>(X);
     {
         ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(static_cast<const uint16_t *>(X), M, K,
-                                                          static_cast<const uint16_t *>(A), r, scale,
-                                                          static_cast<uint16_t *>(U_save), r, f.sU, r8);
+        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
+                                                          static_cast<uint16_t *>(U_save), r, f.sU, rp);
     }
     if ((st = launch_check("k_lora_down"))) return st;
-    dim3 grid((unsigned)cdiv(N, kSt), (unsigned)cdiv(M, kSt));
-    {
-        ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
-        k_fwd_simt<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(X), M, K, w->codes, w->absmax_q,
-                                        w->absmax_scale, w->absmax_mean, N, f.sU, r8,
-                                        static_cast<const uint16_t *>(B), r, static_cast<uint16_t *>(Y));
+    if (M < kTcMinM) {
+        dim3 grid((unsigned)cdiv(N, kSt), (unsigned)cdiv(M, kSt));
+        {
+            ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
+            k_fwd_simt<<<grid, 256, 0, s>>>(X16, M, K, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, N,
+                                            f.sU, rp, static_cast<const uint16_t *>(B), r,
+                                            static_cast<uint16_t *>(Y));
+        }
+        if ((st = launch_check("k_fwd_simt"))) return st;
+        return ok();
     }
-    if ((st = launch_check("k_fwd_simt"))) return st;
+    if ((st = tc_device_ok()) || (st = tc_setup<kFwd>())) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_pad_cols<<<(unsigned)cdiv(N * rp, 256), 256, 0, s>>>(static_cast<const uint16_t *>(B), N, r, rp, f.Bp);
+    }
+    if ((st = launch_check("k_pad_cols(B)"))) return st;
+    CUtensorMap tmX, tmC, tmU, tmB;
+    if ((st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
+        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 32, 256,
+                       CU_TENSOR_MAP_SWIZZLE_32B, "codes")) ||
+        (st = make_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rp, M, rp * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "sU")) ||
+        (st = make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.Bp, rp, N, rp * 2, 64, 256,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+        return st;
+    TcParams prm{};
+    prm.M = M;
+    prm.Nd = N;
+    prm.w_rows = N;
+    prm.w_cols = K;
+    prm.nk_main = K / TcCfg::BK;
+    prm.lora_steps = rp / 64;
+    prm.r = r;
+    prm.q = w->absmax_q;
+    prm.s2 = w->absmax_scale;
+    prm.mean = w->absmax_mean;
+    prm.out = static_cast<uint16_t *>(Y);
+    prm.ldo = N;
+    prm.wait_ns = wait_ns();
+    prm.kernel_id = 1;
+    dim3 grid((unsigned)cdiv(N, TcCfg::BN), (unsigned)cdiv(M, TcCfg::BM));
+    {
+        ProfScope ps(QLORA_KERNEL_FWD_GEMM, s);
+        k_gemm_tc<kFwd><<<grid, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(tmX, tmC, tmU, tmB, prm);
+    }
+    if ((st = launch_check("k_gemm_tc<fwd>"))) return st;
     return ok();
 }
 
@@ -352,17 +462,17 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     const size_t need = bwd_ws(M, N, K, r, ws, &b);
     if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
     if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "backward workspace %zu < %zu bytes", ws_bytes, need);
-    const int r8 = (int)up(r, 8);
+    const int r8 = (int)up(r, 8), rp = lora_pad(r);
     const uint16_t *dY16 = static_cast<const uint16_t *>(dY), *X16 = static_cast<const uint16_t *>(X);
     {
         ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
         k_transpose<<<(unsigned)cdiv(N, 256), 256, 0, s>>>(static_cast<const uint16_t *>(B), N, r, r8, b.Bt);
     }
     if ((st = launch_check("k_transpose"))) return st;
-    // sV = bf16(s * dY B)
+    // sV = bf16(s * dY B), rp columns (zero beyond r)
     {
         ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, r8);
+        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, rp);
     }
     if ((st = launch_check("k_lora_down(V)"))) return st;
     const uint16_t *U = static_cast<const uint16_t *>(U_saved);
@@ -377,18 +487,61 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
         U = b.U;
         ldu = r8;
     }
-    dim3 grid((unsigned)cdiv(K, kSt), (unsigned)cdiv(M, kSt));
-    {
-        ProfScope ps(QLORA_KERNEL_DX_SIMT, s);
-        k_dx_simt<<<grid, 256, 0, s>>>(dY16, M, N, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, K, b.sV,
-                                       r8, static_cast<const uint16_t *>(A), r, static_cast<uint16_t *>(dX));
+    const bool tc = M >= kTcMinM && (N % 8) == 0;
+    if (!tc) {
+        dim3 grid((unsigned)cdiv(K, kSt), (unsigned)cdiv(M, kSt));
+        {
+            ProfScope ps(QLORA_KERNEL_DX_SIMT, s);
+            k_dx_simt<<<grid, 256, 0, s>>>(dY16, M, N, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, K,
+                                           b.sV, rp, static_cast<const uint16_t *>(A), r,
+                                           static_cast<uint16_t *>(dX));
+        }
+        if ((st = launch_check("k_dx_simt"))) return st;
+    } else {
+        if ((st = tc_device_ok()) || (st = tc_setup<kDx>())) return st;
+        {
+            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+            // A [r, K] -> Ap [rp, K] with zero rows r..rp-1 (row-padded copy)
+            k_pad_rows<<<(unsigned)cdiv(rp * K, 256), 256, 0, s>>>(static_cast<const uint16_t *>(A), r, rp, K, b.Ap);
+        }
+        if ((st = launch_check("k_pad_rows(A)"))) return st;
+        CUtensorMap tmD, tmC, tmV, tmA;
+        if ((st = make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, N, M, N * 2, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "dY")) ||
+            (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "codes")) ||
+            (st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rp, M, rp * 2, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "sV")) ||
+            (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.Ap, K, rp, K * 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+            return st;
+        TcParams prm{};
+        prm.M = M;
+        prm.Nd = K;
+        prm.w_rows = N;
+        prm.w_cols = K;
+        prm.nk_main = cdiv(N, TcCfg::BK);
+        prm.lora_steps = rp / 64;
+        prm.r = r;
+        prm.q = w->absmax_q;
+        prm.s2 = w->absmax_scale;
+        prm.mean = w->absmax_mean;
+        prm.out = static_cast<uint16_t *>(dX);
+        prm.ldo = K;
+        prm.wait_ns = wait_ns();
+        prm.kernel_id = 2;
+        dim3 grid((unsigned)cdiv(K, TcCfg::BN), (unsigned)cdiv(M, TcCfg::BM));
+        {
+            ProfScope ps(QLORA_KERNEL_DX_GEMM, s);
+            k_gemm_tc<kDx><<<grid, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(tmD, tmC, tmV, tmA, prm);
+        }
+        if ((st = launch_check("k_gemm_tc<dx>"))) return st;
     }
-    if ((st = launch_check("k_dx_simt"))) return st;
     // dA = (sV)^T X
     GradSplit ga = grad_split(M, K);
     {
         ProfScope ps(QLORA_KERNEL_GRADS, s);
-        k_lora_grad<<<dim3((unsigned)cdiv(K, 64), (unsigned)ga.nchunks), 256, 0, s>>>(b.sV, r8, X16, M, K, r,
+        k_lora_grad<<<dim3((unsigned)cdiv(K, 64), (unsigned)ga.nchunks), 256, 0, s>>>(b.sV, rp, X16, M, K, r,
                                                                                    ga.rows_per_chunk, b.part);
     }
     if ((st = launch_check("k_lora_grad(dA)"))) return st;

@@ -63,6 +63,9 @@ def run_and_check(g, oracle, M, N, K, r, scale, seed, **kw):
     (130, 256, 640, 64, 0.25),
     (64, 128, 128, 128, 0.5),      # largest rank
     (300, 448, 384, 1, 4.0),       # smallest rank
+    (512, 1024, 2048, 16, 2.0),    # tensor-core path, full tiles
+    (200, 520, 1088, 64, 0.25),    # tensor-core path: ragged M, N and K tiles
+    (128, 256, 4096, 72, 0.5),     # two LoRA k-steps
 ])
 def test_fwd_bwd_parity(g, oracle, M, N, K, r, scale):
     run_and_check(g, oracle, M, N, K, r, scale, seed=3000 + M + N + r)
