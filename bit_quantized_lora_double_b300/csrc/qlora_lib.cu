@@ -130,16 +130,44 @@ size_t quantize_ws(int64_t rows, int64_t cols, float **absmax, double **gsum, do
 // ceil(r / 64) columns so every TMA box lies inside its tensor.
 inline int lora_pad(int r) { return (int)up((size_t)r, 64); }
 
+// Tokens at or above which the tensor-core path runs.
+constexpr int64_t kTcMinM = 64;
+
+// Split of one skinny tcgen05 pass: output rows in 128-row tiles, rank in
+// 64-wide column tiles, contraction in chunks of steps_per_chunk x 64.
+struct SkPlan {
+    int64_t rows, rows_pad, L, spc, chunks;
+    int zt;
+    size_t part_floats;
+};
+SkPlan sk_plan(int64_t rows, int64_t L, int rp) {
+    SkPlan p;
+    p.rows = rows;
+    p.rows_pad = (int64_t)up((size_t)rows, 128);
+    p.L = L;
+    p.zt = rp / 64;
+    const int64_t tiles = p.rows_pad / 128 * p.zt;
+    const int64_t steps = std::max<int64_t>(1, cdiv(L, 64));
+    const int64_t ch = std::min<int64_t>(steps, std::max<int64_t>(1, cdiv(2 * 148, tiles)));
+    p.spc = cdiv(steps, ch);
+    p.chunks = cdiv(steps, p.spc);
+    p.part_floats = (size_t)p.zt * p.chunks * p.rows_pad * 64;
+    return p;
+}
+
 struct FwdWs {
-    uint16_t *sU, *Bp;
+    uint16_t *sU, *Bp, *Ap;
+    float *part;
 };
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
-    (void)K;
     const int rp = lora_pad(r);
+    const bool tc = M >= kTcMinM;
     Carve c(ws);
     uint16_t *sU = c.take<uint16_t>((size_t)M * rp);
-    uint16_t *Bp = c.take<uint16_t>((size_t)N * rp);
-    if (out) *out = FwdWs{sU, Bp};
+    uint16_t *Bp = c.take<uint16_t>(tc ? (size_t)N * rp : 0);
+    uint16_t *Ap = c.take<uint16_t>(tc ? (size_t)rp * K : 0);
+    float *part = c.take<float>(tc ? sk_plan(M, K, rp).part_floats : 0);
+    if (out) *out = FwdWs{sU, Bp, Ap, part};
     return c.off;
 }
 
@@ -158,20 +186,28 @@ GradSplit grad_split(int64_t M, int64_t C) {
 }
 
 struct BwdWs {
-    uint16_t *Bt, *sV, *U, *Ap;
+    uint16_t *Bt, *sV, *U, *Bp, *Ap;
     float *part;
 };
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, BwdWs *out) {
     const int r8 = (int)up(r, 8), rp = lora_pad(r);
-    const GradSplit ga = grad_split(M, K), gb = grad_split(M, N);
-    const size_t part = (size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N);
+    const bool tc = M >= kTcMinM && (N % 8) == 0;
+    size_t part;
+    if (tc) {
+        part = std::max(std::max(sk_plan(M, N, rp).part_floats, sk_plan(M, K, rp).part_floats),
+                        std::max(sk_plan(K, M, rp).part_floats, sk_plan(N, M, rp).part_floats));
+    } else {
+        const GradSplit ga = grad_split(M, K), gb = grad_split(M, N);
+        part = (size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N);
+    }
     Carve c(ws);
-    uint16_t *Bt = c.take<uint16_t>((size_t)r8 * N);
+    uint16_t *Bt = c.take<uint16_t>(tc ? 0 : (size_t)r8 * N);
     uint16_t *sV = c.take<uint16_t>((size_t)M * rp);
-    uint16_t *U = c.take<uint16_t>((size_t)M * r8);
-    uint16_t *Ap = c.take<uint16_t>((size_t)rp * K);
+    uint16_t *U = c.take<uint16_t>((size_t)M * rp);
+    uint16_t *Bp = c.take<uint16_t>(tc ? (size_t)N * rp : 0);
+    uint16_t *Ap = c.take<uint16_t>(tc ? (size_t)rp * K : 0);
     float *p = c.take<float>(part);
-    if (out) *out = BwdWs{Bt, sV, U, Ap, p};
+    if (out) *out = BwdWs{Bt, sV, U, Bp, Ap, p};
     return c.off;
 }
 
@@ -236,8 +272,35 @@ qlora_status tc_setup() {
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per bounded wait
 uint64_t wait_ns() { return g_wait_limit > 0 ? (uint64_t)g_wait_limit * 1000ull : kDefaultWaitNs; }
 
-// Tokens at or above which the tensor-core path runs.
-constexpr int64_t kTcMinM = 64;
+template <int A_MN, int B_MN>
+qlora_status run_skinny(const CUtensorMap &ta, const CUtensorMap &tb, const SkPlan &pl, float *part, cudaStream_t s,
+                        unsigned id) {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(k_gemm_skinny<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   SkCfg::SMEM_BYTES);
+    });
+    if (err != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(err));
+    SkParams prm{pl.rows, pl.rows_pad, pl.L, pl.spc, part, wait_ns(), id};
+    dim3 grid((unsigned)(pl.rows_pad / 128), (unsigned)pl.chunks, (unsigned)pl.zt);
+    {
+        ProfScope ps(id == 5 || id == 6 ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
+        k_gemm_skinny<A_MN, B_MN><<<grid, SkCfg::THREADS, SkCfg::SMEM_BYTES, s>>>(ta, tb, prm);
+    }
+    return launch_check("k_gemm_skinny");
+}
+
+qlora_status run_reduce(const SkPlan &pl, const float *part, int r, int rp, float scale, int mode, uint16_t *o16a,
+                        int lda, uint16_t *o16b, int ldb, float *o32, cudaStream_t s) {
+    {
+        ProfScope ps(mode >= kRedDA ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
+        k_skinny_reduce<<<(unsigned)cdiv(pl.rows * rp, 256), 256, 0, s>>>(part, (int)pl.chunks, pl.rows, pl.rows_pad,
+                                                                         r, rp, scale, mode, o16a, lda, o16b, ldb,
+                                                                         o32);
+    }
+    return launch_check("k_skinny_reduce");
+}
 
 }  // namespace
 
@@ -383,13 +446,16 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int rp = lora_pad(r);
     const uint16_t *X16 = static_cast<const uint16_t *>(X);
-    {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
-                                                          static_cast<uint16_t *>(U_save), r, f.sU, rp);
-    }
-    if ((st = launch_check("k_lora_down"))) return st;
+    uint16_t *U16 = static_cast<uint16_t *>(U_save);
+
     if (M < kTcMinM) {
+        // small M: CUDA-core kernels
+        {
+            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+            k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
+                                                              U16, r, f.sU, rp);
+        }
+        if ((st = launch_check("k_lora_down"))) return st;
         dim3 grid((unsigned)cdiv(N, kSt), (unsigned)cdiv(M, kSt));
         {
             ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
@@ -400,15 +466,23 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         if ((st = launch_check("k_fwd_simt"))) return st;
         return ok();
     }
+
     if ((st = tc_device_ok()) || (st = tc_setup<kFwd>())) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_pad_rows<<<(unsigned)cdiv(rp * K, 256), 256, 0, s>>>(static_cast<const uint16_t *>(A), r, rp, K, f.Ap);
+    }
+    if ((st = launch_check("k_pad_rows(A)"))) return st;
     {
         ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
         k_pad_cols<<<(unsigned)cdiv(N * rp, 256), 256, 0, s>>>(static_cast<const uint16_t *>(B), N, r, rp, f.Bp);
     }
     if ((st = launch_check("k_pad_cols(B)"))) return st;
-    CUtensorMap tmX, tmC, tmU, tmB;
+    CUtensorMap tmX, tmC, tmU, tmB, tmA;
     if ((st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
+        (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.Ap, K, rp, K * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
         (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 32, 256,
                        CU_TENSOR_MAP_SWIZZLE_32B, "codes")) ||
         (st = make_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rp, M, rp * 2, 64, 128,
@@ -416,6 +490,10 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         (st = make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.Bp, rp, N, rp * 2, 64, 256,
                        CU_TENSOR_MAP_SWIZZLE_128B, "B")))
         return st;
+    // U = X A^T on the tensor cores; U (bf16) to U_save, s*U (bf16) to the workspace
+    const SkPlan pu = sk_plan(M, K, rp);
+    if ((st = run_skinny<0, 0>(tmX, tmA, pu, f.part, s, 3))) return st;
+    if ((st = run_reduce(pu, f.part, r, rp, scale, kRedU, U16, r, f.sU, rp, nullptr, s))) return st;
     TcParams prm{};
     prm.M = M;
     prm.Nd = N;
@@ -464,107 +542,147 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "backward workspace %zu < %zu bytes", ws_bytes, need);
     const int r8 = (int)up(r, 8), rp = lora_pad(r);
     const uint16_t *dY16 = static_cast<const uint16_t *>(dY), *X16 = static_cast<const uint16_t *>(X);
-    {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_transpose<<<(unsigned)cdiv(N, 256), 256, 0, s>>>(static_cast<const uint16_t *>(B), N, r, r8, b.Bt);
-    }
-    if ((st = launch_check("k_transpose"))) return st;
-    // sV = bf16(s * dY B), rp columns (zero beyond r)
-    {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, rp);
-    }
-    if ((st = launch_check("k_lora_down(V)"))) return st;
-    const uint16_t *U = static_cast<const uint16_t *>(U_saved);
-    int ldu = r;
-    if (!U) {
+    const uint16_t *A16 = static_cast<const uint16_t *>(A), *B16 = static_cast<const uint16_t *>(B);
+    const bool tc = M >= kTcMinM && (N % 8) == 0;
+
+    if (!tc) {
+        // small M (or N not a multiple of 8): CUDA-core kernels
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, 1.0f,
-                                                              nullptr, 0, b.U, r8);
+            k_transpose<<<(unsigned)cdiv(N, 256), 256, 0, s>>>(B16, N, r, r8, b.Bt);
         }
-        if ((st = launch_check("k_lora_down(U)"))) return st;
-        U = b.U;
-        ldu = r8;
-    }
-    const bool tc = M >= kTcMinM && (N % 8) == 0;
-    if (!tc) {
+        if ((st = launch_check("k_transpose"))) return st;
+        {
+            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+            k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, rp);
+        }
+        if ((st = launch_check("k_lora_down(V)"))) return st;
+        const uint16_t *U = static_cast<const uint16_t *>(U_saved);
+        int ldu = r;
+        if (!U) {
+            {
+                ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+                k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, A16, r, 1.0f, nullptr, 0, b.U, rp);
+            }
+            if ((st = launch_check("k_lora_down(U)"))) return st;
+            U = b.U;
+            ldu = rp;
+        }
         dim3 grid((unsigned)cdiv(K, kSt), (unsigned)cdiv(M, kSt));
         {
             ProfScope ps(QLORA_KERNEL_DX_SIMT, s);
             k_dx_simt<<<grid, 256, 0, s>>>(dY16, M, N, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, K,
-                                           b.sV, rp, static_cast<const uint16_t *>(A), r,
-                                           static_cast<uint16_t *>(dX));
+                                           b.sV, rp, A16, r, static_cast<uint16_t *>(dX));
         }
         if ((st = launch_check("k_dx_simt"))) return st;
+        GradSplit ga = grad_split(M, K);
+        {
+            ProfScope ps(QLORA_KERNEL_GRADS, s);
+            k_lora_grad<<<dim3((unsigned)cdiv(K, 64), (unsigned)ga.nchunks), 256, 0, s>>>(b.sV, rp, X16, M, K, r,
+                                                                                       ga.rows_per_chunk, b.part);
+        }
+        if ((st = launch_check("k_lora_grad(dA)"))) return st;
+        {
+            ProfScope ps(QLORA_KERNEL_GRADS, s);
+            k_grad_reduce<<<(unsigned)cdiv((int64_t)r * K, 256), 256, 0, s>>>(b.part, (int)ga.nchunks, r, K, 1.0f,
+                                                                              0, dA);
+        }
+        if ((st = launch_check("k_grad_reduce(dA)"))) return st;
+        GradSplit gb = grad_split(M, N);
+        {
+            ProfScope ps(QLORA_KERNEL_GRADS, s);
+            k_lora_grad<<<dim3((unsigned)cdiv(N, 64), (unsigned)gb.nchunks), 256, 0, s>>>(U, ldu, dY16, M, N, r,
+                                                                                       gb.rows_per_chunk, b.part);
+        }
+        if ((st = launch_check("k_lora_grad(dB)"))) return st;
+        {
+            ProfScope ps(QLORA_KERNEL_GRADS, s);
+            k_grad_reduce<<<(unsigned)cdiv((int64_t)r * N, 256), 256, 0, s>>>(b.part, (int)gb.nchunks, r, N, scale,
+                                                                              1, dB);
+        }
+        if ((st = launch_check("k_grad_reduce(dB)"))) return st;
+        return ok();
+    }
+
+    if ((st = tc_device_ok()) || (st = tc_setup<kDx>())) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_pad_cols<<<(unsigned)cdiv(N * rp, 256), 256, 0, s>>>(B16, N, r, rp, b.Bp);
+    }
+    if ((st = launch_check("k_pad_cols(B)"))) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_pad_rows<<<(unsigned)cdiv(rp * K, 256), 256, 0, s>>>(A16, r, rp, K, b.Ap);
+    }
+    if ((st = launch_check("k_pad_rows(A)"))) return st;
+    CUtensorMap tmD, tmDmn, tmXk, tmXmn, tmC, tmV, tmA, tmBp, tmUp;
+    if ((st = make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, N, M, N * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "dY")) ||
+        (st = make_map(&tmDmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, N, M, N * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "dY (MN)")) ||
+        (st = make_map(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
+        (st = make_map(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "X (MN)")) ||
+        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "codes")) ||
+        (st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rp, M, rp * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "sV")) ||
+        (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.Ap, K, rp, K * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
+        (st = make_map(&tmBp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.Bp, rp, N, rp * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "B")) ||
+        (st = make_map(&tmUp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.U, rp, M, rp * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "U")))
+        return st;
+    CUtensorMap tmVmn;
+    if ((st = make_map(&tmVmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rp, M, rp * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "sV (MN)")))
+        return st;
+    // V = dY B -> sV = bf16(s * V)
+    const SkPlan pv = sk_plan(M, N, rp);
+    if ((st = run_skinny<0, 1>(tmD, tmBp, pv, b.part, s, 4))) return st;
+    if ((st = run_reduce(pv, b.part, r, rp, scale, kRedV, nullptr, 0, b.sV, rp, nullptr, s))) return st;
+    // U (padded to rp columns): from the forward's U, or recomputed as X A^T
+    if (U_saved) {
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        k_pad_cols<<<(unsigned)cdiv(M * rp, 256), 256, 0, s>>>(static_cast<const uint16_t *>(U_saved), M, r, rp, b.U);
     } else {
-        if ((st = tc_device_ok()) || (st = tc_setup<kDx>())) return st;
-        {
-            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            // A [r, K] -> Ap [rp, K] with zero rows r..rp-1 (row-padded copy)
-            k_pad_rows<<<(unsigned)cdiv(rp * K, 256), 256, 0, s>>>(static_cast<const uint16_t *>(A), r, rp, K, b.Ap);
-        }
-        if ((st = launch_check("k_pad_rows(A)"))) return st;
-        CUtensorMap tmD, tmC, tmV, tmA;
-        if ((st = make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, N, M, N * 2, 64, 128,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "dY")) ||
-            (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, 64,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "codes")) ||
-            (st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rp, M, rp * 2, 64, 128,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "sV")) ||
-            (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.Ap, K, rp, K * 2, 64, 64,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "A")))
-            return st;
-        TcParams prm{};
-        prm.M = M;
-        prm.Nd = K;
-        prm.w_rows = N;
-        prm.w_cols = K;
-        prm.nk_main = cdiv(N, TcCfg::BK);
-        prm.lora_steps = rp / 64;
-        prm.r = r;
-        prm.q = w->absmax_q;
-        prm.s2 = w->absmax_scale;
-        prm.mean = w->absmax_mean;
-        prm.out = static_cast<uint16_t *>(dX);
-        prm.ldo = K;
-        prm.wait_ns = wait_ns();
-        prm.kernel_id = 2;
+        const SkPlan pu = sk_plan(M, K, rp);
+        if ((st = run_skinny<0, 0>(tmXk, tmA, pu, b.part, s, 3))) return st;
+        if ((st = run_reduce(pu, b.part, r, rp, 1.0f, kRedU, nullptr, 0, b.U, rp, nullptr, s))) return st;
+    }
+    if ((st = launch_check("U"))) return st;
+    // dX = dY W' + (sV) A
+    TcParams prm{};
+    prm.M = M;
+    prm.Nd = K;
+    prm.w_rows = N;
+    prm.w_cols = K;
+    prm.nk_main = cdiv(N, TcCfg::BK);
+    prm.lora_steps = rp / 64;
+    prm.r = r;
+    prm.q = w->absmax_q;
+    prm.s2 = w->absmax_scale;
+    prm.mean = w->absmax_mean;
+    prm.out = static_cast<uint16_t *>(dX);
+    prm.ldo = K;
+    prm.wait_ns = wait_ns();
+    prm.kernel_id = 2;
+    {
         dim3 grid((unsigned)cdiv(K, TcCfg::BN), (unsigned)cdiv(M, TcCfg::BM));
-        {
-            ProfScope ps(QLORA_KERNEL_DX_GEMM, s);
-            k_gemm_tc<kDx><<<grid, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(tmD, tmC, tmV, tmA, prm);
-        }
-        if ((st = launch_check("k_gemm_tc<dx>"))) return st;
+        ProfScope ps(QLORA_KERNEL_DX_GEMM, s);
+        k_gemm_tc<kDx><<<grid, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(tmD, tmC, tmV, tmA, prm);
     }
-    // dA = (sV)^T X
-    GradSplit ga = grad_split(M, K);
-    {
-        ProfScope ps(QLORA_KERNEL_GRADS, s);
-        k_lora_grad<<<dim3((unsigned)cdiv(K, 64), (unsigned)ga.nchunks), 256, 0, s>>>(b.sV, rp, X16, M, K, r,
-                                                                                   ga.rows_per_chunk, b.part);
-    }
-    if ((st = launch_check("k_lora_grad(dA)"))) return st;
-    {
-        ProfScope ps(QLORA_KERNEL_GRADS, s);
-        k_grad_reduce<<<(unsigned)cdiv((int64_t)r * K, 256), 256, 0, s>>>(b.part, (int)ga.nchunks, r, K, 1.0f, 0,
-                                                                          dA);
-    }
-    if ((st = launch_check("k_grad_reduce(dA)"))) return st;
-    // dB = s * dY^T U
-    GradSplit gb = grad_split(M, N);
-    {
-        ProfScope ps(QLORA_KERNEL_GRADS, s);
-        k_lora_grad<<<dim3((unsigned)cdiv(N, 64), (unsigned)gb.nchunks), 256, 0, s>>>(U, ldu, dY16, M, N, r,
-                                                                                   gb.rows_per_chunk, b.part);
-    }
-    if ((st = launch_check("k_lora_grad(dB)"))) return st;
-    {
-        ProfScope ps(QLORA_KERNEL_GRADS, s);
-        k_grad_reduce<<<(unsigned)cdiv((int64_t)r * N, 256), 256, 0, s>>>(b.part, (int)gb.nchunks, r, N, scale, 1,
-                                                                          dB);
-    }
-    if ((st = launch_check("k_grad_reduce(dB)"))) return st;
+    if ((st = launch_check("k_gemm_tc<dx>"))) return st;
+    // dA = (sV)^T X   (rows k of dA^T, contraction over the M tokens)
+    const SkPlan pa = sk_plan(K, M, rp);
+    if ((st = run_skinny<1, 1>(tmXmn, tmVmn, pa, b.part, s, 5))) return st;
+    if ((st = run_reduce(pa, b.part, r, rp, 1.0f, kRedDA, nullptr, 0, nullptr, 0, dA, s))) return st;
+    // dB = s dY^T U
+    const SkPlan pb = sk_plan(N, M, rp);
+    if ((st = run_skinny<1, 1>(tmDmn, tmUp, pb, b.part, s, 6))) return st;
+    if ((st = run_reduce(pb, b.part, r, rp, scale, kRedDB, nullptr, 0, nullptr, 0, dB, s))) return st;
     return ok();
 }
 
