@@ -33,17 +33,19 @@ namespace qlora {
 
 enum { kFwd = 0, kDx = 1 };
 
+// One CTA: 256 output rows (two 128-row sub-tiles sharing each decoded W'
+// tile) x 256 output columns; two fp32 accumulators fill the 512 TMEM columns.
 struct TcCfg {
-    static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
-    static constexpr int W_BYTES = BN * BK * 2;  // 32 KB: W' tile (or adapter tile)
-    static constexpr int A_BYTES = BM * BK * 2;  // 16 KB: activation tile
-    static constexpr int C_BYTES = BN * BK / 2;  // 8 KB: packed codes
-    static constexpr int STAGE_BYTES = W_BYTES + A_BYTES + C_BYTES;
+    static constexpr int BM = 256, SUB = 128, BN = 256, BK = 64, STAGES = 3;
+    static constexpr int W_BYTES = BN * BK * 2;    // 32 KB: W' tile (or adapter tile)
+    static constexpr int A_BYTES = SUB * BK * 2;   // 16 KB: one activation sub-tile
+    static constexpr int C_BYTES = BN * BK / 2;    // 8 KB: packed codes
+    static constexpr int STAGE_BYTES = W_BYTES + 2 * A_BYTES + C_BYTES;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
     static constexpr int THREADS = 320;
     static constexpr int DEQ_WARPS = 8;
-    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t TMEM_COLS = 512;
 };
 
 struct TcParams {
@@ -59,6 +61,9 @@ struct TcParams {
     const float *mean;
     uint16_t *out;
     int64_t ldo;
+    int splits;            // contraction splits (grid.z); 1 = no split
+    int64_t steps_per_split;
+    float *part;           // splits > 1: fp32 partials [splits][M][Nd]
     uint64_t wait_ns;
     unsigned kernel_id;
 };
@@ -100,18 +105,24 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     uint64_t *full = bar;                       // TMA bytes landed (producer arrive + tx)
     uint64_t *wfull = bar + C::STAGES;          // W' tile decoded (8 warp arrivals)
     uint64_t *empty = bar + 2 * C::STAGES;      // stage consumed by the MMAs (commit)
-    uint64_t *accfull = bar + 3 * C::STAGES;    // accumulator complete (commit)
+    uint64_t *accfull = bar + 3 * C::STAGES;    // accumulators complete (commit)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * C::STAGES + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     auto wtile = [&](int s) { return smem + s * C::STAGE_BYTES; };
-    auto atile = [&](int s) { return smem + s * C::STAGE_BYTES + C::W_BYTES; };
-    auto ctile = [&](int s) { return smem + s * C::STAGE_BYTES + C::W_BYTES + C::A_BYTES; };
+    auto atile = [&](int s, int h) { return smem + s * C::STAGE_BYTES + C::W_BYTES + h * C::A_BYTES; };
+    auto ctile = [&](int s) { return smem + s * C::STAGE_BYTES + C::W_BYTES + 2 * C::A_BYTES; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t m0 = (int64_t)blockIdx.y * C::BM;
     const int64_t c0 = (int64_t)blockIdx.x * C::BN;  // first output column
-    const int64_t nk = p.nk_main + p.lora_steps;
+    // this CTA's share of the contraction: main k-steps [kbeg, kbeg + nmain),
+    // then the LoRA steps if it holds the last split
+    const int z = (int)blockIdx.z;
+    const int64_t kbeg = (int64_t)z * p.steps_per_split;
+    const int64_t nmain = max((int64_t)0, min(p.steps_per_split, p.nk_main - kbeg));
+    const int64_t nk = nmain + (z == p.splits - 1 ? p.lora_steps : 0);
+    const bool two = m0 + C::SUB < p.M;               // second 128-row sub-tile has rows
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -142,22 +153,26 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
+            const uint32_t abytes = (two ? 2 : 1) * C::A_BYTES;
             int64_t issued = 0;
             for (int64_t it = 0; it < nk; ++it) {
                 const int s = (int)(it % C::STAGES);
                 const uint32_t u = (uint32_t)(it / C::STAGES);
                 if (u > 0 && !tc_wait(&empty[s], (u - 1) & 1, p.wait_ns, (p.kernel_id << 16) | 1, abort_flag)) break;
-                if (it < p.nk_main) {
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::C_BYTES);
-                    tma_load_2d(atile(s), &tm_act, &full[s], (int32_t)(it * C::BK), (int32_t)m0);
+                if (it < nmain) {
+                    mbar_arrive_expect_tx(&full[s], abytes + C::C_BYTES);
+                    const int32_t k = (int32_t)((kbeg + it) * C::BK);
+                    tma_load_2d(atile(s, 0), &tm_act, &full[s], k, (int32_t)m0);
+                    if (two) tma_load_2d(atile(s, 1), &tm_act, &full[s], k, (int32_t)(m0 + C::SUB));
                     if (MODE == kFwd)
-                        tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(it * C::BK / 2), (int32_t)c0);
+                        tma_load_2d(ctile(s), &tm_codes, &full[s], k / 2, (int32_t)c0);
                     else
-                        tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(c0 / 2), (int32_t)(it * C::BK));
+                        tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(c0 / 2), k);
                 } else {
-                    const int32_t j = (int32_t)(it - p.nk_main) * C::BK;
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::W_BYTES);
-                    tma_load_2d(atile(s), &tm_lact, &full[s], j, (int32_t)m0);
+                    const int32_t j = (int32_t)(it - nmain) * C::BK;
+                    mbar_arrive_expect_tx(&full[s], abytes + C::W_BYTES);
+                    tma_load_2d(atile(s, 0), &tm_lact, &full[s], j, (int32_t)m0);
+                    if (two) tma_load_2d(atile(s, 1), &tm_lact, &full[s], j, (int32_t)(m0 + C::SUB));
                     if (MODE == kFwd) {
                         tma_load_2d(wtile(s), &tm_lw, &full[s], j, (int32_t)c0);
                     } else {
@@ -172,7 +187,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
             for (int s = 0; s < C::STAGES; ++s) {
                 if (issued <= s) break;
                 const int64_t last = issued - 1 - ((issued - 1 - s) % C::STAGES);
-                uint64_t t0 = globaltimer();
+                const uint64_t t0 = globaltimer();
                 while (!mbar_try_wait(&full[s], (uint32_t)(last / C::STAGES) & 1))
                     if (globaltimer() - t0 > p.wait_ns) break;
             }
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer ----
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(C::BM, C::BN, 0, MODE == kDx ? 1 : 0);
+            constexpr uint32_t idesc = idesc_bf16(C::SUB, C::BN, 0, MODE == kDx ? 1 : 0);
             for (int64_t it = 0; it < nk; ++it) {
                 const int s = (int)(it % C::STAGES);
                 const uint32_t par = (uint32_t)(it / C::STAGES) & 1;
@@ -188,16 +203,17 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
                 if (!tc_wait(&wfull[s], par, p.wait_ns, (p.kernel_id << 16) | 4, abort_flag)) break;
                 tc_fence_after();
                 int nmma = 4;
-                if (it >= p.nk_main) {
-                    const int rem = p.r - (int)(it - p.nk_main) * C::BK;
+                if (it >= nmain) {
+                    const int rem = p.r - (int)(it - nmain) * C::BK;
                     nmma = rem >= C::BK ? 4 : (rem + 15) / 16;
                 }
-                const uint32_t a0 = smem_u32(atile(s)), w0 = smem_u32(wtile(s));
+                const uint32_t a0 = smem_u32(atile(s, 0)), a1 = smem_u32(atile(s, 1)), w0 = smem_u32(wtile(s));
                 for (int kk = 0; kk < nmma; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
                     const uint64_t bd = MODE == kFwd ? smem_desc_sw128(w0 + kk * 32, 16, 1024)
                                                      : smem_desc_sw128(w0 + kk * 2048, 8192, 1024);
-                    tc_mma_bf16(tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), bd, idesc, acc);
+                    if (two) tc_mma_bf16(tmem + 256, smem_desc_sw128(a1 + kk * 32, 16, 1024), bd, idesc, acc);
                 }
                 tc_commit(&empty[s]);
             }
@@ -208,45 +224,66 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         const int dt = threadIdx.x - 64;  // 0..255
         const float mean = *p.mean;
         const int64_t kblocks = p.w_cols / kBlock;
+        // This thread's W row / 64-column block at k-step `it`, its slot in
+        // the code tile and the byte offsets of its 8 output chunks.
+        int64_t wrow0, kb0, wrow_step, kb_step;
+        int crow, ccol;
+        uint32_t dst[8];
+        if (MODE == kFwd) {
+            // row c0 + dt of W, block `it`; K-major 128-byte swizzled row
+            wrow0 = c0 + dt;
+            wrow_step = 0;
+            kb0 = 0;
+            kb_step = 1;
+            crow = dt;
+            ccol = 0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) dst[c] = (uint32_t)((dt >> 3) * 1024 + (dt & 7) * 128 + ((c ^ (dt & 7)) << 4));
+        } else {
+            // row it*64 + nl of W (K-group of the MN-major operand), block b4
+            const int nlo = dt & 7, b4 = (dt >> 3) & 3, nhi = dt >> 5;
+            const int nl = nhi * 8 + nlo;
+            wrow0 = nl;
+            wrow_step = C::BK;
+            kb0 = c0 / kBlock + b4;
+            kb_step = 0;
+            crow = nl;
+            ccol = b4;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) dst[c] = (uint32_t)(b4 * 8192 + nhi * 1024 + nlo * 128 + ((c ^ nlo) << 4));
+        }
+        // absmax code and scale for local k-step `it` (prefetched one step ahead)
+        auto fetch = [&](int64_t it, int &qv, float &sv) {
+            const int64_t g = kbeg + it;
+            const int64_t wrow = wrow0 + g * wrow_step, kb = kb0 + g * kb_step;
+            if (it < nmain && wrow < p.w_rows && kb < kblocks) {
+                const int64_t b = wrow * kblocks + kb;
+                qv = __ldg(p.q + b);
+                sv = __ldg(p.s2 + (b >> 8));
+                return true;
+            }
+            qv = 0;
+            sv = 0.0f;
+            return false;
+        };
+        int q_cur, q_nxt;
+        float s_cur, s_nxt;
+        bool v_cur = fetch(0, q_cur, s_cur), v_nxt = false;
         bool alive = true;
         for (int64_t it = 0; it < nk && alive; ++it) {
             const int s = (int)(it % C::STAGES);
             const uint32_t par = (uint32_t)(it / C::STAGES) & 1;
+            v_nxt = fetch(it + 1, q_nxt, s_nxt);
             if (!tc_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag)) {
                 alive = false;
                 break;
             }
-            if (it < p.nk_main) {
+            if (it < nmain) {
                 uint8_t *wt = wtile(s);
                 const uint8_t *ct = ctile(s);
-                int64_t wrow, kb;  // W row and 64-column block this thread decodes
-                int crow, ccol;    // its row / 32-byte slot in the code tile
-                uint32_t dst[8];   // byte offsets of its 8 output chunks in the W' tile
-                if (MODE == kFwd) {
-                    // row n = c0 + dt of W, block it; K-major 128-byte swizzled row
-                    wrow = c0 + dt;
-                    kb = it;
-                    crow = dt;
-                    ccol = 0;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dst[c] = (uint32_t)((dt >> 3) * 1024 + (dt & 7) * 128 + ((c ^ (dt & 7)) << 4));
-                } else {
-                    // row n of W (K-group of the MN-major operand), 64-column block b4
-                    const int nlo = dt & 7, b4 = (dt >> 3) & 3, nhi = dt >> 5;
-                    const int nl = nhi * 8 + nlo;
-                    wrow = it * C::BK + nl;
-                    kb = c0 / kBlock + b4;
-                    crow = nl;
-                    ccol = b4;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dst[c] = (uint32_t)(b4 * 8192 + nhi * 1024 + nlo * 128 + ((c ^ nlo) << 4));
-                }
                 uint32_t o[8][4];
-                if (wrow < p.w_rows && kb < kblocks) {
-                    const int64_t b = wrow * kblocks + kb;
-                    const Nf4Table tab = make_table(dq_absmax(__ldg(p.q + b), __ldg(p.s2 + b / kGroup), mean));
+                if (v_cur) {
+                    const Nf4Table tab = make_table(dq_absmax((int8_t)q_cur, s_cur, mean));
                     uint4 cw[2];
                     if (MODE == kFwd) {
                         // 32-byte rows, 32-byte swizzle: half h sits at h ^ bit 2 of the row
@@ -273,22 +310,38 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&wfull[s]);
+            q_cur = q_nxt;
+            s_cur = s_nxt;
+            v_cur = v_nxt;
         }
         // ------------------------------------------------------ epilogue
         const bool acc_ok = tc_wait(accfull, 0, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag);
         tc_fence_after();
-        if (acc_ok && alive) {
-            const int quarter = warp & 3, half = (warp - 2) >> 2;
-            const int64_t row = m0 + quarter * 32 + lane;
+        const int quarter = warp & 3, sub = (warp - 2) >> 2;
+        if (acc_ok && alive && (sub == 0 || two)) {
+            const int64_t row = m0 + sub * C::SUB + quarter * 32 + lane;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col = half * 128 + cc * 32;
+            for (int cc = 0; cc < C::BN / 32; ++cc) {
+                const int col = cc * 32;
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col, v);
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(sub * 256 + col), v);
                 tmem_ld_wait();
-                if (row < p.M) {
-                    uint16_t *dst = p.out + row * p.ldo + c0 + col;
-                    const int64_t ncol = p.Nd - (c0 + col);  // valid columns from here
+                const int64_t ncol = p.Nd - (c0 + col);  // valid columns from here
+                if (row < p.M && p.splits > 1) {
+                    float *dstf = p.part + ((int64_t)z * p.M + row) * p.Nd + c0 + col;
+                    if (ncol >= 32 && ((p.Nd & 3) == 0)) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            reinterpret_cast<float4 *>(dstf)[g] =
+                                make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                            __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e < ncol) dstf[e] = __uint_as_float(v[e]);
+                    }
+                } else if (row < p.M) {
+                    uint16_t *dstp = p.out + row * p.ldo + c0 + col;
                     if (ncol >= 32 && ((p.ldo & 7) == 0)) {
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
@@ -297,12 +350,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
                             pk.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
                             pk.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
                             pk.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
-                            reinterpret_cast<uint4 *>(dst)[g] = pk;
+                            reinterpret_cast<uint4 *>(dstp)[g] = pk;
                         }
                     } else {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (e < ncol) dst[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
+                            if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
                     }
                 }
             }
@@ -319,6 +372,42 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
 }  // namespace qlora
 
 namespace qlora {
+
+// out[row, col] = bf16( sum over splits, in split order, of part[z][row][col] )
+__global__ void k_split_reduce(const float *__restrict__ part, int splits, int64_t M, int64_t Nd,
+                               uint16_t *__restrict__ out, int64_t ldo) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= M * Nd) return;
+    const int64_t row = i / Nd, col = i % Nd;
+    if (col + 4 <= Nd && (Nd & 3) == 0) {
+        float4 a = reinterpret_cast<const float4 *>(part + i)[0];
+        for (int zz = 1; zz < splits; ++zz) {
+            const float4 b = reinterpret_cast<const float4 *>(part + (int64_t)zz * M * Nd + i)[0];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        uint2 pk;
+        pk.x = pack_bf16x2(a.x, a.y);
+        pk.y = pack_bf16x2(a.z, a.w);
+        if ((ldo & 3) == 0) {
+            *reinterpret_cast<uint2 *>(out + row * ldo + col) = pk;
+            return;
+        }
+        out[row * ldo + col] = (uint16_t)(pk.x & 0xFFFF);
+        out[row * ldo + col + 1] = (uint16_t)(pk.x >> 16);
+        out[row * ldo + col + 2] = (uint16_t)(pk.y & 0xFFFF);
+        out[row * ldo + col + 3] = (uint16_t)(pk.y >> 16);
+        return;
+    }
+    for (int e = 0; e < 4 && i + e < M * Nd; ++e) {
+        const int64_t ii = i + e, r = ii / Nd, c = ii % Nd;
+        float a = part[ii];
+        for (int zz = 1; zz < splits; ++zz) a += part[(int64_t)zz * M * Nd + ii];
+        out[r * ldo + c] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+    }
+}
 
 // ---------------------------------------------------------------------------
 // Skinny tcgen05 GEMM for the LoRA side path:

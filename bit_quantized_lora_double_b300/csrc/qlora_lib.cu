@@ -155,6 +155,20 @@ SkPlan sk_plan(int64_t rows, int64_t L, int rp) {
     return p;
 }
 
+// Contraction splits of the fused GEMM: split only when the output tiles fill
+// less than three quarters of the 148 SMs, keeping >= 4 k-steps per split.
+struct GemmSplit {
+    int splits;
+    int64_t steps_per_split;
+};
+GemmSplit gemm_split(int64_t M, int64_t Nd, int64_t nk_main) {
+    const int64_t tiles = cdiv(Nd, 256) * cdiv(M, 256);
+    int64_t sp = 1;
+    if (tiles * 4 < 3 * 148) sp = std::max<int64_t>(1, std::min<int64_t>({148 / tiles, nk_main / 4, 8}));
+    const int64_t sps = cdiv(nk_main, sp);
+    return {(int)cdiv(nk_main, sps), sps};
+}
+
 struct FwdWs {
     uint16_t *sU, *Bp, *Ap;
     float *part;
@@ -166,7 +180,12 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     uint16_t *sU = c.take<uint16_t>((size_t)M * rp);
     uint16_t *Bp = c.take<uint16_t>(tc ? (size_t)N * rp : 0);
     uint16_t *Ap = c.take<uint16_t>(tc ? (size_t)rp * K : 0);
-    float *part = c.take<float>(tc ? sk_plan(M, K, rp).part_floats : 0);
+    size_t pf = 0;
+    if (tc) {
+        const GemmSplit g = gemm_split(M, N, K / 64);
+        pf = std::max(sk_plan(M, K, rp).part_floats, g.splits > 1 ? (size_t)g.splits * M * N : (size_t)0);
+    }
+    float *part = c.take<float>(pf);
     if (out) *out = FwdWs{sU, Bp, Ap, part};
     return c.off;
 }
@@ -196,6 +215,8 @@ size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, BwdWs *out) {
     if (tc) {
         part = std::max(std::max(sk_plan(M, N, rp).part_floats, sk_plan(M, K, rp).part_floats),
                         std::max(sk_plan(K, M, rp).part_floats, sk_plan(N, M, rp).part_floats));
+        const GemmSplit g = gemm_split(M, K, cdiv(N, 64));
+        if (g.splits > 1) part = std::max(part, (size_t)g.splits * M * K);
     } else {
         const GradSplit ga = grad_split(M, K), gb = grad_split(M, N);
         part = (size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N);
@@ -507,14 +528,26 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     prm.mean = w->absmax_mean;
     prm.out = static_cast<uint16_t *>(Y);
     prm.ldo = N;
+    const GemmSplit gs = gemm_split(M, N, prm.nk_main);
+    prm.splits = gs.splits;
+    prm.steps_per_split = gs.steps_per_split;
+    prm.part = f.part;
     prm.wait_ns = wait_ns();
     prm.kernel_id = 1;
-    dim3 grid((unsigned)cdiv(N, TcCfg::BN), (unsigned)cdiv(M, TcCfg::BM));
+    dim3 grid((unsigned)cdiv(N, TcCfg::BN), (unsigned)cdiv(M, TcCfg::BM), (unsigned)gs.splits);
     {
         ProfScope ps(QLORA_KERNEL_FWD_GEMM, s);
         k_gemm_tc<kFwd><<<grid, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(tmX, tmC, tmU, tmB, prm);
     }
     if ((st = launch_check("k_gemm_tc<fwd>"))) return st;
+    if (gs.splits > 1) {
+        {
+            ProfScope ps(QLORA_KERNEL_FWD_GEMM, s);
+            k_split_reduce<<<(unsigned)cdiv(cdiv(M * N, 4), 256), 256, 0, s>>>(f.part, gs.splits, M, N,
+                                                                             static_cast<uint16_t *>(Y), N);
+        }
+        if ((st = launch_check("k_split_reduce"))) return st;
+    }
     return ok();
 }
 
@@ -667,14 +700,26 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     prm.mean = w->absmax_mean;
     prm.out = static_cast<uint16_t *>(dX);
     prm.ldo = K;
+    const GemmSplit gs = gemm_split(M, K, prm.nk_main);
+    prm.splits = gs.splits;
+    prm.steps_per_split = gs.steps_per_split;
+    prm.part = b.part;
     prm.wait_ns = wait_ns();
     prm.kernel_id = 2;
     {
-        dim3 grid((unsigned)cdiv(K, TcCfg::BN), (unsigned)cdiv(M, TcCfg::BM));
+        dim3 grid((unsigned)cdiv(K, TcCfg::BN), (unsigned)cdiv(M, TcCfg::BM), (unsigned)gs.splits);
         ProfScope ps(QLORA_KERNEL_DX_GEMM, s);
         k_gemm_tc<kDx><<<grid, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(tmD, tmC, tmV, tmA, prm);
     }
     if ((st = launch_check("k_gemm_tc<dx>"))) return st;
+    if (gs.splits > 1) {
+        {
+            ProfScope ps(QLORA_KERNEL_DX_GEMM, s);
+            k_split_reduce<<<(unsigned)cdiv(cdiv(M * K, 4), 256), 256, 0, s>>>(b.part, gs.splits, M, K,
+                                                                             static_cast<uint16_t *>(dX), K);
+        }
+        if ((st = launch_check("k_split_reduce"))) return st;
+    }
     // dA = (sV)^T X   (rows k of dA^T, contraction over the M tokens)
     const SkPlan pa = sk_plan(K, M, rp);
     if ((st = run_skinny<1, 1>(tmXmn, tmVmn, pa, b.part, s, 5))) return st;
