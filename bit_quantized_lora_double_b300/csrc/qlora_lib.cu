@@ -410,6 +410,74 @@ qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, 
     return ok();
 }
 
+// ---- quantize without a caller workspace ------------------------------------
+// The scratch lives in this file-scope device array. In host code its name is
+// only a host-side stand-in, so the device address is looked up with
+// cudaGetSymbolAddress, once per device, with that device current.
+static __device__ __align__(256) unsigned char g_quantize_scratch[QLORA_NF4_NOALLOC_SCRATCH_BYTES];
+static std::mutex g_scratch_mu;
+static void *g_scratch_ptr[128] = {};
+
+static qlora_status quantize_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 128) return fail(QLORA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_quantize_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(QLORA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return QLORA_OK;
+}
+
+qlora_status qlora_nf4_quantize_noalloc(const void *W, qlora_nf4_weight *out, qlora_stream_t stream) {
+    qlora_status st = check_weight(out, false);
+    if (st) return st;
+    if (!W) return fail(QLORA_ERR_NULL, "W is NULL");
+    if (!al16(W)) return fail(QLORA_ERR_ALIGN, "W must be 16-byte aligned");
+    const int64_t rows = out->rows, cols = out->cols;
+    if (rows == 0) return ok();
+    const size_t need = quantize_ws(rows, cols, nullptr, nullptr, nullptr, nullptr, nullptr);
+    if (need > QLORA_NF4_NOALLOC_SCRATCH_BYTES)
+        return fail(QLORA_ERR_WORKSPACE,
+                    "weight [%lld, %lld] needs %zu bytes of scratch; the built-in scratch holds %u bytes "
+                    "(use qlora_nf4_quantize with a workspace)",
+                    (long long)rows, (long long)cols, need, QLORA_NF4_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    if ((st = quantize_scratch(&scratch))) return st;
+    float *absmax;
+    double *gsum, *b0, *b1;
+    quantize_ws(rows, cols, &absmax, &gsum, &b0, &b1, scratch);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t nb = rows * cols / kBlock, ng = cdiv(nb, kGroup);
+    k_nf4_encode<<<(unsigned)ng, 256, 0, s>>>(static_cast<const uint4 *>(W), nb,
+                                             reinterpret_cast<uint32_t *>(out->codes), absmax, gsum);
+    if ((st = launch_check("k_nf4_encode"))) return st;
+    const double *cur = gsum;
+    int64_t n = ng;
+    double *bufs[2] = {b0, b1};
+    int flip = 0;
+    while (n > 256) {
+        const int64_t chunks = cdiv(n, 256);
+        k_pairwise_reduce<<<(unsigned)cdiv(chunks, 8), 256, 0, s>>>(cur, n, bufs[flip], nullptr, nb);
+        if ((st = launch_check("k_pairwise_reduce"))) return st;
+        cur = bufs[flip];
+        flip ^= 1;
+        n = chunks;
+    }
+    k_pairwise_reduce<<<1, 256, 0, s>>>(cur, n, nullptr, out->absmax_mean, nb);
+    if ((st = launch_check("k_pairwise_reduce(mean)"))) return st;
+    k_dq_encode<<<(unsigned)cdiv(ng, 8), 256, 0, s>>>(absmax, nb, out->absmax_mean, out->absmax_q,
+                                                      out->absmax_scale);
+    if ((st = launch_check("k_dq_encode"))) return st;
+    return ok();
+}
+
 qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream) {
     qlora_status st = check_weight(w, false);
     if (st) return st;

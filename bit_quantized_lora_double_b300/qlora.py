@@ -26,7 +26,8 @@ STATUS = {0: "QLORA_OK", 1: "QLORA_ERR_NULL", 2: "QLORA_ERR_SHAPE", 3: "QLORA_ER
 
 EXPORTS = [
     "qlora_nf4_codes_bytes", "qlora_nf4_absmax_count", "qlora_nf4_scale_count", "qlora_nf4_storage_bytes",
-    "qlora_nf4_quantize_workspace", "qlora_nf4_table", "qlora_nf4_quantize", "qlora_nf4_dequantize",
+    "qlora_nf4_quantize_workspace", "qlora_nf4_table", "qlora_nf4_quantize", "qlora_nf4_quantize_noalloc",
+    "qlora_nf4_dequantize",
     "qlora_linear_fwd_workspace", "qlora_linear_bwd_workspace", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_last_error", "qlora_check_device_status", "qlora_set_wait_limit", "qlora_version",
     "qlora_profile_start", "qlora_profile_stop",
@@ -64,6 +65,8 @@ def lib():
         L.qlora_nf4_table.argtypes = [vp]
         L.qlora_nf4_quantize.restype = i32
         L.qlora_nf4_quantize.argtypes = [vp, W, vp, sz, vp]
+        L.qlora_nf4_quantize_noalloc.restype = i32
+        L.qlora_nf4_quantize_noalloc.argtypes = [vp, W, vp]
         L.qlora_nf4_dequantize.restype = i32
         L.qlora_nf4_dequantize.argtypes = [W, vp, vp]
         L.qlora_linear_fwd_workspace.restype = sz
@@ -183,6 +186,12 @@ def qlora_nf4_quantize(W: torch.Tensor, out: Nf4Weight, ws: torch.Tensor, stream
     d = out.desc
     _check(lib().qlora_nf4_quantize(_ptr(W), ctypes.byref(d), _ptr(ws), ws.numel() * ws.element_size(),
                                     _stream(stream)))
+
+
+def qlora_nf4_quantize_noalloc(W: torch.Tensor, out: Nf4Weight, stream=None):
+    """Quantize with the library's built-in scratch (no workspace, no allocation)."""
+    d = out.desc
+    _check(lib().qlora_nf4_quantize_noalloc(_ptr(W), ctypes.byref(d), _stream(stream)))
 
 
 def qlora_nf4_dequantize(w: Nf4Weight, out: torch.Tensor, stream=None):

@@ -130,6 +130,31 @@ void qlora_nf4_table(float levels[16]);
 qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, size_t ws_bytes,
                                 qlora_stream_t stream);
 
+/* Quantizes like qlora_nf4_quantize, bit for bit, but takes no workspace and
+ * allocates nothing. The pages have no counterpart: this is an interface
+ * variant for callers that cannot allocate device memory, for example a
+ * plugin inside a host application or framework that owns every device
+ * buffer through its own pool and hands the plugin only its inputs and
+ * outputs, or code that must not trigger cudaMalloc's implicit device
+ * synchronization (or its failure under fragmentation) mid-run.
+ *  - Scratch comes from one array of QLORA_NF4_NOALLOC_SCRATCH_BYTES compiled
+ *    into the library; every GPU that loads the library holds it until the
+ *    process exits. A weight whose quantize workspace
+ *    (qlora_nf4_quantize_workspace) exceeds that size is rejected with
+ *    QLORA_ERR_WORKSPACE and nothing is launched (16 MiB covers about
+ *    2.6e8 weights, e.g. 28672 x 8192).
+ *  - The first call on each device (with that device current) looks up the
+ *    array's device address once; make that first call before any stream
+ *    capture.
+ *  - All calls share the one array, which keeps the last call's contents;
+ *    nothing in it needs to start at zero. Calls that can overlap on the GPU
+ *    (different streams without ordering between them) race on it: order
+ *    them.
+ *  - The caller still passes W and allocates `out`'s arrays as for
+ *    qlora_nf4_quantize. */
+#define QLORA_NF4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+qlora_status qlora_nf4_quantize_noalloc(const void *W, qlora_nf4_weight *out, qlora_stream_t stream);
+
 /* Writes the dequantized bf16 weight W' [rows, cols] (device) to `out`:
  * w' = bf16_rne(fp32(L[code] * a')) with a' = fp32(q)*scale + mean.
  * Source: ashishsrivastav.com, section "Double Quantization" (dequantize on
