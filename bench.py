@@ -173,8 +173,10 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--prof-steps", type=int, default=20)
+    ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -228,10 +230,10 @@ def main():
 
     def step():
         for d in P:
-            qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"], stream)
+            qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"])
         for d in reversed(P):
             qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
-                                   d["dB"], d["ws"], stream)
+                                   d["dB"], d["ws"])
             if world > 1:
                 dist.all_reduce(d["dA"])
                 dist.all_reduce(d["dB"])
@@ -246,16 +248,27 @@ def main():
     qlora.qlora_check_device_status(stream)
     barrier()
 
+    # The timed region replays one CUDA graph of the step (captured after the
+    # warm-up; the library's calls allocate and synchronize nothing, so they
+    # capture as they are), or launches the step eagerly with --no-graph.
+    graph = None
+    if not args.no_graph and world == 1:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        barrier()
+        qlora.qlora_check_device_status(stream)
+    run_step = graph.replay if graph is not None else step
+
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
-        qlora.qlora_profile_start()
         barrier()
-        ev0.record(stream)
+        ev0.record()
         for _ in range(args.steps):
-            step()
-        ev1.record(stream)
+            run_step()
+        ev1.record()
         barrier()
-        prof_ms, prof_n, launches = qlora.qlora_profile_stop()
     ms = ev0.elapsed_time(ev1)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -268,6 +281,18 @@ def main():
     ms_step = ms / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
 
+    # Per-kernel device times: the same step launched eagerly with the
+    # library's profiling hooks (a CUDA event pair around every launch, on the
+    # launch stream), right after the timed region.
+    prof_steps = max(1, min(args.steps, args.prof_steps))
+    qlora.qlora_profile_start()
+    barrier()
+    for _ in range(prof_steps):
+        step()
+    barrier()
+    prof_ms, prof_n, _ = qlora.qlora_profile_stop()
+    launches = sum(prof_n.values()) // prof_steps * args.steps
+
     # dominant kernel of the step and its roofline: per kind, the summed
     # device time of its launches in the timed region against the algorithmic
     # flops of those launches (a kind's split-reduction launches count with it)
@@ -279,13 +304,14 @@ def main():
                   "dx_simt": sum(dx_gemm_flops(M, n, k, r) for _, n, k in projs)}
     roof = None
     if dom in gemm_flops:
-        ms_kind = prof_ms[dom] / args.steps
+        ms_kind = prof_ms[dom] / prof_steps
         ach = gemm_flops[dom] / (ms_kind * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                 "frac": ach / pk["bf16_sus"], "traffic": None,
                 "peak_note": f"bf16 dense sustained ({pk['src']}); a kernel timed inside a long step",
                 "flops_per_launch": gemm_flops[dom] / len(projs),
-                "launches_per_step": prof_n[dom] / args.steps, "ms_per_step": ms_kind}
+                "launches_per_step": prof_n[dom] / prof_steps, "ms_per_step": ms_kind,
+                "timing": f"CUDA events around each launch, {prof_steps} eager profiled steps after the timed region"}
 
     # ---- end to end through the C ABI with host buffers ----------------------
     hY = {d["name"]: torch.empty(d["Y"].shape, dtype=torch.bfloat16, pin_memory=True) for d in P}
@@ -298,12 +324,12 @@ def main():
     def e2e_step():
         for d in P:
             d["X"].copy_(d["hX"], non_blocking=True)
-            qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"], stream)
+            qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"])
             hY[d["name"]].copy_(d["Y"], non_blocking=True)
         for d in reversed(P):
             d["dY"].copy_(d["hdY"], non_blocking=True)
             qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
-                                   d["dB"], d["ws"], stream)
+                                   d["dB"], d["ws"])
             if world > 1:
                 dist.all_reduce(d["dA"])
                 dist.all_reduce(d["dB"])
@@ -387,8 +413,9 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
-            "kernels_ms": {k: v for k, v in prof_ms.items() if prof_n[k]},
-            "kernels_launches": {k: v for k, v in prof_n.items() if v},
+            "kernels_ms_per_step": {k: v / prof_steps for k, v in prof_ms.items() if prof_n[k]},
+            "kernels_launches_per_step": {k: v // prof_steps for k, v in prof_n.items() if v},
+            "timed_region": "CUDA graph of one step replayed" if graph is not None else "eager launches",
             "clocks": clocks,
             "codec": codec,
         }

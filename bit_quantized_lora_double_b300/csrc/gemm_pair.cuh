@@ -1,0 +1,408 @@
+// gemm_pair.cuh -- fused NF4-dequant + LoRA GEMM on a CTA pair (tcgen05
+// cta_group::2) for sm_103a.
+//
+//   forward (kFwd):  Y [M, N]  = X [M, K]  . W'^T       + (sU) [M, r] . B^T
+//   dX      (kDx):   dX [M, K] = dY [M, N] . W'          + (sV) [M, r] . A
+//
+// Two CTAs of a cluster compute a 512 x 256 output tile together. Each
+// tcgen05.mma (M = 256, N = 256, K = 16) issued by the even CTA reads 128
+// activation rows and 128 of the 256 weight columns from each CTA's shared
+// memory and accumulates 128 x 256 fp32 in each CTA's TMEM. Two such 256-row
+// sub-tiles fill the 512 TMEM columns, so every decoded weight tile feeds
+// 2 x 256 rows while each CTA decodes only its half of it: 128 x 64 weights
+// per 64-deep k-step against 2 x (128 x 256 x 64) MACs.
+//
+// Roles per CTA (10 warps):
+//   warp 0      TMA producer: two 128 x 64 activation tiles and this CTA's
+//               half of the packed-code tile per stage (in the LoRA steps
+//               the s*U or s*V tiles and this CTA's half of the adapter
+//               tile instead).
+//   warp 1      TMEM allocation (both CTAs); in the even CTA one lane waits
+//               until both halves of a stage are decoded, issues the MMAs and
+//               commits to the stage's `empty` barriers of both CTAs.
+//   warps 2..9  two decode groups of 4 warps taking alternate k-steps: each
+//               thread expands one block of 64 codes through the per-block
+//               scaled byte-plane table into the UMMA operand layout, then
+//               arrives on the even CTA's `ready` barrier; after the last
+//               k-step all 8 warps read the accumulators and store bf16 rows.
+// The LoRA term enters as ceil(r/64) extra k-steps into the same
+// accumulators. Every wait is bounded in time; a wait that runs out records
+// the error word, raises the abort flag in both CTAs, and the kernel drains
+// and exits.
+// Sources: ashishsrivastav.com "QLoRA: Fine-Tuning a 70B on One GPU", section
+// "Double Quantization" (dequantize on the fly for the matmul);
+// xingyuzhitong.com "Fine-Tuning Memory Requirements", section "QLoRA: quantize
+// the frozen base to 4 bits".
+#pragma once
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+
+namespace qlora {
+
+struct PairCfg {
+    static constexpr int SUB = 128;               // rows per CTA per sub-tile
+    static constexpr int PAIR_M = 512;            // rows per pair tile (2 sub-tiles x 256)
+    static constexpr int BN = 256, HN = 128, BK = 64, STAGES = 4;
+    static constexpr int A_BYTES = SUB * BK * 2;  // 16 KB: one activation tile
+    static constexpr int W_BYTES = HN * BK * 2;   // 16 KB: this CTA's half of W' (or adapter)
+    static constexpr int C_BYTES = HN * BK / 2;   // 4 KB: this CTA's half of the codes
+    static constexpr int STAGE_BYTES = W_BYTES + 2 * A_BYTES + C_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int THREADS = 320;
+    static constexpr int GROUP_WARPS = 4;         // decode warps per group
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+// ---- cta_group::2 wrappers -------------------------------------------------
+__device__ __forceinline__ void tmem_alloc2(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the barrier at this shared-memory offset in every CTA of
+// the pair when all tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void tc_commit2_both(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)0x3)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t pair_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r & 1u;
+}
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster
+// address (possibly in the peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void pair_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Bounded wait like tc_wait; on running out it also raises the peer CTA's
+// abort flag (given by its shared::cluster address).
+__device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns, unsigned code,
+                                          volatile int *abort_flag, uint32_t peer_abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            record_error(code);
+            *abort_flag = 1;
+            st_cluster_u32(peer_abort, 1u);
+            return false;
+        }
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(PairCfg::THREADS, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
+                const __grid_constant__ CUtensorMap tm_lact, const __grid_constant__ CUtensorMap tm_lw,
+                const TcParams p) {
+    using C = PairCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t *full = bar;                       // this CTA's TMA bytes landed
+    uint64_t *ready = bar + C::STAGES;          // even CTA: both halves decoded (8 warp arrivals)
+    uint64_t *empty = bar + 2 * C::STAGES;      // stage consumed by the MMAs (commit from the even CTA)
+    uint64_t *accfull = bar + 3 * C::STAGES;    // accumulators complete (commit from the even CTA)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * C::STAGES + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    auto wtile = [&](int s) { return smem + s * C::STAGE_BYTES; };
+    auto atile = [&](int s, int h) { return smem + s * C::STAGE_BYTES + C::W_BYTES + h * C::A_BYTES; };
+    auto ctile = [&](int s) { return smem + s * C::STAGE_BYTES + C::W_BYTES + 2 * C::A_BYTES; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = pair_rank();
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t peer_abort = mapa_u32(smem_u32((const void *)abort_flag), peer);
+    const int64_t m0 = (int64_t)blockIdx.y * C::PAIR_M;
+    const int64_t c0 = (int64_t)(blockIdx.x >> 1) * C::BN;       // first output column of the pair
+    const int64_t ch = c0 + (int64_t)rank * C::HN;                // first of this CTA's 128 weight columns
+    const int64_t rowA0 = m0 + (int64_t)rank * C::SUB;            // this CTA's rows of sub-tile 0
+    const int64_t rowA1 = m0 + 256 + (int64_t)rank * C::SUB;      // and of sub-tile 1
+    const int z = (int)blockIdx.z;
+    const int64_t kbeg = (int64_t)z * p.steps_per_split;
+    const int64_t nmain = max((int64_t)0, min(p.steps_per_split, p.nk_main - kbeg));
+    const int64_t nk = nmain + (z == p.splits - 1 ? p.lora_steps : 0);
+    const bool two = m0 + 256 < p.M;  // sub-tile 1 has rows (same decision in both CTAs)
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&ready[s], 2 * C::GROUP_WARPS);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc2(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish2();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_codes);
+        prefetch_tmap(&tm_lact);
+        prefetch_tmap(&tm_lw);
+    }
+    tc_fence_before();
+    __syncthreads();
+    pair_sync();  // barriers of both CTAs initialised before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            const uint32_t abytes = (two ? 2 : 1) * C::A_BYTES;
+            int64_t issued = 0;
+            for (int64_t it = 0; it < nk; ++it) {
+                const int s = (int)(it % C::STAGES);
+                const uint32_t u = (uint32_t)(it / C::STAGES);
+                if (u > 0 && !pair_wait(&empty[s], (u - 1) & 1, p.wait_ns, (p.kernel_id << 16) | 1, abort_flag,
+                                        peer_abort))
+                    break;
+                if (it < nmain) {
+                    mbar_arrive_expect_tx(&full[s], abytes + C::C_BYTES);
+                    const int32_t k = (int32_t)((kbeg + it) * C::BK);
+                    tma_load_2d(atile(s, 0), &tm_act, &full[s], k, (int32_t)rowA0);
+                    if (two) tma_load_2d(atile(s, 1), &tm_act, &full[s], k, (int32_t)rowA1);
+                    if (MODE == kFwd)
+                        tma_load_2d(ctile(s), &tm_codes, &full[s], k / 2, (int32_t)ch);
+                    else
+                        tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(ch / 2), k);
+                } else {
+                    const int32_t j = (int32_t)(it - nmain) * C::BK;
+                    mbar_arrive_expect_tx(&full[s], abytes + C::W_BYTES);
+                    tma_load_2d(atile(s, 0), &tm_lact, &full[s], j, (int32_t)rowA0);
+                    if (two) tma_load_2d(atile(s, 1), &tm_lact, &full[s], j, (int32_t)rowA1);
+                    if (MODE == kFwd) {
+                        tma_load_2d(wtile(s), &tm_lw, &full[s], j, (int32_t)ch);
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < 2; ++b)
+                            tma_load_2d(wtile(s) + b * 8192, &tm_lw, &full[s], (int32_t)(ch + 64 * b), j);
+                    }
+                }
+                ++issued;
+            }
+            // drain: the last load issued into each stage must have landed
+            for (int s = 0; s < C::STAGES; ++s) {
+                if (issued <= s) break;
+                const int64_t last = issued - 1 - ((issued - 1 - s) % C::STAGES);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(&full[s], (uint32_t)(last / C::STAGES) & 1))
+                    if (globaltimer() - t0 > p.wait_ns) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------- MMA issuer (even CTA) ----
+        if (rank == 0 && lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(2 * C::SUB, C::BN, 0, MODE == kDx ? 1 : 0);
+            for (int64_t it = 0; it < nk; ++it) {
+                const int s = (int)(it % C::STAGES);
+                const uint32_t par = (uint32_t)(it / C::STAGES) & 1;
+                if (!pair_wait(&ready[s], par, p.wait_ns, (p.kernel_id << 16) | 4, abort_flag, peer_abort)) break;
+                tc_fence_after();
+                int nmma = 4;
+                if (it >= nmain) {
+                    const int rem = p.r - (int)(it - nmain) * C::BK;
+                    nmma = rem >= C::BK ? 4 : (rem + 15) / 16;
+                }
+                const uint32_t a0 = smem_u32(atile(s, 0)), a1 = smem_u32(atile(s, 1)), w0 = smem_u32(wtile(s));
+                for (int kk = 0; kk < nmma; ++kk) {
+                    const uint64_t bd = MODE == kFwd ? smem_desc_sw128(w0 + kk * 32, 16, 1024)
+                                                     : smem_desc_sw128(w0 + kk * 2048, 8192, 1024);
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma2_bf16(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), bd, idesc, acc);
+                    if (two) tc_mma2_bf16(tmem + 256, smem_desc_sw128(a1 + kk * 32, 16, 1024), bd, idesc, acc);
+                }
+                tc_commit2_both(&empty[s]);
+            }
+            tc_commit2_both(accfull);
+        }
+    } else {
+        // ---------------------- decode (alternate k-steps), then epilogue ----
+        const int dw = warp - 2;                    // 0..7
+        const int grp = dw / C::GROUP_WARPS;        // decode group: k-steps it % 2 == grp
+        const int dt = (dw % C::GROUP_WARPS) * 32 + lane;  // 0..127 within the group
+        const float mean = *p.mean;
+        const int64_t kblocks = p.w_cols / kBlock;
+        const uint32_t ready_addr0 = mapa_u32(smem_u32(ready), 0);
+        int64_t wrow0, kb0, wrow_step, kb_step;
+        int crow;
+        uint32_t dst[8], csrc[2];
+        if (MODE == kFwd) {
+            // W row ch + dt, block `it`; K-major 128-byte swizzled row dt
+            wrow0 = ch + dt;
+            wrow_step = 0;
+            kb0 = 0;
+            kb_step = 1;
+            crow = dt;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) dst[c] = (uint32_t)((dt >> 3) * 1024 + (dt & 7) * 128 + ((c ^ (dt & 7)) << 4));
+            // 32-byte code rows, 32-byte swizzle: half h sits at h ^ bit 2 of the row
+#pragma unroll
+            for (int h = 0; h < 2; ++h) csrc[h] = (uint32_t)(crow * 32 + ((h ^ ((crow >> 2) & 1)) << 4));
+        } else {
+            // W row it*64 + nl (a K-group row of the MN-major operand), column block b2
+            const int nlo = dt & 7, b2 = (dt >> 3) & 1, nhi = dt >> 4;
+            const int nl = nhi * 8 + nlo;
+            wrow0 = nl;
+            wrow_step = C::BK;
+            kb0 = ch / kBlock + b2;
+            kb_step = 0;
+            crow = nl;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) dst[c] = (uint32_t)(b2 * 8192 + nhi * 1024 + nlo * 128 + ((c ^ nlo) << 4));
+            // 64-byte code rows, 64-byte swizzle: 16-byte chunk q sits at q ^ ((row >> 1) & 3)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) csrc[h] = (uint32_t)(crow * 64 + (((b2 * 2 + h) ^ ((crow >> 1) & 3)) << 4));
+        }
+        auto fetch = [&](int64_t it, int &qv, float &sv) {
+            const int64_t g = kbeg + it;
+            const int64_t wrow = wrow0 + g * wrow_step, kb = kb0 + g * kb_step;
+            if (it < nmain && wrow < p.w_rows && kb < kblocks) {
+                const int64_t b = wrow * kblocks + kb;
+                qv = __ldg(p.q + b);
+                sv = __ldg(p.s2 + (b >> 8));
+                return true;
+            }
+            qv = 0;
+            sv = 0.0f;
+            return false;
+        };
+        int q_cur, q_nxt;
+        float s_cur, s_nxt;
+        bool v_cur = fetch(grp, q_cur, s_cur), v_nxt = false;
+        bool alive = true;
+        for (int64_t it = grp; it < nk && alive; it += 2) {
+            const int s = (int)(it % C::STAGES);
+            const uint32_t par = (uint32_t)(it / C::STAGES) & 1;
+            v_nxt = fetch(it + 2, q_nxt, s_nxt);
+            if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) {
+                alive = false;
+                break;
+            }
+            if (it < nmain) {
+                uint8_t *wt = wtile(s);
+                const uint8_t *ct = ctile(s);
+                uint32_t o[8][4];
+                if (v_cur) {
+                    const Nf4Table tab = make_table(dq_absmax((int8_t)q_cur, s_cur, mean));
+                    uint4 cw[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) cw[h] = *reinterpret_cast<const uint4 *>(ct + csrc[h]);
+                    const uint32_t w[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w, cw[1].x, cw[1].y, cw[1].z, cw[1].w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) decode8(tab, w[c], o[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0u;
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(wt + dst[c]) = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(ready_addr0 + (uint32_t)(s * 8));
+            q_cur = q_nxt;
+            s_cur = s_nxt;
+            v_cur = v_nxt;
+        }
+        // ------------------------------------------------------ epilogue
+        const bool acc_ok = pair_wait(accfull, 0, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag, peer_abort);
+        tc_fence_after();
+        const int quarter = warp & 3, sub = dw >> 2;
+        if (acc_ok && alive && (sub == 0 || two)) {
+            const int64_t row = (sub ? rowA1 : rowA0) + quarter * 32 + lane;
+#pragma unroll 1
+            for (int cc = 0; cc < C::BN / 32; ++cc) {
+                const int col = cc * 32;
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(sub * 256 + col), v);
+                tmem_ld_wait();
+                const int64_t ncol = p.Nd - (c0 + col);  // valid columns from here
+                if (row < p.M && p.splits > 1) {
+                    float *dstf = p.part + ((int64_t)z * p.M + row) * p.Nd + c0 + col;
+                    if (ncol >= 32 && ((p.Nd & 3) == 0)) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            reinterpret_cast<float4 *>(dstf)[g] =
+                                make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                            __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e < ncol) dstf[e] = __uint_as_float(v[e]);
+                    }
+                } else if (row < p.M) {
+                    uint16_t *dstp = p.out + row * p.ldo + c0 + col;
+                    if (ncol >= 32 && ((p.ldo & 7) == 0)) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            uint4 pk;
+                            pk.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
+                            pk.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+                            pk.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+                            pk.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+                            reinterpret_cast<uint4 *>(dstp)[g] = pk;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    pair_sync();  // both CTAs done with the MMAs' shared memory and TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc2(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace qlora

@@ -409,200 +409,4 @@ __global__ void k_split_reduce(const float *__restrict__ part, int splits, int64
     }
 }
 
-// ---------------------------------------------------------------------------
-// Skinny tcgen05 GEMM for the LoRA side path:
-//   part[chunk][row][j] = sum over the chunk's contraction range of
-//                         Aop[row, l] * Bop[j, l],   row < rows, j < 64
-// with Aop a 128-row tile and Bop 64 wide (the rank padded to 64 with zeros).
-// Each operand is loaded by TMA from a row-major array and is either
-// K-major (contraction index contiguous) or MN-major (row index contiguous):
-//   U  = X  A^T : A = X  [M, K]  K-major,  B = A' [64, K] K-major
-//   V  = dY B   : A = dY [M, N]  K-major,  B = B' [N, 64] MN-major
-//   dA^T = X^T (sV) : A = X [M, K] MN-major, B = sV [M, 64] MN-major
-//   dB   = dY^T U   : A = dY [M, N] MN-major, B = U' [M, 64] MN-major
-// The contraction is split into chunks (grid.y) for parallelism and ranks
-// above 64 use a second 64-wide column tile (grid.z); partial sums go to fp32
-// workspace [z][chunk][rows_pad][64] and a reduction kernel adds them in
-// chunk order.
-// ---------------------------------------------------------------------------
-struct SkCfg {
-    static constexpr int BM = 128, BN = 64, BK = 64, STAGES = 4;
-    static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-    static constexpr int B_BYTES = BN * BK * 2;  // 8 KB
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
-    static constexpr int THREADS = 192;
-    static constexpr uint32_t TMEM_COLS = 64;
-};
-
-struct SkParams {
-    int64_t rows;      // valid output rows
-    int64_t rows_pad;  // rows rounded up to 128 (partials row stride)
-    int64_t L;         // contraction length (multiple of 64 not required)
-    int64_t steps_per_chunk;
-    float *part;       // [chunks][rows_pad][64]
-    uint64_t wait_ns;
-    unsigned kernel_id;
-};
-
-template <int A_MN, int B_MN>
-__global__ void __launch_bounds__(SkCfg::THREADS, 1)
-    k_gemm_skinny(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                  const SkParams p) {
-    using C = SkCfg;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
-    uint64_t *full = bar, *empty = bar + C::STAGES, *accfull = bar + 2 * C::STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2 * C::STAGES + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    auto atile = [&](int s) { return smem + s * C::STAGE_BYTES; };
-    auto btile = [&](int s) { return smem + s * C::STAGE_BYTES + C::A_BYTES; };
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row0 = (int64_t)blockIdx.x * C::BM;
-    const int64_t l0 = (int64_t)blockIdx.y * p.steps_per_chunk * C::BK;
-    int64_t nsteps = (p.L - l0 + C::BK - 1) / C::BK;
-    if (nsteps > p.steps_per_chunk) nsteps = p.steps_per_chunk;
-    if (nsteps < 0) nsteps = 0;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(accfull, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        fence_proxy_async_smem();
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            int64_t issued = 0;
-            for (int64_t it = 0; it < nsteps; ++it) {
-                const int s = (int)(it % C::STAGES);
-                const uint32_t u = (uint32_t)(it / C::STAGES);
-                if (u > 0 && !tc_wait(&empty[s], (u - 1) & 1, p.wait_ns, (p.kernel_id << 16) | 1, abort_flag)) break;
-                const int32_t l = (int32_t)(l0 + it * C::BK);
-                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-                if (A_MN) {
-                    tma_load_2d(atile(s), &tm_a, &full[s], (int32_t)row0, l);
-                    tma_load_2d(atile(s) + 8192, &tm_a, &full[s], (int32_t)(row0 + 64), l);
-                } else {
-                    tma_load_2d(atile(s), &tm_a, &full[s], l, (int32_t)row0);
-                }
-                const int32_t jz = (int32_t)blockIdx.z * C::BN;
-                if (B_MN)
-                    tma_load_2d(btile(s), &tm_b, &full[s], jz, l);
-                else
-                    tma_load_2d(btile(s), &tm_b, &full[s], l, jz);
-                ++issued;
-            }
-            for (int s = 0; s < C::STAGES; ++s) {
-                if (issued <= s) break;
-                const int64_t last = issued - 1 - ((issued - 1 - s) % C::STAGES);
-                const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(&full[s], (uint32_t)(last / C::STAGES) & 1))
-                    if (globaltimer() - t0 > p.wait_ns) break;
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(C::BM, C::BN, A_MN, B_MN);
-            for (int64_t it = 0; it < nsteps; ++it) {
-                const int s = (int)(it % C::STAGES);
-                if (!tc_wait(&full[s], (uint32_t)(it / C::STAGES) & 1, p.wait_ns, (p.kernel_id << 16) | 3, abort_flag))
-                    break;
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(atile(s)), b0 = smem_u32(btile(s));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = A_MN ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
-                                             : smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                    const uint64_t bd = B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
-                                             : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                    tc_mma_bf16(tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(&empty[s]);
-            }
-            tc_commit(accfull);
-        }
-    } else {
-        // warps 2..5: epilogue, one TMEM lane (output row) per thread
-        const bool ok = tc_wait(accfull, 0, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag);
-        tc_fence_after();
-        const int quarter = warp & 3;
-        const int64_t row = row0 + quarter * 32 + lane;
-        float *dst = p.part + (((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * p.rows_pad + row) * C::BN;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(h * 32), v);
-            tmem_ld_wait();
-            if (ok && row < p.rows_pad) {
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    float4 f;
-                    f.x = nsteps > 0 ? __uint_as_float(v[4 * g + 0]) : 0.0f;
-                    f.y = nsteps > 0 ? __uint_as_float(v[4 * g + 1]) : 0.0f;
-                    f.z = nsteps > 0 ? __uint_as_float(v[4 * g + 2]) : 0.0f;
-                    f.w = nsteps > 0 ? __uint_as_float(v[4 * g + 3]) : 0.0f;
-                    reinterpret_cast<float4 *>(dst + h * 32)[g] = f;
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
-    }
-}
-
-// Sums the chunk partials in chunk order, then writes one of (rp = padded
-// rank, a multiple of 64; j runs over [0, rp)):
-//   kRedU:  U [rows, lda] bf16 = sum (j < r, if U != null),
-//           sU [rows, ldb] bf16 = s * sum (zero for j >= r)
-//   kRedV:  sV [rows, ldb] bf16 = s * sum (zero for j >= r)
-//   kRedDA: dA [r, rows] fp32 = sum  (element [j, row])
-//   kRedDB: dB [rows, r] fp32 = s * sum
-enum { kRedU = 0, kRedV = 1, kRedDA = 2, kRedDB = 3 };
-
-__global__ void k_skinny_reduce(const float *__restrict__ part, int nchunks, int64_t rows, int64_t rows_pad, int r,
-                                int rp, float s, int mode, uint16_t *__restrict__ o16a, int lda,
-                                uint16_t *__restrict__ o16b, int ldb, float *__restrict__ o32) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= rows * rp) return;
-    const int64_t row = i / rp;
-    const int jg = (int)(i % rp), z = jg >> 6, j = jg & 63;
-    float acc = 0.0f;
-    for (int c = 0; c < nchunks; ++c) acc += part[(((int64_t)z * nchunks + c) * rows_pad + row) * 64 + j];
-    if (jg >= r) acc = 0.0f;
-    switch (mode) {
-        case kRedU:
-            if (o16a && jg < r) o16a[row * lda + jg] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-            if (jg < ldb) o16b[row * ldb + jg] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, acc)));
-            break;
-        case kRedV:
-            if (jg < ldb) o16b[row * ldb + jg] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, acc)));
-            break;
-        case kRedDA:
-            if (jg < r) o32[(int64_t)jg * rows + row] = acc;
-            break;
-        default:
-            if (jg < r) o32[row * r + jg] = __fmul_rn(s, acc);
-            break;
-    }
-}
-
 }  // namespace qlora

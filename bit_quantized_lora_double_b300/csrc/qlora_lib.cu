@@ -15,6 +15,7 @@
 #include "codec.cuh"
 #include "lora_simt.cuh"
 #include "gemm_tc.cuh"
+#include "lora_tc.cuh"
 
 using namespace qlora;
 
@@ -126,32 +127,31 @@ size_t quantize_ws(int64_t rows, int64_t cols, float **absmax, double **gsum, do
 }
 
 // ---- linear workspaces
-// The LoRA operands of the tensor-core path are zero-padded to rp = 64 *
-// ceil(r / 64) columns so every TMA box lies inside its tensor.
+// Small-M (CUDA-core) path: the LoRA operands sU / sV / U are kept with rows
+// of rp = 64 * ceil(r / 64) columns.
 inline int lora_pad(int r) { return (int)up((size_t)r, 64); }
+// Tensor-core path: sU / sV / U rows of rs = 8 * ceil(r / 8) columns (16-byte
+// rows for TMA); the TMA zero fill supplies the rank padding up to 64.
+inline int lora_rs(int r) { return (int)up((size_t)r, 8); }
 
 // Tokens at or above which the tensor-core path runs.
 constexpr int64_t kTcMinM = 64;
 
-// Split of one skinny tcgen05 pass: output rows in 128-row tiles, rank in
-// 64-wide column tiles, contraction in chunks of steps_per_chunk x 64.
+// One skinny tcgen05 pass (k_lora_skinny): output rows in 128-row tiles,
+// rank in 64-wide tiles; the contraction is split into `chunks` (one cluster
+// per tile), chosen at launch (see skinny_chunks).
 struct SkPlan {
-    int64_t rows, rows_pad, L, spc, chunks;
+    int64_t rows, L, spc, chunks, tiles;
     int zt;
-    size_t part_floats;
 };
-SkPlan sk_plan(int64_t rows, int64_t L, int rp) {
+SkPlan sk_plan(int64_t rows, int64_t L, int r) {
     SkPlan p;
     p.rows = rows;
-    p.rows_pad = (int64_t)up((size_t)rows, 128);
+    p.tiles = cdiv(rows, 128);
     p.L = L;
-    p.zt = rp / 64;
-    const int64_t tiles = p.rows_pad / 128 * p.zt;
-    const int64_t steps = std::max<int64_t>(1, cdiv(L, 64));
-    const int64_t ch = std::min<int64_t>(steps, std::max<int64_t>(1, cdiv(2 * 148, tiles)));
-    p.spc = cdiv(steps, ch);
-    p.chunks = cdiv(steps, p.spc);
-    p.part_floats = (size_t)p.zt * p.chunks * p.rows_pad * 64;
+    p.zt = (r + 63) / 64;
+    p.spc = std::max<int64_t>(1, cdiv(L, 64));
+    p.chunks = 1;
     return p;
 }
 
@@ -170,23 +170,24 @@ GemmSplit gemm_split(int64_t M, int64_t Nd, int64_t nk_main) {
 }
 
 struct FwdWs {
-    uint16_t *sU, *Bp, *Ap;
+    uint16_t *sU, *Bp;
     float *part;
 };
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
-    const int rp = lora_pad(r);
     const bool tc = M >= kTcMinM;
     Carve c(ws);
-    uint16_t *sU = c.take<uint16_t>((size_t)M * rp);
-    uint16_t *Bp = c.take<uint16_t>(tc ? (size_t)N * rp : 0);
-    uint16_t *Ap = c.take<uint16_t>(tc ? (size_t)rp * K : 0);
-    size_t pf = 0;
-    if (tc) {
+    FwdWs f{};
+    if (!tc) {
+        f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
+        f.part = c.take<float>(0);
+    } else {
+        const int rs = lora_rs(r);
         const GemmSplit g = gemm_split(M, N, K / 64);
-        pf = std::max(sk_plan(M, K, rp).part_floats, g.splits > 1 ? (size_t)g.splits * M * N : (size_t)0);
+        f.sU = c.take<uint16_t>((size_t)M * rs);
+        f.Bp = c.take<uint16_t>(r % 8 ? (size_t)N * rs : 0);
+        f.part = c.take<float>(g.splits > 1 ? (size_t)g.splits * M * N : (size_t)0);
     }
-    float *part = c.take<float>(pf);
-    if (out) *out = FwdWs{sU, Bp, Ap, part};
+    if (out) *out = f;
     return c.off;
 }
 
@@ -205,30 +206,29 @@ GradSplit grad_split(int64_t M, int64_t C) {
 }
 
 struct BwdWs {
-    uint16_t *Bt, *sV, *U, *Bp, *Ap;
+    uint16_t *Bt, *sV, *U, *Bp;
     float *part;
 };
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, BwdWs *out) {
-    const int r8 = (int)up(r, 8), rp = lora_pad(r);
+    const int r8 = (int)up(r, 8), rp = lora_pad(r), rs = lora_rs(r);
     const bool tc = M >= kTcMinM && (N % 8) == 0;
-    size_t part;
-    if (tc) {
-        part = std::max(std::max(sk_plan(M, N, rp).part_floats, sk_plan(M, K, rp).part_floats),
-                        std::max(sk_plan(K, M, rp).part_floats, sk_plan(N, M, rp).part_floats));
-        const GemmSplit g = gemm_split(M, K, cdiv(N, 64));
-        if (g.splits > 1) part = std::max(part, (size_t)g.splits * M * K);
-    } else {
-        const GradSplit ga = grad_split(M, K), gb = grad_split(M, N);
-        part = (size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N);
-    }
     Carve c(ws);
-    uint16_t *Bt = c.take<uint16_t>(tc ? 0 : (size_t)r8 * N);
-    uint16_t *sV = c.take<uint16_t>((size_t)M * rp);
-    uint16_t *U = c.take<uint16_t>((size_t)M * rp);
-    uint16_t *Bp = c.take<uint16_t>(tc ? (size_t)N * rp : 0);
-    uint16_t *Ap = c.take<uint16_t>(tc ? (size_t)rp * K : 0);
-    float *p = c.take<float>(part);
-    if (out) *out = BwdWs{Bt, sV, U, Bp, Ap, p};
+    BwdWs b{};
+    if (!tc) {
+        const GradSplit ga = grad_split(M, K), gb = grad_split(M, N);
+        b.Bt = c.take<uint16_t>((size_t)r8 * N);
+        b.sV = c.take<uint16_t>((size_t)M * rp);
+        b.U = c.take<uint16_t>((size_t)M * rp);
+        b.part = c.take<float>((size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N));
+    } else {
+        const GemmSplit g = gemm_split(M, K, cdiv(N, 64));
+        const size_t part = g.splits > 1 ? (size_t)g.splits * M * K : 0;
+        b.sV = c.take<uint16_t>((size_t)M * rs);
+        b.U = c.take<uint16_t>((size_t)M * rs);
+        b.Bp = c.take<uint16_t>(r % 8 ? (size_t)N * rs : 0);
+        b.part = c.take<float>(part);
+    }
+    if (out) *out = b;
     return c.off;
 }
 
@@ -293,34 +293,123 @@ qlora_status tc_setup() {
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per bounded wait
 uint64_t wait_ns() { return g_wait_limit > 0 ? (uint64_t)g_wait_limit * 1000ull : kDefaultWaitNs; }
 
+// One skinny problem: its operand maps, split plan and output.
+struct SkJob {
+    const CUtensorMap *ta, *tb;
+    SkPlan pl;
+    int mode;
+    float scale;
+    uint16_t *o16a;
+    int lda;
+    uint16_t *o16b;
+    int ldb;
+    float *o32;
+};
+
+SkParams sk_params(const SkJob &j, int r, unsigned id) {
+    SkParams prm{};
+    prm.rows = j.pl.rows;
+    prm.L = j.pl.L;
+    prm.steps_per_chunk = j.pl.spc;
+    prm.nchunks = (int)j.pl.chunks;
+    prm.r = r;
+    prm.s = j.scale;
+    prm.mode = j.mode;
+    prm.o16a = j.o16a;
+    prm.lda = j.lda;
+    prm.o16b = j.o16b;
+    prm.ldb = j.ldb;
+    prm.o32 = j.o32;
+    prm.wait_ns = wait_ns();
+    prm.kernel_id = id;
+    return prm;
+}
+
+// Largest number of clusters of `c` CTAs of this kernel that the device
+// holds at once (cached per cluster size; 0 if the query fails).
 template <int A_MN, int B_MN>
-qlora_status run_skinny(const CUtensorMap &ta, const CUtensorMap &tb, const SkPlan &pl, float *part, cudaStream_t s,
-                        unsigned id) {
+int skinny_max_clusters(int c) {
+    static std::mutex mu;
+    static int cache[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    std::lock_guard<std::mutex> g(mu);
+    if (cache[c] < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, (unsigned)c, 1);
+        cfg.blockDim = dim3(SkCfg::THREADS);
+        cfg.dynamicSmemBytes = SkCfg::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)c;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_lora_skinny<A_MN, B_MN>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cache[c] = n;
+    }
+    return cache[c];
+}
+
+// Contraction chunks per tile: the largest cluster size (at most 8, and at
+// least 4 steps of 64 per chunk) for which every tile's cluster is resident
+// at once, so the launch runs as a single wave.
+template <int A_MN, int B_MN>
+int64_t skinny_chunks(int64_t clusters, int64_t steps) {
+    for (int64_t c = std::min<int64_t>(8, steps / 4); c > 1; --c)
+        if (skinny_max_clusters<A_MN, B_MN>((int)c) >= clusters) return c;
+    return 1;
+}
+
+// Launches one skinny problem, or two (j1 != null) of the same kind and
+// contraction length in one grid.
+template <int A_MN, int B_MN>
+qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsigned id) {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(k_gemm_skinny<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(k_lora_skinny<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    SkCfg::SMEM_BYTES);
     });
     if (err != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(err));
-    SkParams prm{pl.rows, pl.rows_pad, pl.L, pl.spc, part, wait_ns(), id};
-    dim3 grid((unsigned)(pl.rows_pad / 128), (unsigned)pl.chunks, (unsigned)pl.zt);
+    SkJob j1v = j1p ? *j1p : j0;
+    const SkJob *j1 = j1p ? &j1v : nullptr;
+    if (j1 && (j1->pl.L != j0.pl.L || j1->pl.zt != j0.pl.zt))
+        return fail(QLORA_ERR_CUDA, "internal: grouped skinny problems differ in contraction or rank");
+    const int64_t steps = std::max<int64_t>(1, cdiv(j0.pl.L, 64));
+    const int64_t ch0 = skinny_chunks<A_MN, B_MN>((j0.pl.tiles + (j1 ? j1->pl.tiles : 0)) * j0.pl.zt, steps);
+    j0.pl.spc = cdiv(steps, ch0);
+    j0.pl.chunks = cdiv(steps, j0.pl.spc);
+    j1v.pl.spc = j0.pl.spc;
+    j1v.pl.chunks = j0.pl.chunks;
+    const SkJob &jb = j1 ? *j1 : j0;
+    const SkParams p0 = sk_params(j0, r, id), p1 = sk_params(jb, r, id);
+    const int tiles0 = (int)j0.pl.tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(j0.pl.tiles + (j1 ? j1->pl.tiles : 0)), (unsigned)j0.pl.chunks, (unsigned)j0.pl.zt);
+    cfg.blockDim = dim3(SkCfg::THREADS);
+    cfg.dynamicSmemBytes = SkCfg::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)j0.pl.chunks;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = j0.pl.chunks > 1 ? 1 : 0;
+    cudaError_t e;
     {
-        ProfScope ps(id == 5 || id == 6 ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
-        k_gemm_skinny<A_MN, B_MN><<<grid, SkCfg::THREADS, SkCfg::SMEM_BYTES, s>>>(ta, tb, prm);
+        ProfScope ps(j0.mode >= kRedDA ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
+        e = cudaLaunchKernelEx(&cfg, k_lora_skinny<A_MN, B_MN>, *j0.ta, *j0.tb, *jb.ta, *jb.tb, p0, p1, tiles0);
     }
-    return launch_check("k_gemm_skinny");
-}
-
-qlora_status run_reduce(const SkPlan &pl, const float *part, int r, int rp, float scale, int mode, uint16_t *o16a,
-                        int lda, uint16_t *o16b, int ldb, float *o32, cudaStream_t s) {
-    {
-        ProfScope ps(mode >= kRedDA ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
-        k_skinny_reduce<<<(unsigned)cdiv(pl.rows * rp, 256), 256, 0, s>>>(part, (int)pl.chunks, pl.rows, pl.rows_pad,
-                                                                         r, rp, scale, mode, o16a, lda, o16b, ldb,
-                                                                         o32);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(QLORA_ERR_CUDA, "k_lora_skinny: launch failed: %s", cudaGetErrorString(e));
     }
-    return launch_check("k_skinny_reduce");
+    return launch_check("k_lora_skinny");
 }
 
 }  // namespace
@@ -557,32 +646,34 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     }
 
     if ((st = tc_device_ok()) || (st = tc_setup<kFwd>())) return st;
-    {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_pad_rows<<<(unsigned)cdiv(rp * K, 256), 256, 0, s>>>(static_cast<const uint16_t *>(A), r, rp, K, f.Ap);
+    const int rs = lora_rs(r);
+    // B as the LoRA tile of the GEMM: [N, r] directly when its rows are 16-byte
+    // multiples, else a copy with rows of rs (zero columns beyond r)
+    const void *Bl = B;
+    if (r % 8) {
+        {
+            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+            k_pad_cols<<<(unsigned)cdiv(N * rs, 256), 256, 0, s>>>(static_cast<const uint16_t *>(B), N, r, rs, f.Bp);
+        }
+        if ((st = launch_check("k_pad_cols(B)"))) return st;
+        Bl = f.Bp;
     }
-    if ((st = launch_check("k_pad_rows(A)"))) return st;
-    {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_pad_cols<<<(unsigned)cdiv(N * rp, 256), 256, 0, s>>>(static_cast<const uint16_t *>(B), N, r, rp, f.Bp);
-    }
-    if ((st = launch_check("k_pad_cols(B)"))) return st;
     CUtensorMap tmX, tmC, tmU, tmB, tmA;
     if ((st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
-        (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.Ap, K, rp, K * 2, 64, 64,
+        (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, r, K * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
         (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 32, 256,
                        CU_TENSOR_MAP_SWIZZLE_32B, "codes")) ||
-        (st = make_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rp, M, rp * 2, 64, 128,
+        (st = make_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rs, M, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "sU")) ||
-        (st = make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.Bp, rp, N, rp * 2, 64, 256,
+        (st = make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bl, rs, N, rs * 2, 64, 256,
                        CU_TENSOR_MAP_SWIZZLE_128B, "B")))
         return st;
     // U = X A^T on the tensor cores; U (bf16) to U_save, s*U (bf16) to the workspace
-    const SkPlan pu = sk_plan(M, K, rp);
-    if ((st = run_skinny<0, 0>(tmX, tmA, pu, f.part, s, 3))) return st;
-    if ((st = run_reduce(pu, f.part, r, rp, scale, kRedU, U16, r, f.sU, rp, nullptr, s))) return st;
+    const SkPlan pu = sk_plan(M, K, r);
+    if ((st = run_skinny<0, 0>(SkJob{&tmX, &tmA, pu, kRedU, scale, U16, r, f.sU, rs, nullptr}, nullptr, r, s, 3)))
+        return st;
     TcParams prm{};
     prm.M = M;
     prm.Nd = N;
@@ -706,17 +797,30 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     }
 
     if ((st = tc_device_ok()) || (st = tc_setup<kDx>())) return st;
-    {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_pad_cols<<<(unsigned)cdiv(N * rp, 256), 256, 0, s>>>(B16, N, r, rp, b.Bp);
+    const int rs = lora_rs(r);
+    // B [N, r] and U [M, r] are read by TMA directly when their rows are
+    // 16-byte multiples (r % 8 == 0), else from copies with rows of rs
+    const void *Bl = B16, *Ul = U_saved;
+    if (r % 8) {
+        {
+            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+            k_pad_cols<<<(unsigned)cdiv(N * rs, 256), 256, 0, s>>>(B16, N, r, rs, b.Bp);
+        }
+        if ((st = launch_check("k_pad_cols(B)"))) return st;
+        Bl = b.Bp;
+        if (U_saved) {
+            {
+                ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+                k_pad_cols<<<(unsigned)cdiv(M * rs, 256), 256, 0, s>>>(static_cast<const uint16_t *>(U_saved), M,
+                                                                      r, rs, b.U);
+            }
+            if ((st = launch_check("k_pad_cols(U)"))) return st;
+            Ul = b.U;
+        }
     }
-    if ((st = launch_check("k_pad_cols(B)"))) return st;
-    {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_pad_rows<<<(unsigned)cdiv(rp * K, 256), 256, 0, s>>>(A16, r, rp, K, b.Ap);
-    }
-    if ((st = launch_check("k_pad_rows(A)"))) return st;
-    CUtensorMap tmD, tmDmn, tmXk, tmXmn, tmC, tmV, tmA, tmBp, tmUp;
+    if (!U_saved) Ul = b.U;
+    const int ldb_l = r % 8 ? rs : r;
+    CUtensorMap tmD, tmDmn, tmXk, tmXmn, tmC, tmV, tmA, tmBp, tmUp, tmVmn;
     if ((st = make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, N, M, N * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "dY")) ||
         (st = make_map(&tmDmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, N, M, N * 2, 64, 64,
@@ -727,33 +831,33 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
                        CU_TENSOR_MAP_SWIZZLE_128B, "X (MN)")) ||
         (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "codes")) ||
-        (st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rp, M, rp * 2, 64, 128,
+        (st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rs, M, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "sV")) ||
-        (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.Ap, K, rp, K * 2, 64, 64,
+        (st = make_map(&tmVmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rs, M, rs * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "sV (MN)")) ||
+        (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A16, K, r, K * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
-        (st = make_map(&tmBp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.Bp, rp, N, rp * 2, 64, 64,
+        (st = make_map(&tmBp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bl, ldb_l, N, ldb_l * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "B")) ||
-        (st = make_map(&tmUp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.U, rp, M, rp * 2, 64, 64,
-                       CU_TENSOR_MAP_SWIZZLE_128B, "U")))
-        return st;
-    CUtensorMap tmVmn;
-    if ((st = make_map(&tmVmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rp, M, rp * 2, 64, 64,
-                       CU_TENSOR_MAP_SWIZZLE_128B, "sV (MN)")))
+        (st = make_map(&tmUp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ul, U_saved ? ldb_l : rs, M,
+                       (U_saved ? ldb_l : rs) * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "U")))
         return st;
     // V = dY B -> sV = bf16(s * V)
-    const SkPlan pv = sk_plan(M, N, rp);
-    if ((st = run_skinny<0, 1>(tmD, tmBp, pv, b.part, s, 4))) return st;
-    if ((st = run_reduce(pv, b.part, r, rp, scale, kRedV, nullptr, 0, b.sV, rp, nullptr, s))) return st;
-    // U (padded to rp columns): from the forward's U, or recomputed as X A^T
-    if (U_saved) {
-        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-        k_pad_cols<<<(unsigned)cdiv(M * rp, 256), 256, 0, s>>>(static_cast<const uint16_t *>(U_saved), M, r, rp, b.U);
-    } else {
-        const SkPlan pu = sk_plan(M, K, rp);
-        if ((st = run_skinny<0, 0>(tmXk, tmA, pu, b.part, s, 3))) return st;
-        if ((st = run_reduce(pu, b.part, r, rp, 1.0f, kRedU, nullptr, 0, b.U, rp, nullptr, s))) return st;
+    const SkPlan pv = sk_plan(M, N, r);
+    if ((st = run_skinny<0, 1>(SkJob{&tmD, &tmBp, pv, kRedV, scale, nullptr, 0, b.sV, rs, nullptr}, nullptr, r, s,
+                               4)))
+        return st;
+    // U recomputed as X A^T when the forward's U is not given
+    if (!U_saved) {
+        CUtensorMap tmAk;
+        if ((st = make_map(&tmAk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A16, K, r, K * 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "A")))
+            return st;
+        const SkPlan pu = sk_plan(M, K, r);
+        if ((st = run_skinny<0, 0>(SkJob{&tmXk, &tmAk, pu, kRedV, 1.0f, nullptr, 0, b.U, rs, nullptr}, nullptr, r,
+                                   s, 3)))
+            return st;
     }
-    if ((st = launch_check("U"))) return st;
     // dX = dY W' + (sV) A
     TcParams prm{};
     prm.M = M;
@@ -788,14 +892,11 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
         }
         if ((st = launch_check("k_split_reduce"))) return st;
     }
-    // dA = (sV)^T X   (rows k of dA^T, contraction over the M tokens)
-    const SkPlan pa = sk_plan(K, M, rp);
-    if ((st = run_skinny<1, 1>(tmXmn, tmVmn, pa, b.part, s, 5))) return st;
-    if ((st = run_reduce(pa, b.part, r, rp, 1.0f, kRedDA, nullptr, 0, nullptr, 0, dA, s))) return st;
-    // dB = s dY^T U
-    const SkPlan pb = sk_plan(N, M, rp);
-    if ((st = run_skinny<1, 1>(tmDmn, tmUp, pb, b.part, s, 6))) return st;
-    if ((st = run_reduce(pb, b.part, r, rp, scale, kRedDB, nullptr, 0, nullptr, 0, dB, s))) return st;
+    // dA = (sV)^T X (rows k of dA^T) and dB = s dY^T U (rows n), both
+    // contracting over the M tokens, in one launch
+    const SkJob ja{&tmXmn, &tmVmn, sk_plan(K, M, r), kRedDA, 1.0f, nullptr, 0, nullptr, 0, dA};
+    const SkJob jb{&tmDmn, &tmUp, sk_plan(N, M, r), kRedDB, scale, nullptr, 0, nullptr, 0, dB};
+    if ((st = run_skinny<1, 1>(ja, &jb, r, s, 5))) return st;
     return ok();
 }
 
