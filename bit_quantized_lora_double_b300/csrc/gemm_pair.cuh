@@ -12,7 +12,7 @@
 // 2 x 256 rows while each CTA decodes only its half of it: 128 x 64 weights
 // per 64-deep k-step against 2 x (128 x 256 x 64) MACs.
 //
-// Roles per CTA (10 warps):
+// Roles per CTA (18 warps):
 //   warp 0      TMA producer: two 128 x 64 activation tiles and this CTA's
 //               half of the packed-code tile per stage (in the LoRA steps
 //               the s*U or s*V tiles and this CTA's half of the adapter
@@ -20,11 +20,12 @@
 //   warp 1      TMEM allocation (both CTAs); in the even CTA one lane waits
 //               until both halves of a stage are decoded, issues the MMAs and
 //               commits to the stage's `empty` barriers of both CTAs.
-//   warps 2..9  two decode groups of 4 warps taking alternate k-steps: each
-//               thread expands one block of 64 codes through the per-block
-//               scaled byte-plane table into the UMMA operand layout, then
-//               arrives on the even CTA's `ready` barrier; after the last
-//               k-step all 8 warps read the accumulators and store bf16 rows.
+//   warps 2..17 four decode groups of 4 warps, group g taking the k-steps of
+//               stage g: each thread expands one block of 64 codes through
+//               the per-block scaled byte-plane table into the UMMA operand
+//               layout, then arrives on the even CTA's `ready` barrier; after
+//               the last k-step all 16 warps read the accumulators and store
+//               bf16 rows.
 // The LoRA term enters as ceil(r/64) extra k-steps into the same
 // accumulators. Every wait is bounded in time; a wait that runs out records
 // the error word, raises the abort flag in both CTAs, and the kernel drains
@@ -40,6 +41,7 @@
 
 namespace qlora {
 
+
 struct PairCfg {
     static constexpr int SUB = 128;               // rows per CTA per sub-tile
     static constexpr int PAIR_M = 512;            // rows per pair tile (2 sub-tiles x 256)
@@ -50,9 +52,12 @@ struct PairCfg {
     static constexpr int STAGE_BYTES = W_BYTES + 2 * A_BYTES + C_BYTES;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
-    static constexpr int THREADS = 320;
     static constexpr int GROUP_WARPS = 4;         // decode warps per group
+    static constexpr int DEC_GROUPS = 2;          // groups take alternate k-steps
+    static constexpr int EPI_WARPS = 8;           // two per TMEM lane quarter (column halves)
+    static constexpr int THREADS = 64 + 32 * (GROUP_WARPS * DEC_GROUPS + EPI_WARPS);
     static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int MAX_PAIRS = 74;
 };
 
 // ---- cta_group::2 wrappers -------------------------------------------------
@@ -107,6 +112,10 @@ __device__ __forceinline__ void pair_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch: wait for the preceding kernel's memory, and
+// let the next kernel start its own set-up.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // Bounded wait like tc_wait; on running out it also raises the peer CTA's
 // abort flag (given by its shared::cluster address).
 __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns, unsigned code,
@@ -127,6 +136,29 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// One work unit: a 512 x 256 output tile and one contraction split.
+struct PairUnit {
+    int64_t m0, c0, kbeg, nmain, nk;
+    int z;
+    bool two;
+};
+
+__device__ __forceinline__ PairUnit pair_unit(const TcParams &p, int64_t u, int64_t mt, int64_t nt) {
+    PairUnit w;
+    const int64_t t = u % (mt * nt);
+    w.z = (int)(u / (mt * nt));
+    w.m0 = (t % mt) * PairCfg::PAIR_M;
+    w.c0 = (t / mt) * PairCfg::BN;
+    w.kbeg = (int64_t)w.z * p.steps_per_split;
+    w.nmain = max((int64_t)0, min(p.steps_per_split, p.nk_main - w.kbeg));
+    w.nk = w.nmain + (w.z == p.splits - 1 ? p.lora_steps : 0);
+    w.two = w.m0 + 256 < p.M;
+    return w;
+}
+
+// Persistent kernel: pair q (q = blockIdx.x / 2) takes work units q, q + P,
+// q + 2P, ... (P = gridDim.x / 2); units run over the row tiles fastest, so
+// the pairs working at the same time share weight tiles through L2.
 template <int MODE>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
@@ -139,8 +171,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     uint64_t *full = bar;                       // this CTA's TMA bytes landed
     uint64_t *ready = bar + C::STAGES;          // even CTA: both halves decoded (8 warp arrivals)
     uint64_t *empty = bar + 2 * C::STAGES;      // stage consumed by the MMAs (commit from the even CTA)
-    uint64_t *accfull = bar + 3 * C::STAGES;    // accumulators complete (commit from the even CTA)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * C::STAGES + 1);
+    uint64_t *tfull = bar + 3 * C::STAGES;      // accumulators complete (commit from the even CTA)
+    uint64_t *tempty = bar + 3 * C::STAGES + 1; // even CTA: accumulators drained (8 warp arrivals)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * C::STAGES + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     auto wtile = [&](int s) { return smem + s * C::STAGE_BYTES; };
@@ -151,16 +184,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     const uint32_t rank = pair_rank();
     const uint32_t peer = rank ^ 1u;
     const uint32_t peer_abort = mapa_u32(smem_u32((const void *)abort_flag), peer);
-    const int64_t m0 = (int64_t)blockIdx.y * C::PAIR_M;
-    const int64_t c0 = (int64_t)(blockIdx.x >> 1) * C::BN;       // first output column of the pair
-    const int64_t ch = c0 + (int64_t)rank * C::HN;                // first of this CTA's 128 weight columns
-    const int64_t rowA0 = m0 + (int64_t)rank * C::SUB;            // this CTA's rows of sub-tile 0
-    const int64_t rowA1 = m0 + 256 + (int64_t)rank * C::SUB;      // and of sub-tile 1
-    const int z = (int)blockIdx.z;
-    const int64_t kbeg = (int64_t)z * p.steps_per_split;
-    const int64_t nmain = max((int64_t)0, min(p.steps_per_split, p.nk_main - kbeg));
-    const int64_t nk = nmain + (z == p.splits - 1 ? p.lora_steps : 0);
-    const bool two = m0 + 256 < p.M;  // sub-tile 1 has rows (same decision in both CTAs)
+    const int64_t mt = (p.M + C::PAIR_M - 1) / C::PAIR_M, nt = (p.Nd + C::BN - 1) / C::BN;
+    const int64_t units = mt * nt * p.splits;
+    const int64_t npairs = gridDim.x >> 1, pair_id = blockIdx.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -168,7 +194,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             mbar_init(&ready[s], 2 * C::GROUP_WARPS);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accfull, 1);
+        mbar_init(tfull, 1);
+        mbar_init(tempty, 2 * C::EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -188,46 +215,55 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     pair_sync();  // barriers of both CTAs initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();     // inputs written by the preceding kernel are visible from here on
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
-            const uint32_t abytes = (two ? 2 : 1) * C::A_BYTES;
-            int64_t issued = 0;
-            for (int64_t it = 0; it < nk; ++it) {
-                const int s = (int)(it % C::STAGES);
-                const uint32_t u = (uint32_t)(it / C::STAGES);
-                if (u > 0 && !pair_wait(&empty[s], (u - 1) & 1, p.wait_ns, (p.kernel_id << 16) | 1, abort_flag,
-                                        peer_abort))
-                    break;
-                if (it < nmain) {
-                    mbar_arrive_expect_tx(&full[s], abytes + C::C_BYTES);
-                    const int32_t k = (int32_t)((kbeg + it) * C::BK);
-                    tma_load_2d(atile(s, 0), &tm_act, &full[s], k, (int32_t)rowA0);
-                    if (two) tma_load_2d(atile(s, 1), &tm_act, &full[s], k, (int32_t)rowA1);
-                    if (MODE == kFwd)
-                        tma_load_2d(ctile(s), &tm_codes, &full[s], k / 2, (int32_t)ch);
-                    else
-                        tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(ch / 2), k);
-                } else {
-                    const int32_t j = (int32_t)(it - nmain) * C::BK;
-                    mbar_arrive_expect_tx(&full[s], abytes + C::W_BYTES);
-                    tma_load_2d(atile(s, 0), &tm_lact, &full[s], j, (int32_t)rowA0);
-                    if (two) tma_load_2d(atile(s, 1), &tm_lact, &full[s], j, (int32_t)rowA1);
-                    if (MODE == kFwd) {
-                        tma_load_2d(wtile(s), &tm_lw, &full[s], j, (int32_t)ch);
+            int64_t g = 0;
+            bool alive = true;
+            for (int64_t u = pair_id; u < units && alive; u += npairs) {
+                const PairUnit w = pair_unit(p, u, mt, nt);
+                const int64_t rowA0 = w.m0 + (int64_t)rank * C::SUB, rowA1 = rowA0 + 256;
+                const int64_t ch = w.c0 + (int64_t)rank * C::HN;
+                const uint32_t abytes = (w.two ? 2 : 1) * C::A_BYTES;
+                for (int64_t it = 0; it < w.nk; ++it, ++g) {
+                    const int s = (int)(g % C::STAGES);
+                    const uint32_t ph = (uint32_t)(g / C::STAGES);
+                    if (ph > 0 && !pair_wait(&empty[s], (ph - 1) & 1, p.wait_ns, (p.kernel_id << 16) | 1, abort_flag,
+                                             peer_abort)) {
+                        alive = false;
+                        break;
+                    }
+                    if (it < w.nmain) {
+                        mbar_arrive_expect_tx(&full[s], abytes + C::C_BYTES);
+                        const int32_t k = (int32_t)((w.kbeg + it) * C::BK);
+                        tma_load_2d(atile(s, 0), &tm_act, &full[s], k, (int32_t)rowA0);
+                        if (w.two) tma_load_2d(atile(s, 1), &tm_act, &full[s], k, (int32_t)rowA1);
+                        if (MODE == kFwd)
+                            tma_load_2d(ctile(s), &tm_codes, &full[s], k / 2, (int32_t)ch);
+                        else
+                            tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(ch / 2), k);
                     } else {
+                        const int32_t j = (int32_t)(it - w.nmain) * C::BK;
+                        mbar_arrive_expect_tx(&full[s], abytes + C::W_BYTES);
+                        tma_load_2d(atile(s, 0), &tm_lact, &full[s], j, (int32_t)rowA0);
+                        if (w.two) tma_load_2d(atile(s, 1), &tm_lact, &full[s], j, (int32_t)rowA1);
+                        if (MODE == kFwd) {
+                            tma_load_2d(wtile(s), &tm_lw, &full[s], j, (int32_t)ch);
+                        } else {
 #pragma unroll
-                        for (int b = 0; b < 2; ++b)
-                            tma_load_2d(wtile(s) + b * 8192, &tm_lw, &full[s], (int32_t)(ch + 64 * b), j);
+                            for (int b = 0; b < 2; ++b)
+                                tma_load_2d(wtile(s) + b * 8192, &tm_lw, &full[s], (int32_t)(ch + 64 * b), j);
+                        }
                     }
                 }
-                ++issued;
             }
             // drain: the last load issued into each stage must have landed
             for (int s = 0; s < C::STAGES; ++s) {
-                if (issued <= s) break;
-                const int64_t last = issued - 1 - ((issued - 1 - s) % C::STAGES);
+                if (g <= s) break;
+                const int64_t last = g - 1 - ((g - 1 - s) % C::STAGES);
                 const uint64_t t0 = globaltimer();
                 while (!mbar_try_wait(&full[s], (uint32_t)(last / C::STAGES) & 1))
                     if (globaltimer() - t0 > p.wait_ns) break;
@@ -237,160 +273,189 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         // ------------------------------------- MMA issuer (even CTA) ----
         if (rank == 0 && lane == 0) {
             constexpr uint32_t idesc = idesc_bf16(2 * C::SUB, C::BN, 0, MODE == kDx ? 1 : 0);
-            for (int64_t it = 0; it < nk; ++it) {
-                const int s = (int)(it % C::STAGES);
-                const uint32_t par = (uint32_t)(it / C::STAGES) & 1;
-                if (!pair_wait(&ready[s], par, p.wait_ns, (p.kernel_id << 16) | 4, abort_flag, peer_abort)) break;
+            int64_t g = 0, tl = 0;
+            bool alive = true;
+            for (int64_t u = pair_id; u < units && alive; u += npairs, ++tl) {
+                const PairUnit w = pair_unit(p, u, mt, nt);
+                if (tl > 0 && !pair_wait(tempty, (uint32_t)(tl - 1) & 1, p.wait_ns, (p.kernel_id << 16) | 6,
+                                         abort_flag, peer_abort))
+                    break;
                 tc_fence_after();
-                int nmma = 4;
-                if (it >= nmain) {
-                    const int rem = p.r - (int)(it - nmain) * C::BK;
-                    nmma = rem >= C::BK ? 4 : (rem + 15) / 16;
+                for (int64_t it = 0; it < w.nk; ++it, ++g) {
+                    const int s = (int)(g % C::STAGES);
+                    const uint32_t par = (uint32_t)(g / C::STAGES) & 1;
+                    if (!pair_wait(&ready[s], par, p.wait_ns, (p.kernel_id << 16) | 4, abort_flag, peer_abort)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    int nmma = 4;
+                    if (it >= w.nmain) {
+                        const int rem = p.r - (int)(it - w.nmain) * C::BK;
+                        nmma = rem >= C::BK ? 4 : (rem + 15) / 16;
+                    }
+                    const uint32_t a0 = smem_u32(atile(s, 0)), a1 = smem_u32(atile(s, 1)), w0 = smem_u32(wtile(s));
+                    for (int kk = 0; kk < nmma; ++kk) {
+                        const uint64_t bd = MODE == kFwd ? smem_desc_sw128(w0 + kk * 32, 16, 1024)
+                                                         : smem_desc_sw128(w0 + kk * 2048, 8192, 1024);
+                        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                        tc_mma2_bf16(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), bd, idesc, acc);
+                        if (w.two) tc_mma2_bf16(tmem + 256, smem_desc_sw128(a1 + kk * 32, 16, 1024), bd, idesc, acc);
+                    }
+                    tc_commit2_both(&empty[s]);
                 }
-                const uint32_t a0 = smem_u32(atile(s, 0)), a1 = smem_u32(atile(s, 1)), w0 = smem_u32(wtile(s));
-                for (int kk = 0; kk < nmma; ++kk) {
-                    const uint64_t bd = MODE == kFwd ? smem_desc_sw128(w0 + kk * 32, 16, 1024)
-                                                     : smem_desc_sw128(w0 + kk * 2048, 8192, 1024);
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    tc_mma2_bf16(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), bd, idesc, acc);
-                    if (two) tc_mma2_bf16(tmem + 256, smem_desc_sw128(a1 + kk * 32, 16, 1024), bd, idesc, acc);
-                }
-                tc_commit2_both(&empty[s]);
+                tc_commit2_both(tfull);
             }
-            tc_commit2_both(accfull);
         }
-    } else {
-        // ---------------------- decode (alternate k-steps), then epilogue ----
-        const int dw = warp - 2;                    // 0..7
-        const int grp = dw / C::GROUP_WARPS;        // decode group: k-steps it % 2 == grp
+    } else if (warp < 2 + C::GROUP_WARPS * C::DEC_GROUPS) {
+        // ------------------------------ decode groups (alternate k-steps) ----
+        const int dw = warp - 2;
+        const int grp = dw / C::GROUP_WARPS;
         const int dt = (dw % C::GROUP_WARPS) * 32 + lane;  // 0..127 within the group
         const float mean = *p.mean;
         const int64_t kblocks = p.w_cols / kBlock;
         const uint32_t ready_addr0 = mapa_u32(smem_u32(ready), 0);
-        int64_t wrow0, kb0, wrow_step, kb_step;
-        int crow;
         uint32_t dst[8], csrc[2];
+        int b2 = 0, nl = 0;
         if (MODE == kFwd) {
-            // W row ch + dt, block `it`; K-major 128-byte swizzled row dt
-            wrow0 = ch + dt;
-            wrow_step = 0;
-            kb0 = 0;
-            kb_step = 1;
-            crow = dt;
+            // row dt of the K-major, 128-byte swizzled W' half-tile
 #pragma unroll
             for (int c = 0; c < 8; ++c) dst[c] = (uint32_t)((dt >> 3) * 1024 + (dt & 7) * 128 + ((c ^ (dt & 7)) << 4));
             // 32-byte code rows, 32-byte swizzle: half h sits at h ^ bit 2 of the row
 #pragma unroll
-            for (int h = 0; h < 2; ++h) csrc[h] = (uint32_t)(crow * 32 + ((h ^ ((crow >> 2) & 1)) << 4));
+            for (int h = 0; h < 2; ++h) csrc[h] = (uint32_t)(dt * 32 + ((h ^ ((dt >> 2) & 1)) << 4));
         } else {
             // W row it*64 + nl (a K-group row of the MN-major operand), column block b2
-            const int nlo = dt & 7, b2 = (dt >> 3) & 1, nhi = dt >> 4;
-            const int nl = nhi * 8 + nlo;
-            wrow0 = nl;
-            wrow_step = C::BK;
-            kb0 = ch / kBlock + b2;
-            kb_step = 0;
-            crow = nl;
+            const int nlo = dt & 7, nhi = dt >> 4;
+            b2 = (dt >> 3) & 1;
+            nl = nhi * 8 + nlo;
 #pragma unroll
             for (int c = 0; c < 8; ++c) dst[c] = (uint32_t)(b2 * 8192 + nhi * 1024 + nlo * 128 + ((c ^ nlo) << 4));
             // 64-byte code rows, 64-byte swizzle: 16-byte chunk q sits at q ^ ((row >> 1) & 3)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) csrc[h] = (uint32_t)(crow * 64 + (((b2 * 2 + h) ^ ((crow >> 1) & 3)) << 4));
+            for (int h = 0; h < 2; ++h) csrc[h] = (uint32_t)(nl * 64 + (((b2 * 2 + h) ^ ((nl >> 1) & 3)) << 4));
         }
-        auto fetch = [&](int64_t it, int &qv, float &sv) {
-            const int64_t g = kbeg + it;
-            const int64_t wrow = wrow0 + g * wrow_step, kb = kb0 + g * kb_step;
-            if (it < nmain && wrow < p.w_rows && kb < kblocks) {
-                const int64_t b = wrow * kblocks + kb;
-                qv = __ldg(p.q + b);
-                sv = __ldg(p.s2 + (b >> 8));
-                return true;
-            }
-            qv = 0;
-            sv = 0.0f;
-            return false;
-        };
-        int q_cur, q_nxt;
-        float s_cur, s_nxt;
-        bool v_cur = fetch(grp, q_cur, s_cur), v_nxt = false;
+        int64_t g = 0;
         bool alive = true;
-        for (int64_t it = grp; it < nk && alive; it += 2) {
-            const int s = (int)(it % C::STAGES);
-            const uint32_t par = (uint32_t)(it / C::STAGES) & 1;
-            v_nxt = fetch(it + 2, q_nxt, s_nxt);
-            if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) {
-                alive = false;
-                break;
-            }
-            if (it < nmain) {
-                uint8_t *wt = wtile(s);
-                const uint8_t *ct = ctile(s);
-                uint32_t o[8][4];
-                if (v_cur) {
-                    const Nf4Table tab = make_table(dq_absmax((int8_t)q_cur, s_cur, mean));
-                    uint4 cw[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) cw[h] = *reinterpret_cast<const uint4 *>(ct + csrc[h]);
-                    const uint32_t w[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w, cw[1].x, cw[1].y, cw[1].z, cw[1].w};
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) decode8(tab, w[c], o[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0u;
+        for (int64_t u = pair_id; u < units && alive; u += npairs) {
+            const PairUnit w = pair_unit(p, u, mt, nt);
+            const int64_t ch = w.c0 + (int64_t)rank * C::HN;
+            for (int64_t it = 0; it < w.nk; ++it, ++g) {
+                if ((int)(g % C::DEC_GROUPS) != grp) continue;
+                const int s = (int)(g % C::STAGES);
+                const uint32_t par = (uint32_t)(g / C::STAGES) & 1;
+                // this thread's block: forward W row ch + dt, k-block kbeg + it;
+                // dX W row (kbeg + it) * 64 + nl, k-block ch / 64 + b2
+                int qv = 0;
+                float sv = 0.0f;
+                bool valid = false;
+                if (it < w.nmain) {
+                    const int64_t wrow = MODE == kFwd ? ch + dt : (w.kbeg + it) * C::BK + nl;
+                    const int64_t kb = MODE == kFwd ? w.kbeg + it : ch / kBlock + b2;
+                    if (wrow < p.w_rows && kb < kblocks) {
+                        const int64_t b = wrow * kblocks + kb;
+                        qv = __ldg(p.q + b);
+                        sv = __ldg(p.s2 + (b >> 8));
+                        valid = true;
+                    }
                 }
+                if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) {
+                    alive = false;
+                    break;
+                }
+                if (it < w.nmain) {
+                    uint8_t *wt = wtile(s);
+                    const uint8_t *ct = ctile(s);
+                    uint32_t o[8][4];
+                    if (valid) {
+                        const Nf4Table tab = make_table(dq_absmax((int8_t)qv, sv, mean));
+                        uint4 cw[2];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(wt + dst[c]) = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
-                fence_proxy_async_smem();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(ready_addr0 + (uint32_t)(s * 8));
-            q_cur = q_nxt;
-            s_cur = s_nxt;
-            v_cur = v_nxt;
-        }
-        // ------------------------------------------------------ epilogue
-        const bool acc_ok = pair_wait(accfull, 0, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag, peer_abort);
-        tc_fence_after();
-        const int quarter = warp & 3, sub = dw >> 2;
-        if (acc_ok && alive && (sub == 0 || two)) {
-            const int64_t row = (sub ? rowA1 : rowA0) + quarter * 32 + lane;
-#pragma unroll 1
-            for (int cc = 0; cc < C::BN / 32; ++cc) {
-                const int col = cc * 32;
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(sub * 256 + col), v);
-                tmem_ld_wait();
-                const int64_t ncol = p.Nd - (c0 + col);  // valid columns from here
-                if (row < p.M && p.splits > 1) {
-                    float *dstf = p.part + ((int64_t)z * p.M + row) * p.Nd + c0 + col;
-                    if (ncol >= 32 && ((p.Nd & 3) == 0)) {
+                        for (int h = 0; h < 2; ++h) cw[h] = *reinterpret_cast<const uint4 *>(ct + csrc[h]);
+                        const uint32_t wv[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w, cw[1].x, cw[1].y, cw[1].z, cw[1].w};
 #pragma unroll
-                        for (int g = 0; g < 8; ++g)
-                            reinterpret_cast<float4 *>(dstf)[g] =
-                                make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                            __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+                        for (int c = 0; c < 8; ++c) decode8(tab, wv[c], o[c]);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (e < ncol) dstf[e] = __uint_as_float(v[e]);
+                        for (int c = 0; c < 8; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0u;
                     }
-                } else if (row < p.M) {
-                    uint16_t *dstp = p.out + row * p.ldo + c0 + col;
-                    if (ncol >= 32 && ((p.ldo & 7) == 0)) {
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            uint4 pk;
-                            pk.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
-                            pk.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
-                            pk.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
-                            pk.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
-                            reinterpret_cast<uint4 *>(dstp)[g] = pk;
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(wt + dst[c]) = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(ready_addr0 + (uint32_t)(s * 8));
+            }
+        }
+    } else {
+        // --------------------------------------------------- epilogue ----
+        // Warp e of the 8 reads TMEM lanes 32 * (warp % 4) .. + 31 (one row of
+        // each 128-row sub-tile per thread) and the accumulator columns of
+        // its half, chalf = e / 4 (128 of the 256), 64 columns per wait. The
+        // accumulators are released to the next unit's MMAs right after the
+        // last read; the stores (one 128-byte row segment per thread and
+        // batch) drain while the next unit runs.
+        const int ew = warp - (2 + C::GROUP_WARPS * C::DEC_GROUPS);  // 0..7
+        const int quarter = warp & 3, chalf = ew >> 2;
+        const int r = quarter * 32 + lane;  // row within the sub-tile
+        const uint32_t tempty_addr0 = mapa_u32(smem_u32(tempty), 0);
+        int64_t tl = 0;
+        for (int64_t u = pair_id; u < units; u += npairs, ++tl) {
+            const PairUnit w = pair_unit(p, u, mt, nt);
+            if (!pair_wait(tfull, (uint32_t)tl & 1, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag, peer_abort))
+                break;
+            tc_fence_after();
+            for (int sub = 0; sub < 2; ++sub) {
+                if (sub == 1 && !w.two) break;
+                const int64_t row = w.m0 + sub * 256 + (int64_t)rank * C::SUB + r;
+#pragma unroll 1
+                for (int cp = 0; cp < 2; ++cp) {
+                    const int col = chalf * 128 + cp * 64;
+                    uint32_t v[64];
+                    const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(sub * 256 + col);
+                    tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                    tmem_ld_wait();
+                    if (sub == (w.two ? 1 : 0) && cp == 1) {
+                        // every accumulator column this warp owns has been read:
+                        // the MMAs of the next unit may overwrite them
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(tempty_addr0);
+                    }
+                    if (row >= p.M) continue;
+                    const int64_t ncol = p.Nd - (w.c0 + col);  // valid columns from here
+                    if (p.splits > 1) {
+                        float *dstf = p.part + ((int64_t)w.z * p.M + row) * p.Nd + w.c0 + col;
+                        if (ncol >= 64 && ((p.Nd & 3) == 0)) {
+#pragma unroll
+                            for (int g4 = 0; g4 < 16; ++g4)
+                                reinterpret_cast<float4 *>(dstf)[g4] =
+                                    make_float4(__uint_as_float(v[4 * g4]), __uint_as_float(v[4 * g4 + 1]),
+                                                __uint_as_float(v[4 * g4 + 2]), __uint_as_float(v[4 * g4 + 3]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e)
+                                if (e < ncol) dstf[e] = __uint_as_float(v[e]);
                         }
                     } else {
+                        uint16_t *dstp = p.out + row * p.ldo + w.c0 + col;
+                        if (ncol >= 64 && (p.ldo & 7) == 0) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
+                            for (int q = 0; q < 8; ++q) {
+                                uint4 pk;
+                                pk.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                                pk.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                                pk.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                                pk.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                                reinterpret_cast<uint4 *>(dstp)[q] = pk;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e)
+                                if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
+                        }
                     }
                 }
             }
