@@ -77,6 +77,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or about `hint_ns` nanoseconds pass, so that waiting warps do not
+// take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kWaitHintNs = 20000;
+
 // Bounded wait: spins at most `limit` times on try_wait (each try_wait itself
 // suspends for a hardware-defined interval). On running out it records
 // `code` in the device error word and returns false; the caller then stops
@@ -84,7 +100,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int64_t limit,
                                                   unsigned int code) {
     for (int64_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
     record_error(code);
     return false;
 }

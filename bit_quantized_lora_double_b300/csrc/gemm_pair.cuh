@@ -124,8 +124,8 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64
     const uint64_t t0 = globaltimer();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 4; ++i)
+            if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > limit_ns) {
             record_error(code);

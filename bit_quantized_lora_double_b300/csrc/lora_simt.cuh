@@ -24,63 +24,47 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// U[m, j] = sum_k P[m, k] Q[j, k] (fp32), j < r. One warp per 2 rows m,
-// 16 values of j per pass; lanes stride over K in 8-element chunks.
-// Writes U (bf16, stride ldu, may be null) and sU = bf16(s * U) (stride lds,
-// zero for r <= j < lds).
+// U[m, j] = sum_k P[m, k] Q[j, k] (fp32) for j < r: one warp per output
+// (m, j), lanes striding over K in 8-element (16-byte) chunks, then a warp
+// reduction. Writes U (bf16, stride ldu, may be null) and sU = bf16(s * U)
+// (stride lds); the warps of the outputs (m, j) with r <= j < lds write the
+// zero padding of sU.
 __global__ void __launch_bounds__(256) k_lora_down(const uint16_t *__restrict__ P, int64_t M, int64_t K,
                                                    const uint16_t *__restrict__ Q, int r, float s,
                                                    uint16_t *__restrict__ U, int ldu, uint16_t *__restrict__ sU,
                                                    int lds) {
     const int lane = threadIdx.x & 31;
-    const int64_t m0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * 2;
-    if (m0 >= M) return;
-    const bool has1 = m0 + 1 < M;
-    const int64_t nch = K / 8;
-    for (int j0 = 0; j0 < r; j0 += 16) {
-        float acc0[16], acc1[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc0[j] = acc1[j] = 0.0f;
-        for (int64_t c = lane; c < nch; c += 32) {
-            const uint4 x0 = reinterpret_cast<const uint4 *>(P + m0 * K)[c];
-            const uint4 x1 = has1 ? reinterpret_cast<const uint4 *>(P + (m0 + 1) * K)[c] : make_uint4(0, 0, 0, 0);
-            const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (j0 + j < r) {
-                    const uint4 qv = reinterpret_cast<const uint4 *>(Q + (int64_t)(j0 + j) * K)[c];
-                    const uint32_t b[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float bl = bf16lo_to_f32(b[e]), bh = bf16hi_to_f32(b[e]);
-                        acc0[j] = fmaf(bf16lo_to_f32(a0[e]), bl, acc0[j]);
-                        acc0[j] = fmaf(bf16hi_to_f32(a0[e]), bh, acc0[j]);
-                        acc1[j] = fmaf(bf16lo_to_f32(a1[e]), bl, acc1[j]);
-                        acc1[j] = fmaf(bf16hi_to_f32(a1[e]), bh, acc1[j]);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float u0 = warp_sum(acc0[j]), u1 = warp_sum(acc1[j]);
-            if (lane == j) {
-                const int jj = j0 + j;
-                if (jj < r) {
-                    if (U) {
-                        U[m0 * ldu + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(u0));
-                        if (has1) U[(m0 + 1) * ldu + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(u1));
-                    }
-                    sU[m0 * lds + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, u0)));
-                    if (has1) sU[(m0 + 1) * lds + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, u1)));
-                }
-            }
-        }
+    const int64_t o = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (o >= M * lds) return;
+    const int64_t m = o / lds;
+    const int j = (int)(o % lds);
+    if (j >= r) {
+        if (lane == 0) sU[m * lds + j] = 0;
+        return;
     }
-    // zero the padding columns of sU
-    for (int jj = r + lane; jj < lds; jj += 32) {
-        sU[m0 * lds + jj] = 0;
-        if (has1) sU[(m0 + 1) * lds + jj] = 0;
+    float acc = 0.0f;
+    if ((K & 7) == 0) {
+        // rows are 16-byte aligned (the arrays are): 8 elements per load
+        const uint4 *pr = reinterpret_cast<const uint4 *>(P + m * K);
+        const uint4 *qr = reinterpret_cast<const uint4 *>(Q + (int64_t)j * K);
+#pragma unroll 4
+        for (int64_t c = lane; c < K / 8; c += 32) {
+            const uint4 x = __ldg(pr + c), a = __ldg(qr + c);
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, as[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc = fmaf(bf16lo_to_f32(xs[e]), bf16lo_to_f32(as[e]), acc);
+                acc = fmaf(bf16hi_to_f32(xs[e]), bf16hi_to_f32(as[e]), acc);
+            }
+        }
+    } else {
+        for (int64_t c = lane; c < K; c += 32)
+            acc = fmaf(bf16lo_to_f32(P[m * K + c]), bf16lo_to_f32(Q[(int64_t)j * K + c]), acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) {
+        if (U) U[m * ldu + j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+        sU[m * lds + j] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, acc)));
     }
 }
 

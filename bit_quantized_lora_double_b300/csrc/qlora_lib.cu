@@ -17,6 +17,7 @@
 #include "gemm_tc.cuh"
 #include "gemm_pair.cuh"
 #include "lora_tc.cuh"
+#include "small_m.cuh"
 
 using namespace qlora;
 
@@ -184,7 +185,7 @@ struct FwdWs {
     float *part;
 };
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
-    const bool tc = M >= kTcMinM;
+    const bool tc = M > kSmallMaxM || K > kSmallMaxK;
     Carve c(ws);
     FwdWs f{};
     if (!tc) {
@@ -707,22 +708,29 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     const uint16_t *X16 = static_cast<const uint16_t *>(X);
     uint16_t *U16 = static_cast<uint16_t *>(U_save);
 
-    if (M < kTcMinM) {
-        // small M: CUDA-core kernels
+    if (M <= kSmallMaxM && K <= kSmallMaxK) {
+        // few tokens: HBM-bound path (mma.sync over the decoded weight rows)
+        if ((st = tc_device_ok())) return st;
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
+            k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
                                                               U16, r, f.sU, rp);
         }
         if ((st = launch_check("k_lora_down"))) return st;
-        dim3 grid((unsigned)cdiv(N, kSt), (unsigned)cdiv(M, kSt));
+        CUtensorMap tmC;
+        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, SmallCfg::ROWS,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "codes")))
+            return st;
+        const unsigned grid = (unsigned)cdiv(N, SmallCfg::ROWS);
+        const int nt = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
         {
             ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
-            k_fwd_simt<<<grid, 256, 0, s>>>(X16, M, K, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, N,
-                                            f.sU, rp, static_cast<const uint16_t *>(B), r,
-                                            static_cast<uint16_t *>(Y));
+            auto kern = nt == 1 ? k_fwd_small<1> : (nt == 2 ? k_fwd_small<2> : k_fwd_small<4>);
+            kern<<<grid, SmallCfg::THREADS, 0, s>>>(tmC, X16, M, K, w->absmax_q, w->absmax_scale, w->absmax_mean, N,
+                                                    f.sU, rp, static_cast<const uint16_t *>(B), r,
+                                                    static_cast<uint16_t *>(Y), wait_ns());
         }
-        if ((st = launch_check("k_fwd_simt"))) return st;
+        if ((st = launch_check("k_fwd_small"))) return st;
         return ok();
     }
 
@@ -822,7 +830,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
         if ((st = launch_check("k_transpose"))) return st;
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, rp);
+            k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, rp);
         }
         if ((st = launch_check("k_lora_down(V)"))) return st;
         const uint16_t *U = static_cast<const uint16_t *>(U_saved);
@@ -830,7 +838,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
         if (!U) {
             {
                 ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-                k_lora_down<<<(unsigned)cdiv(M, 16), 256, 0, s>>>(X16, M, K, A16, r, 1.0f, nullptr, 0, b.U, rp);
+                k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(X16, M, K, A16, r, 1.0f, nullptr, 0, b.U, rp);
             }
             if ((st = launch_check("k_lora_down(U)"))) return st;
             U = b.U;

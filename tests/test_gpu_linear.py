@@ -66,6 +66,10 @@ def run_and_check(g, oracle, M, N, K, r, scale, seed, **kw):
     (512, 1024, 2048, 16, 2.0),    # tensor-core path, full tiles
     (200, 520, 1088, 64, 0.25),    # tensor-core path: ragged M, N and K tiles
     (128, 256, 4096, 72, 0.5),     # two LoRA k-steps
+    (20, 100, 192, 8, 2.0),        # few tokens, N not a multiple of 8
+    (70, 100, 192, 8, 2.0),        # tensor-core forward, CUDA-core backward (N % 8 != 0)
+    (32, 2048, 1024, 16, 2.0),     # largest few-token forward (four 8-token tiles)
+    (24, 512, 14336, 16, 2.0),     # few tokens, longest K of the table
 ])
 def test_fwd_bwd_parity(g, oracle, M, N, K, r, scale):
     run_and_check(g, oracle, M, N, K, r, scale, seed=3000 + M + N + r)
