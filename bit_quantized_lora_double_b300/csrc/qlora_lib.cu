@@ -656,12 +656,24 @@ qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_st
     if (!al16(out)) return fail(QLORA_ERR_ALIGN, "output must be 16-byte aligned");
     if (w->rows == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t nhalf = w->rows * w->cols / 32;
+    const int64_t nb = w->rows * w->cols / kBlock;
+    static std::once_flag once;
+    static cudaError_t aerr = cudaSuccess;
+    std::call_once(once, [] {
+        aerr = cudaFuncSetAttribute(k_nf4_dequant, cudaFuncAttributeMaxDynamicSharedMemorySize, kDeqSmem);
+    });
+    if (aerr != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
+    // the output viewed as [blocks, 64] bf16 rows of 128 bytes
+    CUtensorMap tmO;
+    if ((st = make_map(&tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, kBlock, nb, kBlock * 2, 64, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "output")))
+        return st;
+    const int64_t nchunks = cdiv(nb, 32);
+    const unsigned grid = (unsigned)std::min<int64_t>(cdiv(nchunks, kDeqWarps), 148 * 3);
     {
         ProfScope ps(QLORA_KERNEL_DEQUANT, s);
-        k_nf4_dequant<<<(unsigned)cdiv(nhalf, 256), 256, 0, s>>>(reinterpret_cast<const uint4 *>(w->codes),
-                                                                 w->absmax_q, w->absmax_scale, w->absmax_mean,
-                                                                 nhalf, static_cast<uint4 *>(out));
+        k_nf4_dequant<<<grid, kDeqWarps * 32, kDeqSmem, s>>>(tmO, reinterpret_cast<const uint4 *>(w->codes),
+                                                             w->absmax_q, w->absmax_scale, w->absmax_mean, nb);
     }
     if ((st = launch_check("k_nf4_dequant"))) return st;
     return ok();
