@@ -170,6 +170,141 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def device_projection(qlora, torch, dev, gen, n, k, M, r, w_std, b_std, copies=1):
+    """Seeded device-side inputs of one projection (torch Philox generator,
+    the same distributions as the parity inputs): the NF4 weight (and
+    `copies` - 1 extra copies of it), X, dY ~ N(0, 1), A ~ N(0, 1/K),
+    B ~ N(0, b_std); output buffers and one workspace."""
+    bf = torch.bfloat16
+
+    def normal(shape, std):
+        return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * std).to(bf)
+
+    W = normal((n, k), w_std)
+    w = qlora.alloc_nf4_weight(n, k, dev)
+    qlora.qlora_nf4_quantize(W, w, qlora.workspace(qlora.qlora_nf4_quantize_workspace(n, k), dev))
+    del W
+    ws_ = [w]
+    for _ in range(copies - 1):
+        x = qlora.alloc_nf4_weight(n, k, dev)
+        x.codes.copy_(w.codes); x.absmax_q.copy_(w.absmax_q)
+        x.absmax_scale.copy_(w.absmax_scale); x.absmax_mean.copy_(w.absmax_mean)
+        ws_.append(x)
+    d = dict(n=n, k=k, w=ws_, X=normal((M, k), 1.0), dY=normal((M, n), 1.0), A=normal((r, k), 1.0 / k),
+             B=normal((n, r), b_std), Y=torch.empty((M, n), dtype=bf, device=dev),
+             U=torch.empty((M, r), dtype=bf, device=dev), dX=torch.empty((M, k), dtype=bf, device=dev),
+             dA=torch.empty((r, k), dtype=torch.float32, device=dev),
+             dB=torch.empty((n, r), dtype=torch.float32, device=dev))
+    d["ws"] = qlora.workspace(max(qlora.qlora_linear_fwd_workspace(M, w, r),
+                                  qlora.qlora_linear_bwd_workspace(M, w, r)), dev)
+    return d
+
+
+def graph_time(torch, fn, steps, warmup):
+    """ms per call of fn, replayed as one CUDA graph per call after warm-up."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def bench_llama70b(qlora, torch, dev, pk, steps):
+    """The Llama-70B-shaped projections at M = 4096, r = 64: forward +
+    backward of all seven, TFLOP/s."""
+    wl = synth.WORKLOADS[3]
+    M, r, scale = wl["M"], wl["r"], wl["scale"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(synth.seed_for(3, "X"))
+    P = [device_projection(qlora, torch, dev, gen, n, k, M, r, wl["w_std"], wl["b_std"])
+         for _, n, k in wl["projections"]]
+
+    def step():
+        for d in P:
+            qlora.qlora_linear_fwd(d["X"], M, d["w"][0], d["A"], d["B"], r, scale, d["Y"], d["U"], d["ws"])
+        for d in reversed(P):
+            qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"][0], d["A"], d["B"], r, scale, d["dX"],
+                                   d["dA"], d["dB"], d["ws"])
+
+    ms = graph_time(torch, step, steps, 2)
+    flops = step_flops(M, wl["projections"], r)
+    out = {"workload": wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=64 alpha=16", "M": M, "r": r,
+           "ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "pct_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16"],
+           "pct_bf16_peak_sustained": flops / (ms * 1e-3) / 1e12 / pk["bf16_sus"]}
+    del P
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_sweep(qlora, torch, dev, pk):
+    """Token-count sweep on the gate projection 4096 -> 14336 (r = 16): the
+    forward at every M, the backward for M >= 128. For M <= 16 the forward
+    reads six rotating copies of the packed weight (more than L2 holds) and
+    is reported as GB/s against the HBM roofline."""
+    wl = synth.WORKLOADS[4]
+    _, n, k = wl["projections"][0]
+    r, scale = wl["r"], wl["scale"]
+    rows = []
+    for M in wl["M_sweep"]:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(synth.seed_for(4, "X") + M)
+        copies = 6 if M <= 16 else 1
+        d = device_projection(qlora, torch, dev, gen, n, k, M, r, wl["w_std"], wl["b_std"], copies)
+        it = [0]
+
+        def fwd():
+            w = d["w"][it[0] % copies]
+            it[0] += 1
+            qlora.qlora_linear_fwd(d["X"], M, w, d["A"], d["B"], r, scale, d["Y"], d["U"], d["ws"])
+
+        reps = max(3, min(200, int(2e11 / max(1, M * n * k * 2))))
+        if copies > 1:
+            # eager launches (the rotation over weight copies is host-side)
+            for _ in range(5):
+                fwd()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fwd()
+            b.record()
+            torch.cuda.synchronize()
+            f_ms = a.elapsed_time(b) / reps
+        else:
+            f_ms = graph_time(torch, fwd, reps, 3)
+        f_fl = 2 * M * n * k + 2 * M * r * (n + k)
+        row = {"M": M, "fwd_ms": f_ms, "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12}
+        if M <= 16:
+            wbytes = n * k // 2 + n * k // 64 + 4 * ((n * k // 64 + 255) // 256) + 4
+            byts = wbytes + 2 * (M * k + M * n + r * k + n * r)
+            gbs = byts / (f_ms * 1e-3) / 1e9
+            row.update({"fwd_gbs": gbs, "fwd_pct_hbm": gbs / pk["hbm"], "fwd_bytes": byts,
+                        "l2": "6 rotating weight copies (> L2)"})
+        if M >= 128:
+            def bwd():
+                qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"][0], d["A"], d["B"], r, scale, d["dX"],
+                                       d["dA"], d["dB"], d["ws"])
+            b_ms = graph_time(torch, bwd, reps, 3)
+            b_fl = 2 * M * n * k + 4 * M * r * (n + k)
+            row.update({"bwd_ms": b_ms, "bwd_tflops": b_fl / (b_ms * 1e-3) / 1e12,
+                        "fwd_bwd_tflops": (4 * M * n * k + 6 * M * r * (n + k)) / ((f_ms + b_ms) * 1e-3) / 1e12})
+        rows.append(row)
+        del d
+        torch.cuda.empty_cache()
+    return {"workload": wl["name"] + ": gate 4096->14336 NF4+DQ, LoRA r=16 alpha=32", "rows": rows}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -177,6 +312,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--prof-steps", type=int, default=20)
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the 70B-shaped layer and the M sweep")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -321,32 +457,61 @@ def main():
     h2d = sum(d["hX"].numel() * 2 + d["hdY"].numel() * 2 for d in P)
     d2h = sum(d["Y"].numel() * 2 + d["dX"].numel() * 2 + d["dA"].numel() * 4 + d["dB"].numel() * 4 for d in P)
 
+    # Host copies run on two copy streams beside the compute stream: the inputs
+    # of projection p+1 travel while projection p computes, and each result
+    # goes back as soon as its kernel is done.
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    comp = torch.cuda.current_stream()
+
     def e2e_step():
         for d in P:
-            d["X"].copy_(d["hX"], non_blocking=True)
+            with torch.cuda.stream(s_h2d):
+                d["X"].copy_(d["hX"], non_blocking=True)
+                d["ev_x"] = torch.cuda.Event()
+                d["ev_x"].record(s_h2d)
+            with torch.cuda.stream(s_h2d):
+                d["dY"].copy_(d["hdY"], non_blocking=True)
+                d["ev_dy"] = torch.cuda.Event()
+                d["ev_dy"].record(s_h2d)
+        for d in P:
+            comp.wait_event(d["ev_x"])
             qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"])
-            hY[d["name"]].copy_(d["Y"], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(comp)
+            s_d2h.wait_event(ev)
+            with torch.cuda.stream(s_d2h):
+                hY[d["name"]].copy_(d["Y"], non_blocking=True)
         for d in reversed(P):
-            d["dY"].copy_(d["hdY"], non_blocking=True)
+            comp.wait_event(d["ev_dy"])
             qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
                                    d["dB"], d["ws"])
             if world > 1:
                 dist.all_reduce(d["dA"])
                 dist.all_reduce(d["dB"])
-            hdX[d["name"]].copy_(d["dX"], non_blocking=True)
-            hdA[d["name"]].copy_(d["dA"], non_blocking=True)
-            hdB[d["name"]].copy_(d["dB"], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(comp)
+            s_d2h.wait_event(ev)
+            with torch.cuda.stream(s_d2h):
+                hdX[d["name"]].copy_(d["dX"], non_blocking=True)
+                hdA[d["name"]].copy_(d["dA"], non_blocking=True)
+                hdB[d["name"]].copy_(d["dB"], non_blocking=True)
+        # the step ends when every result is on the host
+        ev = torch.cuda.Event()
+        ev.record(s_d2h)
+        comp.wait_event(ev)
 
     e2e_step()
     barrier()
-    ev0.record(stream)
+    ev0.record(comp)
     for _ in range(args.e2e_steps):
         e2e_step()
-    ev1.record(stream)
+    ev1.record(comp)
     barrier()
     e2e_ms = ev0.elapsed_time(ev1) / args.e2e_steps
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "note": "pinned host buffers; H2D of all inputs and D2H of Y, dX, dA, dB on two copy streams "
+                   "overlapping the compute stream"}
 
     # ---- codec: 14336 x 4096 quantize once + dequantize x100 -----------------
     _, cn, ck = synth.WORKLOADS[CODEC_WORKLOAD]["projections"][0]
@@ -395,6 +560,11 @@ def main():
              "quantize": {"value": q_bytes / (q_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": q_ms,
                           "bytes": q_bytes}}
 
+    extra = {}
+    if rank == 0 and world == 1 and not args.no_extra:
+        extra["llama70b_layer"] = bench_llama70b(qlora, torch, dev, pk, 5)
+        extra["gate_sweep"] = bench_sweep(qlora, torch, dev, pk)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(CPU_SAMPLE_TOKENS, projs, r, wl["scale"])
@@ -418,6 +588,7 @@ def main():
             "timed_region": "CUDA graph of one step replayed" if graph is not None else "eager launches",
             "clocks": clocks,
             "codec": codec,
+            **extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
