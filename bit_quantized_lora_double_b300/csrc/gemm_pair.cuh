@@ -112,6 +112,12 @@ __device__ __forceinline__ void pair_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// 32-byte global store (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
 // Programmatic dependent launch: wait for the preceding kernel's memory, and
 // let the next kernel start its own set-up.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -441,7 +447,18 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         }
                     } else {
                         uint16_t *dstp = p.out + row * p.ldo + w.c0 + col;
-                        if (ncol >= 64 && (p.ldo & 7) == 0) {
+                        if (ncol >= 64 && p.out_v8) {
+                            // four 32-byte stores: whole sectors of the row segment
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t pk[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    pk[e] = pack_bf16x2(__uint_as_float(v[16 * q + 2 * e]),
+                                                        __uint_as_float(v[16 * q + 2 * e + 1]));
+                                st_global_v8(dstp + 16 * q, pk);
+                            }
+                        } else if (ncol >= 64 && (p.ldo & 7) == 0) {
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 uint4 pk;

@@ -66,6 +66,7 @@ struct TcParams {
     float *part;           // splits > 1: fp32 partials [splits][M][Nd]
     uint64_t wait_ns;
     unsigned kernel_id;
+    int out_v8;            // out and ldo allow 32-byte stores of 64-column segments
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {

@@ -184,6 +184,10 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent of the preceding kernel: its
+    // outputs are visible from here on; the next kernel may start its set-up
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----

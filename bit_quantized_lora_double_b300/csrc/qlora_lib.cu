@@ -475,13 +475,15 @@ qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsig
     cfg.blockDim = dim3(SkCfg::THREADS);
     cfg.dynamicSmemBytes = SkCfg::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)j0.pl.chunks;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = (unsigned)j0.pl.chunks;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = j0.pl.chunks > 1 ? 1 : 0;
+    cfg.numAttrs = j0.pl.chunks > 1 ? 2 : 1;
     cudaError_t e;
     {
         ProfScope ps(j0.mode >= kRedDA ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
@@ -788,6 +790,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     prm.mean = w->absmax_mean;
     prm.out = static_cast<uint16_t *>(Y);
     prm.ldo = N;
+    prm.out_v8 = (reinterpret_cast<uintptr_t>(Y) & 31) == 0 && (N & 15) == 0;
     const GemmSplit gs = gemm_split(M, N, prm.nk_main);
     prm.splits = gs.splits;
     prm.steps_per_split = gs.steps_per_split;
@@ -968,6 +971,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     prm.mean = w->absmax_mean;
     prm.out = static_cast<uint16_t *>(dX);
     prm.ldo = K;
+    prm.out_v8 = (reinterpret_cast<uintptr_t>(dX) & 31) == 0 && (K & 15) == 0;
     const GemmSplit gs = gemm_split(M, K, prm.nk_main);
     prm.splits = gs.splits;
     prm.steps_per_split = gs.steps_per_split;
