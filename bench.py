@@ -28,7 +28,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from bit_quantized_lora_double_b300 import synth  # noqa: E402
+from bit_quantized_lora_double_b300 import dp, synth  # noqa: E402
 
 WORKLOAD = 1          # Llama-3.1-8B-shaped layer, M = 2048, r = 16
 CODEC_WORKLOAD = 2    # 14336 x 4096 codec
@@ -371,8 +371,7 @@ def main():
             qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
                                    d["dB"], d["ws"])
             if world > 1:
-                dist.all_reduce(d["dA"])
-                dist.all_reduce(d["dB"])
+                dp.allreduce_adapter_grads([d["dA"], d["dB"]])
 
     def barrier():
         if world > 1:
@@ -486,8 +485,7 @@ def main():
             qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
                                    d["dB"], d["ws"])
             if world > 1:
-                dist.all_reduce(d["dA"])
-                dist.all_reduce(d["dB"])
+                dp.allreduce_adapter_grads([d["dA"], d["dB"]])
             ev = torch.cuda.Event()
             ev.record(comp)
             s_d2h.wait_event(ev)
