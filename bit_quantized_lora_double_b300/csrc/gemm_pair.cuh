@@ -341,58 +341,79 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) csrc[h] = (uint32_t)(nl * 64 + (((b2 * 2 + h) ^ ((nl >> 1) & 3)) << 4));
         }
-        int64_t g = 0;
-        bool alive = true;
-        for (int64_t u = pair_id; u < units && alive; u += npairs) {
-            const PairUnit w = pair_unit(p, u, mt, nt);
-            const int64_t ch = w.c0 + (int64_t)rank * C::HN;
-            for (int64_t it = 0; it < w.nk; ++it, ++g) {
-                if ((int)(g % C::DEC_GROUPS) != grp) continue;
-                const int s = (int)(g % C::STAGES);
-                const uint32_t par = (uint32_t)(g / C::STAGES) & 1;
-                // this thread's block: forward W row ch + dt, k-block kbeg + it;
-                // dX W row (kbeg + it) * 64 + nl, k-block ch / 64 + b2
-                int qv = 0;
-                float sv = 0.0f;
-                bool valid = false;
-                if (it < w.nmain) {
-                    const int64_t wrow = MODE == kFwd ? ch + dt : (w.kbeg + it) * C::BK + nl;
-                    const int64_t kb = MODE == kFwd ? w.kbeg + it : ch / kBlock + b2;
-                    if (wrow < p.w_rows && kb < kblocks) {
-                        const int64_t b = wrow * kblocks + kb;
-                        qv = __ldg(p.q + b);
-                        sv = __ldg(p.s2 + (b >> 8));
-                        valid = true;
-                    }
-                }
-                if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) {
-                    alive = false;
-                    break;
-                }
-                if (it < w.nmain) {
-                    uint8_t *wt = wtile(s);
-                    const uint8_t *ct = ctile(s);
-                    uint32_t o[8][4];
-                    if (valid) {
-                        const Nf4Table tab = make_table(dq_absmax((int8_t)qv, sv, mean));
-                        uint4 cw[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) cw[h] = *reinterpret_cast<const uint4 *>(ct + csrc[h]);
-                        const uint32_t wv[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w, cw[1].x, cw[1].y, cw[1].z, cw[1].w};
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) decode8(tab, wv[c], o[c]);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0u;
-                    }
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(wt + dst[c]) = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(ready_addr0 + (uint32_t)(s * 8));
+        // This group's steps (global step g with g % DEC_GROUPS == grp) are
+        // walked with a cursor; the absmax code and group scale of the next
+        // step are loaded before the current step is waited for and decoded.
+        struct Cursor {
+            int64_t u, it, g;
+            PairUnit w;
+        };
+        auto advance = [&](Cursor &c) {
+            ++c.it;
+            ++c.g;
+            while (c.u < units && c.it >= c.w.nk) {
+                c.u += npairs;
+                c.it = 0;
+                if (c.u < units) c.w = pair_unit(p, c.u, mt, nt);
             }
+        };
+        auto fetch = [&](const Cursor &c, int &qv, float &sv) {
+            qv = 0;
+            sv = 0.0f;
+            if (c.u >= units || c.it >= c.w.nmain) return false;
+            const int64_t ch = c.w.c0 + (int64_t)rank * C::HN;
+            const int64_t wrow = MODE == kFwd ? ch + dt : (c.w.kbeg + c.it) * C::BK + nl;
+            const int64_t kb = MODE == kFwd ? c.w.kbeg + c.it : ch / kBlock + b2;
+            if (wrow >= p.w_rows || kb >= kblocks) return false;
+            const int64_t bidx = wrow * kblocks + kb;
+            qv = __ldg(p.q + bidx);
+            sv = __ldg(p.s2 + (bidx >> 8));
+            return true;
+        };
+        Cursor cur;
+        cur.u = pair_id;
+        cur.it = 0;
+        cur.g = 0;
+        if (cur.u < units) cur.w = pair_unit(p, cur.u, mt, nt);
+        for (int i = 0; i < grp; ++i) advance(cur);
+        Cursor nxt = cur;
+        for (int i = 0; i < C::DEC_GROUPS; ++i) advance(nxt);
+        int qv, qn;
+        float sv, sn;
+        bool valid = fetch(cur, qv, sv);
+        while (cur.u < units) {
+            const bool valid_n = fetch(nxt, qn, sn);
+            const int s = (int)(cur.g % C::STAGES);
+            const uint32_t par = (uint32_t)(cur.g / C::STAGES) & 1;
+            if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) break;
+            if (cur.it < cur.w.nmain) {
+                uint8_t *wt = wtile(s);
+                const uint8_t *ct = ctile(s);
+                uint32_t o[8][4];
+                if (valid) {
+                    const Nf4Table tab = make_table(dq_absmax((int8_t)qv, sv, mean));
+                    uint4 cw[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) cw[h] = *reinterpret_cast<const uint4 *>(ct + csrc[h]);
+                    const uint32_t wv[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w, cw[1].x, cw[1].y, cw[1].z, cw[1].w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) decode8(tab, wv[c], o[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0u;
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(wt + dst[c]) = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(ready_addr0 + (uint32_t)(s * 8));
+            cur = nxt;
+            qv = qn;
+            sv = sn;
+            valid = valid_n;
+            for (int i = 0; i < C::DEC_GROUPS; ++i) advance(nxt);
         }
     } else {
         // --------------------------------------------------- epilogue ----
