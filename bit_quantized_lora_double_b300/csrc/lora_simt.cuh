@@ -5,10 +5,9 @@
 //   k_lora_grad     split-M partial sums of out[j, c] = sum_m P[m, j] Q[m, c]
 //   k_grad_reduce   sums the partials in a fixed order, applies s, stores
 //                   dA [r, K] or dB [N, r]
-//   k_fwd_simt      Y = X W'^T + (sU) B^T, NF4 decoded in the K loop
 //   k_dx_simt       dX = dY W' + (sV) A, NF4 decoded in the N loop
-// The tiled GEMMs here serve small M (and any shape, as a reference path on
-// the device); large M runs on the tcgen05 kernels.
+// These serve the backward for M < 64 tokens (and N not a multiple of 8);
+// larger M runs on the tcgen05 kernels.
 // Sources: xingyuzhitong.com "Fine-Tuning Memory Requirements", sections "LoRA:
 // freeze the base, train small adapters" and "QLoRA: quantize the frozen base
 // to 4 bits"; inquiringlines.com note, mechanism paragraph.
@@ -165,88 +164,6 @@ __device__ __forceinline__ void decode_half_block(const uint8_t *__restrict__ co
         for (int e = 0; e < 4; ++e) {
             f[8 * i + 2 * e] = bf16lo_to_f32(o[e]);
             f[8 * i + 2 * e + 1] = bf16hi_to_f32(o[e]);
-        }
-    }
-}
-
-// Y[m, n] = sum_k X[m, k] W'[n, k] + sum_j sU[m, j] B[n, j]
-__global__ void __launch_bounds__(256) k_fwd_simt(const uint16_t *__restrict__ X, int64_t M, int64_t K,
-                                                  const uint8_t *__restrict__ codes, const int8_t *__restrict__ q,
-                                                  const float *__restrict__ s2, const float *__restrict__ mean_p,
-                                                  int64_t N, const uint16_t *__restrict__ sU, int ldu,
-                                                  const uint16_t *__restrict__ B, int r, uint16_t *__restrict__ Y) {
-    __shared__ float Xs[kSt][kSt + 1];  // [m][k]
-    __shared__ float Ws[kSt][kSt + 1];  // [k][n]
-    const int tid = threadIdx.x, tm = tid & 15, tn = tid >> 4;
-    const int64_t m0 = (int64_t)blockIdx.y * kSt, n0 = (int64_t)blockIdx.x * kSt;
-    const float mean = *mean_p;
-    float acc[4][4] = {};
-    for (int64_t k0 = 0; k0 < K; k0 += kSt) {
-        for (int i = tid; i < kSt * 8; i += 256) {
-            const int row = i >> 3, kc = i & 7;
-            const int64_t m = m0 + row;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (m < M) v = *reinterpret_cast<const uint4 *>(X + m * K + k0 + kc * 8);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                Xs[row][kc * 8 + 2 * e] = bf16lo_to_f32(u[e]);
-                Xs[row][kc * 8 + 2 * e + 1] = bf16hi_to_f32(u[e]);
-            }
-        }
-        if (tid < 128) {
-            const int row = tid >> 1, half = tid & 1;
-            const int64_t n = n0 + row;
-            float f[32];
-            if (n < N) {
-                decode_half_block(codes, q, s2, mean, (n * K + k0) / kBlock, half, f);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) f[e] = 0.0f;
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) Ws[half * 32 + e][row] = f[e];
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < kSt; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = Xs[tm * 4 + i][kk];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Ws[kk][tn * 4 + j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-    for (int j = 0; j < r; ++j) {
-        float u[4], b[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t m = m0 + tm * 4 + i;
-            u[i] = m < M ? bf16lo_to_f32(sU[m * ldu + j]) : 0.0f;
-        }
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int64_t n = n0 + tn * 4 + jj;
-            b[jj] = n < N ? bf16lo_to_f32(B[n * r + j]) : 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(u[i], b[jj], acc[i][jj]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t m = m0 + tm * 4 + i;
-        if (m >= M) continue;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int64_t n = n0 + tn * 4 + jj;
-            if (n < N) Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i][jj]));
         }
     }
 }

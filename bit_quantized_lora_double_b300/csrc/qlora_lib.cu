@@ -157,23 +157,16 @@ SkPlan sk_plan(int64_t rows, int64_t L, int r) {
     return p;
 }
 
-#ifndef QLORA_USE_PAIR
-#define QLORA_USE_PAIR 1
-#endif
-// The fused GEMM runs on CTA pairs (512 x 256 tiles, k_gemm_pair); with
-// QLORA_USE_PAIR=0 on single CTAs (256 x 256 tiles, k_gemm_tc).
-constexpr bool kPair = QLORA_USE_PAIR != 0;
-
-// Contraction splits of the fused GEMM: split only when the output tiles fill
-// less than three quarters of the SMs (148, or 74 pairs), keeping >= 4
+// Contraction splits of the fused GEMM: split only when the 512 x 256 output
+// tiles fill less than three quarters of the 74 CTA pairs, keeping >= 4
 // k-steps per split.
 struct GemmSplit {
     int splits;
     int64_t steps_per_split;
 };
 GemmSplit gemm_split(int64_t M, int64_t Nd, int64_t nk_main) {
-    const int64_t units = kPair ? 74 : 148;
-    const int64_t tiles = cdiv(Nd, 256) * cdiv(M, kPair ? PairCfg::PAIR_M : TcCfg::BM);
+    const int64_t units = PairCfg::MAX_PAIRS;
+    const int64_t tiles = cdiv(Nd, PairCfg::BN) * cdiv(M, PairCfg::PAIR_M);
     int64_t sp = 1;
     if (tiles * 4 < 3 * units) sp = std::max<int64_t>(1, std::min<int64_t>({units / tiles, nk_main / 4, 8}));
     const int64_t sps = cdiv(nk_main, sp);
@@ -295,10 +288,8 @@ qlora_status tc_setup() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = kPair ? cudaFuncSetAttribute(k_gemm_pair<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           PairCfg::SMEM_BYTES)
-                    : cudaFuncSetAttribute(k_gemm_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           TcCfg::SMEM_BYTES);
+        err = cudaFuncSetAttribute(k_gemm_pair<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   PairCfg::SMEM_BYTES);
     });
     if (err != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(err));
     return QLORA_OK;
@@ -338,32 +329,24 @@ qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUt
                          const TcParams &prm, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    if (kPair) {
-        const int64_t units = cdiv(prm.Nd, PairCfg::BN) * cdiv(prm.M, PairCfg::PAIR_M) * prm.splits;
-        const int64_t pairs = std::min<int64_t>(units, gemm_pairs_resident<MODE>());
-        cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-        cfg.blockDim = dim3(PairCfg::THREADS);
-        cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 2;
-    } else {
-        cfg.gridDim = dim3((unsigned)cdiv(prm.Nd, TcCfg::BN), (unsigned)cdiv(prm.M, TcCfg::BM), (unsigned)prm.splits);
-        cfg.blockDim = dim3(TcCfg::THREADS);
-        cfg.dynamicSmemBytes = TcCfg::SMEM_BYTES;
-        cfg.numAttrs = 0;
-    }
+    const int64_t units = cdiv(prm.Nd, PairCfg::BN) * cdiv(prm.M, PairCfg::PAIR_M) * prm.splits;
+    const int64_t pairs = std::min<int64_t>(units, gemm_pairs_resident<MODE>());
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(PairCfg::THREADS);
+    cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     cfg.stream = s;
     cudaError_t e;
     {
         ProfScope ps(MODE == kFwd ? QLORA_KERNEL_FWD_GEMM : QLORA_KERNEL_DX_GEMM, s);
-        e = kPair ? cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE>, ta, tc, tl, tw, prm)
-                  : cudaLaunchKernelEx(&cfg, k_gemm_tc<MODE>, ta, tc, tl, tw, prm);
+        e = cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE>, ta, tc, tl, tw, prm);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -766,11 +749,11 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
                        CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
         (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, r, K * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
-        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 32, kPair ? 128 : 256,
+        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 32, 128,
                        CU_TENSOR_MAP_SWIZZLE_32B, "codes")) ||
         (st = make_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rs, M, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "sU")) ||
-        (st = make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bl, rs, N, rs * 2, 64, kPair ? 128 : 256,
+        (st = make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bl, rs, N, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "B")))
         return st;
     // U = X A^T on the tensor cores; U (bf16) to U_save, s*U (bf16) to the workspace
@@ -782,7 +765,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     prm.Nd = N;
     prm.w_rows = N;
     prm.w_cols = K;
-    prm.nk_main = K / TcCfg::BK;
+    prm.nk_main = K / kGemmBK;
     prm.lora_steps = rp / 64;
     prm.r = r;
     prm.q = w->absmax_q;
@@ -928,8 +911,8 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
                        CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
         (st = make_map(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "X (MN)")) ||
-        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, kPair ? 64 : 128, 64,
-                       kPair ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, "codes")) ||
+        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_64B, "codes")) ||
         (st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rs, M, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "sV")) ||
         (st = make_map(&tmVmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rs, M, rs * 2, 64, 64,
@@ -963,7 +946,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     prm.Nd = K;
     prm.w_rows = N;
     prm.w_cols = K;
-    prm.nk_main = cdiv(N, TcCfg::BK);
+    prm.nk_main = cdiv(N, kGemmBK);
     prm.lora_steps = rp / 64;
     prm.r = r;
     prm.q = w->absmax_q;
