@@ -45,6 +45,32 @@ def peaks():
     return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
 
 
+def sources_sha256():
+    """Hash of the library sources (kernels and ABI header)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "bit_quantized_lora_double_b300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "qlora.h"))
+    for f in files:
+        if os.path.isfile(f):
+            h.update(os.path.basename(f).encode())
+            h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic(kind):
+    """DRAM bytes per launch of a kernel kind from the committed ncu summary,
+    or None when the sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("sources_sha256") != sources_sha256():
+        return None
+    return d.get("per_launch_bytes", {}).get(kind)
+
+
 def step_flops(M, projections, r):
     return sum(4 * M * n * k + 6 * M * r * (n + k) for _, n, k in projections)
 
@@ -442,7 +468,9 @@ def main():
         ms_kind = prof_ms[dom] / prof_steps
         ach = gemm_flops[dom] / (ms_kind * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_sus"], "traffic": None,
+                "frac": ach / pk["bf16_sus"], "traffic": measured_traffic(dom),
+                "traffic_note": "DRAM read+write bytes per launch (average over the step's launches) from "
+                                "profiles/roofline_traffic.json",
                 "peak_note": f"bf16 dense sustained ({pk['src']}); a kernel timed inside a long step",
                 "flops_per_launch": gemm_flops[dom] / len(projs),
                 "launches_per_step": prof_n[dom] / prof_steps, "ms_per_step": ms_kind,
@@ -553,7 +581,7 @@ def main():
                          "bytes_per_pass": dq_bytes, "ms_per_pass": dq_kernel_ms, "ms_per_call": dq_ms,
                          "l2": f"{ncopy} rotating copies of the packed weight (> L2)",
                          "roofline": {"bound": "hbm", "achieved": dq_gbs, "peak": pk["hbm"], "unit": "GB/s",
-                                      "frac": dq_gbs / pk["hbm"], "traffic": None,
+                                      "frac": dq_gbs / pk["hbm"], "traffic": measured_traffic("dequant"),
                                       "peak_note": f"HBM copy, {pk['src']}"}},
              "quantize": {"value": q_bytes / (q_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": q_ms,
                           "bytes": q_bytes}}
