@@ -73,6 +73,8 @@ struct SkParams {
 // rows 16 bytes apart in bank terms, so a quarter-warp's float4 accesses to
 // 8 consecutive rows hit distinct banks)
 constexpr int kRedStride = 68;
+// largest cluster (chunks of one tile's contraction) the host plans
+constexpr int kSkMaxCluster = 8;
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -128,6 +130,39 @@ __device__ __forceinline__ void sk_store(const SkParams &p, int64_t row, int jba
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 if (j < nj) p.o32[row * p.r + jbase + j] = __fmul_rn(p.s, acc[j]);
+            break;
+    }
+}
+
+// Writes row `row`, columns j0 .. j0 + nv - 1 (nv <= 4) of the tile's
+// complete sum, v holding those values in order; `pad` also writes the zero
+// columns [r, ldb) of sU / sV for that row.
+__device__ __forceinline__ void sk_store4(const SkParams &p, int64_t row, int j0, int nv, float4 v, bool pad) {
+    const float a[4] = {v.x, v.y, v.z, v.w};
+    switch (p.mode) {
+        case kRedU:
+        case kRedV: {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (e < nv) {
+                    if (p.mode == kRedU && p.o16a)
+                        p.o16a[row * p.lda + j0 + e] = __bfloat16_as_ushort(__float2bfloat16_rn(a[e]));
+                    p.o16b[row * p.ldb + j0 + e] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(p.s, a[e])));
+                }
+            }
+            if (pad)
+                for (int jj = p.r; jj < p.ldb; ++jj) p.o16b[row * p.ldb + jj] = 0;
+            break;
+        }
+        case kRedDA:
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < nv) p.o32[(int64_t)(j0 + e) * p.rows + row] = a[e];
+            break;
+        default:
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < nv) p.o32[row * p.r + j0 + e] = __fmul_rn(p.s, a[e]);
             break;
     }
 }
@@ -278,38 +313,43 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
     __syncwarp();
     if (p.nchunks > 1) {
         cluster_sync_all();  // every partial tile of the cluster is in place
-        if (warp >= 2 && cluster_ctarank() == 0) {
-            const int trow = (warp & 3) * 32 + lane;
-            const int64_t row = row0 + trow;
+        if (warp >= 2) {
+            // The cluster's CTAs share the reduction: work item u covers tile
+            // row u % BM, columns 4 * (u / BM) .. + 3 of this z-slice, and
+            // sums that float4 over the n partial tiles (c = 0 .. n - 1, in
+            // that order). Items are dealt out over the 128 epilogue threads
+            // of every CTA, so all n remote loads of an item are in flight
+            // together and no CTA walks the whole tile.
+            const int n = p.nchunks;  // <= kSkMaxCluster
             const int jbase = (int)blockIdx.z * C::BN;
             const int nj = min(64, p.r - jbase);
-            if (row < p.rows) {
-                const uint32_t local = smem_u32(smem) + (uint32_t)(trow * kRedStride * 4);
-                float acc[64];
+            const int ng = (nj + 3) >> 2;
+            const bool last_z = jbase + 64 >= p.r;
+            const uint32_t local = smem_u32(smem);
+            uint32_t base[kSkMaxCluster];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            for (int c = 0; c < kSkMaxCluster; ++c) base[c] = c < n ? mapa_shared(local, (uint32_t)c) : 0u;
+            const int stride = n * C::BM;
+            for (int u = (int)cluster_ctarank() * C::BM + ((int)threadIdx.x - 64); u < C::BM * ng; u += stride) {
+                const int trow = u % C::BM, g = u / C::BM;
+                const int64_t row = row0 + trow;
+                if (row >= p.rows) continue;
+                const uint32_t off = (uint32_t)(trow * kRedStride + 4 * g) * 4u;
+                float4 f[kSkMaxCluster];
 #pragma unroll
-                for (int g0 = 0; g0 < 16; g0 += 4) {
-                    if (4 * g0 < nj) {
-                        for (int c = 0; c < p.nchunks; ++c) {
-                            const uint32_t base = mapa_shared(local, (uint32_t)c);
-                            float4 f[4];
+                for (int c = 0; c < kSkMaxCluster; ++c)
+                    if (c < n) f[c] = ld_dsmem_f4(base[c] + off);
+                float4 sum = f[0];
 #pragma unroll
-                            for (int g = 0; g < 4; ++g)
-                                if (4 * (g0 + g) < nj) f[g] = ld_dsmem_f4(base + 16u * (uint32_t)(g0 + g));
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                if (4 * (g0 + g) < nj) {
-                                    acc[4 * (g0 + g)] += f[g].x;
-                                    acc[4 * (g0 + g) + 1] += f[g].y;
-                                    acc[4 * (g0 + g) + 2] += f[g].z;
-                                    acc[4 * (g0 + g) + 3] += f[g].w;
-                                }
-                            }
-                        }
+                for (int c = 1; c < kSkMaxCluster; ++c) {
+                    if (c < n) {
+                        sum.x += f[c].x;
+                        sum.y += f[c].y;
+                        sum.z += f[c].z;
+                        sum.w += f[c].w;
                     }
                 }
-                sk_store(p, row, jbase, acc);
+                sk_store4(p, row, jbase + 4 * g, min(4, nj - 4 * g), sum, last_z && g == ng - 1);
             }
         }
         __syncwarp();
