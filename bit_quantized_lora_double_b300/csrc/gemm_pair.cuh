@@ -59,6 +59,9 @@ struct PairCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int MAX_PAIRS = 74;
 };
+static_assert(PairCfg::MAX_PAIRS == kSkPairs, "one stream-K slot and flag set per pair");
+static_assert(PairCfg::EPI_WARPS * 16384 <= PairCfg::STAGES * PairCfg::STAGE_BYTES,
+              "finishing buffers live in the stage ring");
 
 // ---- cta_group::2 wrappers -------------------------------------------------
 __device__ __forceinline__ void tmem_alloc2(uint32_t *dst_smem, uint32_t ncols) {
@@ -142,29 +145,125 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
-// One work unit: a 512 x 256 output tile and one contraction split.
-struct PairUnit {
-    int64_t m0, c0, kbeg, nmain, nk;
-    int z;
-    bool two;
+// Work schedule: data-parallel waves, then a stream-K remainder. The T
+// output tiles of 512 x 256 are numbered with the row tiles of a column tile
+// adjacent; each is S = nk_main + lora_steps k-steps deep. Tiles t < dp_tiles
+// go data-parallel: pair q of the P pairs computes tiles q, q + P, ... whole,
+// all pairs in step (neighbouring pairs share weight and activation tiles
+// through L2 at the same k). The remaining tiles form one line of
+// W = (T - dp_tiles) * S steps, and pair q takes steps [q W / P, (q + 1) W / P)
+// of it. Inside that range a pair works through segments, one per tile
+// touched:
+//   kSegFull  the whole tile: the pair writes the output;
+//   kSegPart  the tile's tail (the range starts inside the tile): always the
+//             pair's first stream-K segment; the fp32 partial goes to the
+//             pair's slot and each epilogue warp raises its ready flag;
+//   kSegHead  the tile's first steps (the range ends inside the tile): always
+//             the pair's last segment; the pair adds the partials of the
+//             following pairs (whose ranges start inside this tile), in pair
+//             order, and writes the output.
+// Every pair holds at most one slot's worth of partial and finishes at most
+// one shared tile, and the tails it waits for were its neighbours' first
+// stream-K work.
+enum { kSegFull = 0, kSegHead = 1, kSegPart = 2 };
+
+struct PairSeg {
+    int64_t t, m0, c0;
+    int64_t kbeg;   // first main k-step
+    int64_t nmain;  // main k-steps
+    int64_t lbeg;   // first LoRA k-step
+    int64_t nk;     // all k-steps
+    int role;
+    bool two;       // the tile has a second 256-row sub-tile
 };
 
-__device__ __forceinline__ PairUnit pair_unit(const TcParams &p, int64_t u, int64_t mt, int64_t nt) {
-    PairUnit w;
-    const int64_t t = u % (mt * nt);
-    w.z = (int)(u / (mt * nt));
-    w.m0 = (t % mt) * PairCfg::PAIR_M;
-    w.c0 = (t / mt) * PairCfg::BN;
-    w.kbeg = (int64_t)w.z * p.steps_per_split;
-    w.nmain = max((int64_t)0, min(p.steps_per_split, p.nk_main - w.kbeg));
-    w.nk = w.nmain + (w.z == p.splits - 1 ? p.lora_steps : 0);
+struct PairPlan {
+    int64_t mt, S, T, dpt, P;
+    int64_t base, W;  // stream-K line: steps [base, base + W)
+    __device__ __forceinline__ int64_t begin(int64_t q) const { return base + W * q / P; }
+};
+
+// Walks one pair's segments: its data-parallel tiles, then its stream-K range.
+struct SegWalk {
+    int64_t dp;   // next data-parallel tile
+    int64_t g;    // next stream-K step
+    int64_t end;  // end of this pair's stream-K range
+};
+
+__device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &pl, int64_t g, int64_t end);
+
+__device__ __forceinline__ SegWalk seg_walk(const PairPlan &pl, int64_t q) {
+    SegWalk sw;
+    sw.dp = q;
+    sw.g = pl.begin(q);
+    sw.end = pl.begin(q + 1);
+    return sw;
+}
+__device__ __forceinline__ bool seg_next(const TcParams &p, const PairPlan &pl, SegWalk &sw, PairSeg &w) {
+    if (sw.dp < pl.dpt) {
+        w = pair_seg(p, pl, sw.dp * pl.S, sw.dp * pl.S + pl.S);
+        sw.dp += pl.P;
+        return true;
+    }
+    if (sw.g < sw.end) {
+        w = pair_seg(p, pl, sw.g, sw.end);
+        sw.g += w.nk;
+        return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &pl, int64_t g, int64_t end) {
+    PairSeg w;
+    w.t = g / pl.S;
+    const int64_t k0 = g - w.t * pl.S, k1 = min(pl.S, k0 + (end - g));
+    w.m0 = (w.t % pl.mt) * PairCfg::PAIR_M;
+    w.c0 = (w.t / pl.mt) * PairCfg::BN;
+    w.kbeg = k0;
+    w.nmain = max((int64_t)0, min(k1, p.nk_main) - k0);
+    w.lbeg = max(k0, p.nk_main) - p.nk_main;
+    w.nk = k1 - k0;
+    w.role = k0 == 0 ? (k1 == pl.S ? kSegFull : kSegHead) : kSegPart;
     w.two = w.m0 + 256 < p.M;
     return w;
 }
 
-// Persistent kernel: pair q (q = blockIdx.x / 2) takes work units q, q + P,
-// q + 2P, ... (P = gridDim.x / 2); units run over the row tiles fastest, so
-// the pairs working at the same time share weight tiles through L2.
+// Global -> shared bulk copy completing on an mbarrier of this CTA.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Bounded wait for a ready flag raised by another pair.
+__device__ __forceinline__ bool flag_wait(const uint32_t *f, uint64_t limit_ns, unsigned code,
+                                          volatile int *abort_flag, uint32_t peer_abort) {
+    if (ld_acquire_gpu(f)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        __nanosleep(256);
+        if (ld_acquire_gpu(f)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            record_error(code);
+            *abort_flag = 1;
+            st_cluster_u32(peer_abort, 1u);
+            return false;
+        }
+    }
+}
+
+// Persistent kernel: pair q (q = blockIdx.x / 2) works through its segments
+// (its data-parallel tiles, then its stream-K range) of the P = gridDim.x / 2
+// pairs' schedule.
 template <int MODE>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
@@ -180,6 +279,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     uint64_t *tfull = bar + 3 * C::STAGES;      // accumulators complete (commit from the even CTA)
     uint64_t *tempty = bar + 3 * C::STAGES + 1; // even CTA: accumulators drained (8 warp arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * C::STAGES + 2);
+    uint64_t *fixbar = bar + 16;                // 2 per epilogue warp: partial tiles fetched for finishing
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     auto wtile = [&](int s) { return smem + s * C::STAGE_BYTES; };
@@ -190,9 +290,15 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     const uint32_t rank = pair_rank();
     const uint32_t peer = rank ^ 1u;
     const uint32_t peer_abort = mapa_u32(smem_u32((const void *)abort_flag), peer);
-    const int64_t mt = (p.M + C::PAIR_M - 1) / C::PAIR_M, nt = (p.Nd + C::BN - 1) / C::BN;
-    const int64_t units = mt * nt * p.splits;
-    const int64_t npairs = gridDim.x >> 1, pair_id = blockIdx.x >> 1;
+    PairPlan pl;
+    pl.mt = (p.M + C::PAIR_M - 1) / C::PAIR_M;
+    pl.S = p.nk_main + p.lora_steps;
+    pl.T = pl.mt * ((p.Nd + C::BN - 1) / C::BN);
+    pl.dpt = min(p.dp_tiles, pl.T);
+    pl.P = gridDim.x >> 1;
+    pl.base = pl.dpt * pl.S;
+    pl.W = (pl.T - pl.dpt) * pl.S;
+    const int64_t pair_id = blockIdx.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -202,6 +308,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         }
         mbar_init(tfull, 1);
         mbar_init(tempty, 2 * C::EPI_WARPS);
+        for (int i = 0; i < 2 * C::EPI_WARPS; ++i) mbar_init(&fixbar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -229,8 +336,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         if (lane == 0) {
             int64_t g = 0;
             bool alive = true;
-            for (int64_t u = pair_id; u < units && alive; u += npairs) {
-                const PairUnit w = pair_unit(p, u, mt, nt);
+            SegWalk sw = seg_walk(pl, pair_id);
+            PairSeg w;
+            while (alive && seg_next(p, pl, sw, w)) {
                 const int64_t rowA0 = w.m0 + (int64_t)rank * C::SUB, rowA1 = rowA0 + 256;
                 const int64_t ch = w.c0 + (int64_t)rank * C::HN;
                 const uint32_t abytes = (w.two ? 2 : 1) * C::A_BYTES;
@@ -252,7 +360,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         else
                             tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(ch / 2), k);
                     } else {
-                        const int32_t j = (int32_t)(it - w.nmain) * C::BK;
+                        const int32_t j = (int32_t)(w.lbeg + it - w.nmain) * C::BK;
                         mbar_arrive_expect_tx(&full[s], abytes + C::W_BYTES);
                         tma_load_2d(atile(s, 0), &tm_lact, &full[s], j, (int32_t)rowA0);
                         if (w.two) tma_load_2d(atile(s, 1), &tm_lact, &full[s], j, (int32_t)rowA1);
@@ -281,8 +389,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             constexpr uint32_t idesc = idesc_bf16(2 * C::SUB, C::BN, 0, MODE == kDx ? 1 : 0);
             int64_t g = 0, tl = 0;
             bool alive = true;
-            for (int64_t u = pair_id; u < units && alive; u += npairs, ++tl) {
-                const PairUnit w = pair_unit(p, u, mt, nt);
+            SegWalk sw = seg_walk(pl, pair_id);
+            PairSeg w;
+            for (; alive && seg_next(p, pl, sw, w); ++tl) {
                 if (tl > 0 && !pair_wait(tempty, (uint32_t)(tl - 1) & 1, p.wait_ns, (p.kernel_id << 16) | 6,
                                          abort_flag, peer_abort))
                     break;
@@ -297,7 +406,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                     tc_fence_after();
                     int nmma = 4;
                     if (it >= w.nmain) {
-                        const int rem = p.r - (int)(it - w.nmain) * C::BK;
+                        const int rem = p.r - (int)(w.lbeg + it - w.nmain) * C::BK;
                         nmma = rem >= C::BK ? 4 : (rem + 15) / 16;
                     }
                     const uint32_t a0 = smem_u32(atile(s, 0)), a1 = smem_u32(atile(s, 1)), w0 = smem_u32(wtile(s));
@@ -344,26 +453,34 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         // This group's steps (global step g with g % DEC_GROUPS == grp) are
         // walked with a cursor; the absmax code and group scale of the next
         // step are loaded before the current step is waited for and decoded.
+        // (only what the decode needs of a segment: its first step and
+        // main steps, its column tile and its length)
         struct Cursor {
-            int64_t u, it, g;
-            PairUnit w;
+            SegWalk sw;
+            bool live;
+            int64_t it, g, nk, nmain, kbeg, c0;
+        };
+        auto enter = [&](Cursor &c) {
+            PairSeg w = {};
+            c.live = seg_next(p, pl, c.sw, w);
+            c.it = 0;
+            c.nk = w.nk;
+            c.nmain = w.nmain;
+            c.kbeg = w.kbeg;
+            c.c0 = w.c0;
         };
         auto advance = [&](Cursor &c) {
             ++c.it;
             ++c.g;
-            while (c.u < units && c.it >= c.w.nk) {
-                c.u += npairs;
-                c.it = 0;
-                if (c.u < units) c.w = pair_unit(p, c.u, mt, nt);
-            }
+            if (c.live && c.it >= c.nk) enter(c);
         };
         auto fetch = [&](const Cursor &c, int &qv, float &sv) {
             qv = 0;
             sv = 0.0f;
-            if (c.u >= units || c.it >= c.w.nmain) return false;
-            const int64_t ch = c.w.c0 + (int64_t)rank * C::HN;
-            const int64_t wrow = MODE == kFwd ? ch + dt : (c.w.kbeg + c.it) * C::BK + nl;
-            const int64_t kb = MODE == kFwd ? c.w.kbeg + c.it : ch / kBlock + b2;
+            if (!c.live || c.it >= c.nmain) return false;
+            const int64_t ch = c.c0 + (int64_t)rank * C::HN;
+            const int64_t wrow = MODE == kFwd ? ch + dt : (c.kbeg + c.it) * C::BK + nl;
+            const int64_t kb = MODE == kFwd ? c.kbeg + c.it : ch / kBlock + b2;
             if (wrow >= p.w_rows || kb >= kblocks) return false;
             const int64_t bidx = wrow * kblocks + kb;
             qv = __ldg(p.q + bidx);
@@ -371,22 +488,21 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             return true;
         };
         Cursor cur;
-        cur.u = pair_id;
-        cur.it = 0;
+        cur.sw = seg_walk(pl, pair_id);
         cur.g = 0;
-        if (cur.u < units) cur.w = pair_unit(p, cur.u, mt, nt);
+        enter(cur);
         for (int i = 0; i < grp; ++i) advance(cur);
         Cursor nxt = cur;
         for (int i = 0; i < C::DEC_GROUPS; ++i) advance(nxt);
         int qv, qn;
         float sv, sn;
         bool valid = fetch(cur, qv, sv);
-        while (cur.u < units) {
+        while (cur.live) {
             const bool valid_n = fetch(nxt, qn, sn);
             const int s = (int)(cur.g % C::STAGES);
             const uint32_t par = (uint32_t)(cur.g / C::STAGES) & 1;
             if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) break;
-            if (cur.it < cur.w.nmain) {
+            if (cur.it < cur.nmain) {
                 uint8_t *wt = wtile(s);
                 const uint8_t *ct = ctile(s);
                 uint32_t o[8][4];
@@ -419,26 +535,71 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         // --------------------------------------------------- epilogue ----
         // Warp e of the 8 reads TMEM lanes 32 * (warp % 4) .. + 31 (one row of
         // each 128-row sub-tile per thread) and the accumulator columns of
-        // its half, chalf = e / 4 (128 of the 256), 64 columns per wait. The
-        // accumulators are released to the next unit's MMAs right after the
-        // last read; the stores (one 128-byte row segment per thread and
-        // batch) drain while the next unit runs.
+        // its half, chalf = e / 4 (128 of the 256), 64 columns per wait
+        // (batch b = 2 * sub + column pair). The accumulators are released to
+        // the next segment's MMAs right after the last read; the stores (one
+        // 128-byte row segment per thread and batch) drain while it runs.
+        //
+        // A partial tile goes to the pair's slot in this warp's own order:
+        // [CTA][warp][batch][8-column chunk][lane][8 fp32], so every store
+        // instruction writes 1 KB of consecutive bytes. Finishing a tile, the
+        // warp fetches the matching 8 KB pieces of the contributors' slots
+        // into the (now idle) stage buffers with bulk copies, two in flight,
+        // and adds them in pair order.
         const int ew = warp - (2 + C::GROUP_WARPS * C::DEC_GROUPS);  // 0..7
         const int quarter = warp & 3, chalf = ew >> 2;
         const int r = quarter * 32 + lane;  // row within the sub-tile
         const uint32_t tempty_addr0 = mapa_u32(smem_u32(tempty), 0);
+        uint8_t *fixbuf = smem + ew * 16384;  // two 8 KB buffers of this warp
+        int fx_issued = 0, fx_waited = 0;     // pieces fetched / consumed (one head segment at most)
         int64_t tl = 0;
-        for (int64_t u = pair_id; u < units; u += npairs, ++tl) {
-            const PairUnit w = pair_unit(p, u, mt, nt);
+        SegWalk sw = seg_walk(pl, pair_id);
+        PairSeg w;
+        for (; seg_next(p, pl, sw, w); ++tl) {
             if (!pair_wait(tfull, (uint32_t)tl & 1, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag, peer_abort))
                 break;
             tc_fence_after();
-            for (int sub = 0; sub < 2; ++sub) {
+            const int nb = w.two ? 4 : 2;
+            // contributors of a head segment: pairs pair_id + 1 .. qend - 1
+            int64_t qend = pair_id + 1;
+            if (w.role == kSegHead) {
+                const int64_t tend = (w.t + 1) * pl.S;
+                while (qend < pl.P && pl.begin(qend) < tend) ++qend;
+            }
+            const int nq = (int)(qend - pair_id - 1);
+            const int nitems = nq * nb;
+            auto fetch_piece = [&](int i) {
+                if (i >= nitems) return;
+                fx_issued = i + 1;
+                if (lane != 0) return;
+                const int b = i / nq;
+                const int64_t q = pair_id + 1 + i % nq;
+                const float *src = p.slots + q * kSlotFloats + (((int64_t)rank * 8 + ew) * 4 + b) * 2048;
+                uint64_t *fb = &fixbar[ew * 2 + (i & 1)];
+                mbar_arrive_expect_tx(fb, 8192);
+                bulk_g2s(fixbuf + (i & 1) * 8192, src, 8192, fb);
+            };
+            if (nq > 0) {
+                bool ok = true;
+                if (lane == 0) {
+                    for (int64_t q = pair_id + 1; q < qend && ok; ++q)
+                        ok = flag_wait(p.flags + (q * 2 + rank) * 8 + ew, p.wait_ns, (p.kernel_id << 16) | 7,
+                                       abort_flag, peer_abort);
+                    if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                fetch_piece(0);
+                fetch_piece(1);
+            }
+            bool alive = true;
+            for (int sub = 0; sub < 2 && alive; ++sub) {
                 if (sub == 1 && !w.two) break;
                 const int64_t row = w.m0 + sub * 256 + (int64_t)rank * C::SUB + r;
 #pragma unroll 1
                 for (int cp = 0; cp < 2; ++cp) {
                     const int col = chalf * 128 + cp * 64;
+                    const int b = sub * 2 + cp;
                     uint32_t v[64];
                     const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(sub * 256 + col);
                     tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(v));
@@ -446,56 +607,92 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                     tmem_ld_wait();
                     if (sub == (w.two ? 1 : 0) && cp == 1) {
                         // every accumulator column this warp owns has been read:
-                        // the MMAs of the next unit may overwrite them
+                        // the MMAs of the next segment may overwrite them
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive_cluster(tempty_addr0);
                     }
+                    if (w.role == kSegPart) {
+                        float *dst = p.slots + pair_id * kSlotFloats + (((int64_t)rank * 8 + ew) * 4 + b) * 2048;
+#pragma unroll
+                        for (int jc = 0; jc < 8; ++jc) {
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) pk[e] = v[8 * jc + e];
+                            st_global_v8(dst + (jc * 32 + lane) * 8, pk);
+                        }
+                        continue;
+                    }
+                    for (int qi = 0; qi < nq; ++qi) {
+                        const int i = b * nq + qi;
+                        if (!pair_wait(&fixbar[ew * 2 + (i & 1)], (uint32_t)(i >> 1) & 1, p.wait_ns,
+                                       (p.kernel_id << 16) | 8, abort_flag, peer_abort)) {
+                            alive = false;
+                            break;
+                        }
+                        fx_waited = i + 1;
+                        const float *src = reinterpret_cast<const float *>(fixbuf + (i & 1) * 8192);
+#pragma unroll
+                        for (int jc = 0; jc < 8; ++jc) {
+                            const float4 a0 = *reinterpret_cast<const float4 *>(src + (jc * 32 + lane) * 8);
+                            const float4 a1 = *reinterpret_cast<const float4 *>(src + (jc * 32 + lane) * 8 + 4);
+                            const float add[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                v[8 * jc + e] = __float_as_uint(__uint_as_float(v[8 * jc + e]) + add[e]);
+                        }
+                        __syncwarp();  // every lane has read the buffer before it is refilled
+                        fetch_piece(i + 2);
+                    }
+                    if (!alive) break;
                     if (row >= p.M) continue;
                     const int64_t ncol = p.Nd - (w.c0 + col);  // valid columns from here
-                    if (p.splits > 1) {
-                        float *dstf = p.part + ((int64_t)w.z * p.M + row) * p.Nd + w.c0 + col;
-                        if (ncol >= 64 && ((p.Nd & 3) == 0)) {
+                    uint16_t *dstp = p.out + row * p.ldo + w.c0 + col;
+                    if (ncol >= 64 && p.out_v8) {
+                        // four 32-byte stores: whole sectors of the row segment
 #pragma unroll
-                            for (int g4 = 0; g4 < 16; ++g4)
-                                reinterpret_cast<float4 *>(dstf)[g4] =
-                                    make_float4(__uint_as_float(v[4 * g4]), __uint_as_float(v[4 * g4 + 1]),
-                                                __uint_as_float(v[4 * g4 + 2]), __uint_as_float(v[4 * g4 + 3]));
-                        } else {
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t pk[8];
 #pragma unroll
-                            for (int e = 0; e < 64; ++e)
-                                if (e < ncol) dstf[e] = __uint_as_float(v[e]);
+                            for (int e = 0; e < 8; ++e)
+                                pk[e] = pack_bf16x2(__uint_as_float(v[16 * q + 2 * e]),
+                                                    __uint_as_float(v[16 * q + 2 * e + 1]));
+                            st_global_v8(dstp + 16 * q, pk);
+                        }
+                    } else if (ncol >= 64 && (p.ldo & 7) == 0) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            uint4 pk;
+                            pk.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                            pk.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                            pk.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                            pk.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                            reinterpret_cast<uint4 *>(dstp)[q] = pk;
                         }
                     } else {
-                        uint16_t *dstp = p.out + row * p.ldo + w.c0 + col;
-                        if (ncol >= 64 && p.out_v8) {
-                            // four 32-byte stores: whole sectors of the row segment
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                uint32_t pk[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    pk[e] = pack_bf16x2(__uint_as_float(v[16 * q + 2 * e]),
-                                                        __uint_as_float(v[16 * q + 2 * e + 1]));
-                                st_global_v8(dstp + 16 * q, pk);
-                            }
-                        } else if (ncol >= 64 && (p.ldo & 7) == 0) {
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                uint4 pk;
-                                pk.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                                pk.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                                pk.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                                pk.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                                reinterpret_cast<uint4 *>(dstp)[q] = pk;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 64; ++e)
-                                if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
-                        }
+                        for (int e = 0; e < 64; ++e)
+                            if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
                     }
                 }
+            }
+            if (!alive) break;
+            if (w.role == kSegPart) {
+                // this warp's share of the partial tile is written: raise its flag
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    st_release_gpu(p.flags + (pair_id * 2 + rank) * 8 + ew, 1u);
+                }
+            }
+        }
+        // after an abort: let the fetches still in flight land before the
+        // shared memory is given up
+        if (lane == 0) {
+            for (int i = fx_waited; i < fx_issued; ++i) {
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(&fixbar[ew * 2 + (i & 1)], (uint32_t)(i >> 1) & 1))
+                    if (globaltimer() - t0 > p.wait_ns) break;
             }
         }
     }

@@ -67,6 +67,8 @@ struct SkParams {
     float *o32;
     uint64_t wait_ns;
     unsigned kernel_id;
+    uint32_t *zero;  // problem 0 only: words set to zero once the preceding kernel is done
+    int nzero;
 };
 
 // floats per row of the partial tile kept in shared memory (64 + 4 padding:
@@ -223,6 +225,8 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
     // outputs are visible from here on; the next kernel may start its set-up
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p0.zero && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < p0.nzero; i += blockDim.x) p0.zero[i] = 0u;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----

@@ -157,25 +157,25 @@ SkPlan sk_plan(int64_t rows, int64_t L, int r) {
     return p;
 }
 
-// Contraction splits of the fused GEMM: split only when the 512 x 256 output
-// tiles fill less than three quarters of the 74 CTA pairs, keeping >= 4
-// k-steps per split.
-struct GemmSplit {
-    int splits;
-    int64_t steps_per_split;
+// Stream-K hand-off area of the fused GEMM: the ready flags (zeroed by the
+// skinny kernel that precedes the GEMM in the same call) and one fp32
+// partial-tile slot per CTA pair.
+struct SkArea {
+    uint32_t *flags;
+    float *slots;
 };
-GemmSplit gemm_split(int64_t M, int64_t Nd, int64_t nk_main) {
-    const int64_t units = PairCfg::MAX_PAIRS;
-    const int64_t tiles = cdiv(Nd, PairCfg::BN) * cdiv(M, PairCfg::PAIR_M);
-    int64_t sp = 1;
-    if (tiles * 4 < 3 * units) sp = std::max<int64_t>(1, std::min<int64_t>({units / tiles, nk_main / 4, 8}));
-    const int64_t sps = cdiv(nk_main, sp);
-    return {(int)cdiv(nk_main, sps), sps};
+SkArea take_sk_area(Carve &c) {
+    SkArea a;
+    a.flags = c.take<uint32_t>((size_t)kSkFlagWords);
+    // 32-byte stores into the slots: align within the (16-byte aligned) workspace
+    char *raw = c.take<char>((size_t)kSkPairs * (size_t)kSlotFloats * sizeof(float) + 32);
+    a.slots = raw ? reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(raw) + 31) & ~uintptr_t(31)) : nullptr;
+    return a;
 }
 
 struct FwdWs {
     uint16_t *sU, *Bp;
-    float *part;
+    SkArea sk;
 };
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     const bool tc = M > kSmallMaxM || K > kSmallMaxK;
@@ -183,13 +183,11 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     FwdWs f{};
     if (!tc) {
         f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
-        f.part = c.take<float>(0);
     } else {
         const int rs = lora_rs(r);
-        const GemmSplit g = gemm_split(M, N, K / 64);
         f.sU = c.take<uint16_t>((size_t)M * rs);
         f.Bp = c.take<uint16_t>(r % 8 ? (size_t)N * rs : 0);
-        f.part = c.take<float>(g.splits > 1 ? (size_t)g.splits * M * N : (size_t)0);
+        f.sk = take_sk_area(c);
     }
     if (out) *out = f;
     return c.off;
@@ -211,7 +209,8 @@ GradSplit grad_split(int64_t M, int64_t C) {
 
 struct BwdWs {
     uint16_t *Bt, *sV, *U, *Bp;
-    float *part;
+    float *part;  // CUDA-core path: per-chunk adapter-gradient partials
+    SkArea sk;
 };
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, BwdWs *out) {
     const int r8 = (int)up(r, 8), rp = lora_pad(r), rs = lora_rs(r);
@@ -225,12 +224,10 @@ size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, BwdWs *out) {
         b.U = c.take<uint16_t>((size_t)M * rp);
         b.part = c.take<float>((size_t)r * (size_t)std::max(ga.nchunks * K, gb.nchunks * N));
     } else {
-        const GemmSplit g = gemm_split(M, K, cdiv(N, 64));
-        const size_t part = g.splits > 1 ? (size_t)g.splits * M * K : 0;
         b.sV = c.take<uint16_t>((size_t)M * rs);
         b.U = c.take<uint16_t>((size_t)M * rs);
         b.Bp = c.take<uint16_t>(r % 8 ? (size_t)N * rs : 0);
-        b.part = c.take<float>(part);
+        b.sk = take_sk_area(c);
     }
     if (out) *out = b;
     return c.off;
@@ -320,17 +317,33 @@ int64_t gemm_pairs_resident() {
     return n > 0 ? std::min<int64_t>(n, PairCfg::MAX_PAIRS) : PairCfg::MAX_PAIRS;
 }
 
-// Launches the fused GEMM (forward or dX): on CTA pairs, a persistent grid of
-// at most one pair per two SMs looping over (512 x 256 tile, split) units,
-// launched as a programmatic dependent of the preceding kernel; or on single
-// CTAs over grid (column tiles, row tiles, splits).
+// Schedule of the fused GEMM over its T tiles (S k-steps each) on P resident
+// pairs: data-parallel when the tiles fill the pairs' rounds well enough
+// (at most one round, a whole number of rounds, or a last round at least half
+// full); stream-K over every tile when there are fewer tiles than half the
+// pairs; otherwise data-parallel rounds with the last one-and-a-fraction
+// rounds stream-K.
+struct GemmSched {
+    int64_t dp_tiles, pairs;
+};
+GemmSched gemm_sched(int64_t T, int64_t S, int64_t P) {
+    if (2 * T < P) return {0, std::min(P, T * S)};
+    if (T <= P || T % P == 0 || 2 * (T % P) >= P) return {T, std::min(P, T)};
+    return {(T / P - 1) * P, P};
+}
+
+// Launches the fused GEMM (forward or dX): a persistent grid of CTA pairs (no
+// more than the device holds at once) on the schedule above, launched as a
+// programmatic dependent of the preceding kernel.
 template <int MODE>
 qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUtensorMap &tl, const CUtensorMap &tw,
-                         const TcParams &prm, cudaStream_t s) {
+                         TcParams prm, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    const int64_t units = cdiv(prm.Nd, PairCfg::BN) * cdiv(prm.M, PairCfg::PAIR_M) * prm.splits;
-    const int64_t pairs = std::min<int64_t>(units, gemm_pairs_resident<MODE>());
+    const GemmSched sc = gemm_sched(cdiv(prm.Nd, PairCfg::BN) * cdiv(prm.M, PairCfg::PAIR_M),
+                                    prm.nk_main + prm.lora_steps, gemm_pairs_resident<MODE>());
+    prm.dp_tiles = sc.dp_tiles;
+    const int64_t pairs = sc.pairs;
     cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
     cfg.blockDim = dim3(PairCfg::THREADS);
     cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
@@ -432,7 +445,8 @@ int64_t skinny_chunks(int64_t clusters, int64_t steps) {
 // Launches one skinny problem, or two (j1 != null) of the same kind and
 // contraction length in one grid.
 template <int A_MN, int B_MN>
-qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsigned id) {
+qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsigned id, uint32_t *zero = nullptr,
+                        int nzero = 0) {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
@@ -451,7 +465,10 @@ qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsig
     j1v.pl.spc = j0.pl.spc;
     j1v.pl.chunks = j0.pl.chunks;
     const SkJob &jb = j1 ? *j1 : j0;
-    const SkParams p0 = sk_params(j0, r, id), p1 = sk_params(jb, r, id);
+    SkParams p0 = sk_params(j0, r, id);
+    const SkParams p1 = sk_params(jb, r, id);
+    p0.zero = zero;
+    p0.nzero = nzero;
     const int tiles0 = (int)j0.pl.tiles;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(j0.pl.tiles + (j1 ? j1->pl.tiles : 0)), (unsigned)j0.pl.chunks, (unsigned)j0.pl.zt);
@@ -758,7 +775,8 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         return st;
     // U = X A^T on the tensor cores; U (bf16) to U_save, s*U (bf16) to the workspace
     const SkPlan pu = sk_plan(M, K, r);
-    if ((st = run_skinny<0, 0>(SkJob{&tmX, &tmA, pu, kRedU, scale, U16, r, f.sU, rs, nullptr}, nullptr, r, s, 3)))
+    if ((st = run_skinny<0, 0>(SkJob{&tmX, &tmA, pu, kRedU, scale, U16, r, f.sU, rs, nullptr}, nullptr, r, s, 3,
+                               f.sk.flags, kSkFlagWords)))
         return st;
     TcParams prm{};
     prm.M = M;
@@ -774,21 +792,11 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     prm.out = static_cast<uint16_t *>(Y);
     prm.ldo = N;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(Y) & 31) == 0 && (N & 15) == 0;
-    const GemmSplit gs = gemm_split(M, N, prm.nk_main);
-    prm.splits = gs.splits;
-    prm.steps_per_split = gs.steps_per_split;
-    prm.part = f.part;
+    prm.flags = f.sk.flags;
+    prm.slots = f.sk.slots;
     prm.wait_ns = wait_ns();
     prm.kernel_id = 1;
     if ((st = launch_gemm<kFwd>(tmX, tmC, tmU, tmB, prm, s))) return st;
-    if (gs.splits > 1) {
-        {
-            ProfScope ps(QLORA_KERNEL_FWD_GEMM, s);
-            k_split_reduce<<<(unsigned)cdiv(cdiv(M * N, 4), 256), 256, 0, s>>>(f.part, gs.splits, M, N,
-                                                                             static_cast<uint16_t *>(Y), N);
-        }
-        if ((st = launch_check("k_split_reduce"))) return st;
-    }
     return ok();
 }
 
@@ -927,7 +935,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     // V = dY B -> sV = bf16(s * V)
     const SkPlan pv = sk_plan(M, N, r);
     if ((st = run_skinny<0, 1>(SkJob{&tmD, &tmBp, pv, kRedV, scale, nullptr, 0, b.sV, rs, nullptr}, nullptr, r, s,
-                               4)))
+                               4, b.sk.flags, kSkFlagWords)))
         return st;
     // U recomputed as X A^T when the forward's U is not given
     if (!U_saved) {
@@ -955,21 +963,11 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     prm.out = static_cast<uint16_t *>(dX);
     prm.ldo = K;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(dX) & 31) == 0 && (K & 15) == 0;
-    const GemmSplit gs = gemm_split(M, K, prm.nk_main);
-    prm.splits = gs.splits;
-    prm.steps_per_split = gs.steps_per_split;
-    prm.part = b.part;
+    prm.flags = b.sk.flags;
+    prm.slots = b.sk.slots;
     prm.wait_ns = wait_ns();
     prm.kernel_id = 2;
     if ((st = launch_gemm<kDx>(tmD, tmC, tmV, tmA, prm, s))) return st;
-    if (gs.splits > 1) {
-        {
-            ProfScope ps(QLORA_KERNEL_DX_GEMM, s);
-            k_split_reduce<<<(unsigned)cdiv(cdiv(M * K, 4), 256), 256, 0, s>>>(b.part, gs.splits, M, K,
-                                                                             static_cast<uint16_t *>(dX), K);
-        }
-        if ((st = launch_check("k_split_reduce"))) return st;
-    }
     // dA = (sV)^T X (rows k of dA^T) and dB = s dY^T U (rows n), both
     // contracting over the M tokens, in one launch
     const SkJob ja{&tmXmn, &tmVmn, sk_plan(K, M, r), kRedDA, 1.0f, nullptr, 0, nullptr, 0, dA};
