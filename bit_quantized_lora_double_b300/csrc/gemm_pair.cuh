@@ -12,7 +12,7 @@
 // 2 x 256 rows while each CTA decodes only its half of it: 128 x 64 weights
 // per 64-deep k-step against 2 x (128 x 256 x 64) MACs.
 //
-// Roles per CTA (18 warps):
+// Roles per CTA (14 warps):
 //   warp 0      TMA producer: two 128 x 64 activation tiles and this CTA's
 //               half of the packed-code tile per stage (in the LoRA steps
 //               the s*U or s*V tiles and this CTA's half of the adapter
@@ -20,12 +20,12 @@
 //   warp 1      TMEM allocation (both CTAs); in the even CTA one lane waits
 //               until both halves of a stage are decoded, issues the MMAs and
 //               commits to the stage's `empty` barriers of both CTAs.
-//   warps 2..17 four decode groups of 4 warps, group g taking the k-steps of
-//               stage g: each thread expands one block of 64 codes through
-//               the per-block scaled byte-plane table into the UMMA operand
-//               layout, then arrives on the even CTA's `ready` barrier; after
-//               the last k-step all 16 warps read the accumulators and store
-//               bf16 rows.
+//   warps 2..9  two decode groups of 4 warps taking alternate k-steps: each
+//               thread expands one block of 64 codes through the per-block
+//               scaled byte-plane table into the UMMA operand layout, then
+//               arrives on the even CTA's `ready` barrier.
+//   warps 10..13 the epilogue, one warp per TMEM lane quarter: accumulators
+//               to bf16 output rows (or to a stream-K partial slot).
 // The LoRA term enters as ceil(r/64) extra k-steps into the same
 // accumulators. Every wait is bounded in time; a wait that runs out records
 // the error word, raises the abort flag in both CTAs, and the kernel drains
@@ -51,10 +51,12 @@ struct PairCfg {
     static constexpr int C_BYTES = HN * BK / 2;   // 4 KB: this CTA's half of the codes
     static constexpr int STAGE_BYTES = W_BYTES + 2 * A_BYTES + C_BYTES;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 4 * 4096 + 1024;
     static constexpr int GROUP_WARPS = 4;         // decode warps per group
     static constexpr int DEC_GROUPS = 2;          // groups take alternate k-steps
-    static constexpr int EPI_WARPS = 8;           // two per TMEM lane quarter (column halves)
+    static constexpr int EPI_WARPS = 4;           // one per TMEM lane quarter
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES + BAR_BYTES;  // per epilogue warp: 4 KB output staging
+    static constexpr int NBATCH = 8;              // 64-column batches per warp and tile (2 sub-tiles x 4)
     static constexpr int THREADS = 64 + 32 * (GROUP_WARPS * DEC_GROUPS + EPI_WARPS);
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int MAX_PAIRS = 74;
@@ -533,12 +535,14 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         }
     } else {
         // --------------------------------------------------- epilogue ----
-        // Warp e of the 8 reads TMEM lanes 32 * (warp % 4) .. + 31 (one row of
-        // each 128-row sub-tile per thread) and the accumulator columns of
-        // its half, chalf = e / 4 (128 of the 256), 64 columns per wait
-        // (batch b = 2 * sub + column pair). The accumulators are released to
-        // the next segment's MMAs right after the last read; the stores (one
-        // 128-byte row segment per thread and batch) drain while it runs.
+        // Epilogue warp e (one per TMEM lane quarter, quarter = warp % 4)
+        // reads lanes 32 * quarter .. + 31 (one row of each 128-row sub-tile
+        // per thread), 64 accumulator columns per wait (batch b = 4 * sub +
+        // column block). The accumulators are released to the next segment's
+        // MMAs right after the last read. Output rows go through the warp's
+        // 4 KB staging buffer (32 rows x 128 bytes, 16-byte chunks rotated by
+        // row so neither side conflicts on banks) and leave as whole 128-byte
+        // lines, four rows per store instruction.
         //
         // A partial tile goes to the pair's slot in this warp's own order:
         // [CTA][warp][batch][8-column chunk][lane][8 fp32], so every store
@@ -546,9 +550,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         // warp fetches the matching 8 KB pieces of the contributors' slots
         // into the (now idle) stage buffers with bulk copies, two in flight,
         // and adds them in pair order.
-        const int ew = warp - (2 + C::GROUP_WARPS * C::DEC_GROUPS);  // 0..7
-        const int quarter = warp & 3, chalf = ew >> 2;
-        const int r = quarter * 32 + lane;  // row within the sub-tile
+        const int ew = warp - (2 + C::GROUP_WARPS * C::DEC_GROUPS);  // 0..3
+        const int quarter = warp & 3;
+        uint8_t *stg = smem + C::EPI_OFF + ew * 4096;
         const uint32_t tempty_addr0 = mapa_u32(smem_u32(tempty), 0);
         uint8_t *fixbuf = smem + ew * 16384;  // two 8 KB buffers of this warp
         int fx_issued = 0, fx_waited = 0;     // pieces fetched / consumed (one head segment at most)
@@ -559,7 +563,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             if (!pair_wait(tfull, (uint32_t)tl & 1, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag, peer_abort))
                 break;
             tc_fence_after();
-            const int nb = w.two ? 4 : 2;
+            const int nb = w.two ? C::NBATCH : C::NBATCH / 2;
             // contributors of a head segment: pairs pair_id + 1 .. qend - 1
             int64_t qend = pair_id + 1;
             if (w.role == kSegHead) {
@@ -574,7 +578,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 if (lane != 0) return;
                 const int b = i / nq;
                 const int64_t q = pair_id + 1 + i % nq;
-                const float *src = p.slots + q * kSlotFloats + (((int64_t)rank * 8 + ew) * 4 + b) * 2048;
+                const float *src =
+                    p.slots + q * kSlotFloats + (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
                 uint64_t *fb = &fixbar[ew * 2 + (i & 1)];
                 mbar_arrive_expect_tx(fb, 8192);
                 bulk_g2s(fixbuf + (i & 1) * 8192, src, 8192, fb);
@@ -583,7 +588,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 bool ok = true;
                 if (lane == 0) {
                     for (int64_t q = pair_id + 1; q < qend && ok; ++q)
-                        ok = flag_wait(p.flags + (q * 2 + rank) * 8 + ew, p.wait_ns, (p.kernel_id << 16) | 7,
+                        ok = flag_wait(p.flags + (q * 2 + rank) * C::EPI_WARPS + ew, p.wait_ns, (p.kernel_id << 16) | 7,
                                        abort_flag, peer_abort);
                     if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
@@ -595,17 +600,18 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             bool alive = true;
             for (int sub = 0; sub < 2 && alive; ++sub) {
                 if (sub == 1 && !w.two) break;
-                const int64_t row = w.m0 + sub * 256 + (int64_t)rank * C::SUB + r;
+                const int64_t rbase = w.m0 + sub * 256 + (int64_t)rank * C::SUB + quarter * 32;  // warp's first row
+                const int64_t row = rbase + lane;
 #pragma unroll 1
-                for (int cp = 0; cp < 2; ++cp) {
-                    const int col = chalf * 128 + cp * 64;
-                    const int b = sub * 2 + cp;
+                for (int cb = 0; cb < 4; ++cb) {
+                    const int col = cb * 64;
+                    const int b = sub * 4 + cb;
                     uint32_t v[64];
                     const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(sub * 256 + col);
                     tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(v));
                     tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                     tmem_ld_wait();
-                    if (sub == (w.two ? 1 : 0) && cp == 1) {
+                    if (sub == (w.two ? 1 : 0) && cb == 3) {
                         // every accumulator column this warp owns has been read:
                         // the MMAs of the next segment may overwrite them
                         tc_fence_before();
@@ -613,7 +619,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         if (lane == 0) mbar_arrive_cluster(tempty_addr0);
                     }
                     if (w.role == kSegPart) {
-                        float *dst = p.slots + pair_id * kSlotFloats + (((int64_t)rank * 8 + ew) * 4 + b) * 2048;
+                        float *dst = p.slots + pair_id * kSlotFloats +
+                                     (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
 #pragma unroll
                         for (int jc = 0; jc < 8; ++jc) {
                             uint32_t pk[8];
@@ -645,35 +652,36 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         fetch_piece(i + 2);
                     }
                     if (!alive) break;
-                    if (row >= p.M) continue;
                     const int64_t ncol = p.Nd - (w.c0 + col);  // valid columns from here
-                    uint16_t *dstp = p.out + row * p.ldo + w.c0 + col;
-                    if (ncol >= 64 && p.out_v8) {
-                        // four 32-byte stores: whole sectors of the row segment
+                    if (ncol >= 64 && p.out_v4) {
+                        // row `lane` into the staging buffer: chunk c (8 columns) at c ^ (lane & 7)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t pk[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                pk[e] = pack_bf16x2(__uint_as_float(v[16 * q + 2 * e]),
-                                                    __uint_as_float(v[16 * q + 2 * e + 1]));
-                            st_global_v8(dstp + 16 * q, pk);
-                        }
-                    } else if (ncol >= 64 && (p.ldo & 7) == 0) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
+                        for (int c = 0; c < 8; ++c) {
                             uint4 pk;
-                            pk.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                            pk.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                            pk.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                            pk.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                            reinterpret_cast<uint4 *>(dstp)[q] = pk;
+                            pk.x = pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1]));
+                            pk.y = pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3]));
+                            pk.z = pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]));
+                            pk.w = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
+                            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = pk;
                         }
-                    } else {
+                        __syncwarp();
+                        // 8 lanes per row, 4 rows per instruction: whole lines
+                        const int ch = lane & 7;
 #pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
+                        for (int j = 0; j < 8; ++j) {
+                            const int rr = j * 4 + (lane >> 3);
+                            const uint4 val = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                            if (rbase + rr < p.M)
+                                *reinterpret_cast<uint4 *>(p.out + (rbase + rr) * p.ldo + w.c0 + col + ch * 8) = val;
+                        }
+                        __syncwarp();  // the buffer is read before the next batch refills it
+                        continue;
                     }
+                    if (row >= p.M) continue;
+                    uint16_t *dstp = p.out + row * p.ldo + w.c0 + col;
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));
                 }
             }
             if (!alive) break;
@@ -682,7 +690,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
-                    st_release_gpu(p.flags + (pair_id * 2 + rank) * 8 + ew, 1u);
+                    st_release_gpu(p.flags + (pair_id * 2 + rank) * C::EPI_WARPS + ew, 1u);
                 }
             }
         }

@@ -20,8 +20,8 @@ enum { kFwd = 0, kDx = 1 };
 // Contraction steps are 64 deep (one NF4 block of a weight row).
 constexpr int kGemmBK = 64;
 
-// Stream-K hand-off area: per pair (at most 74), 2 CTAs x 8 epilogue warps
-// of one ready flag each, and a 512 x 256 fp32 partial tile.
+// Stream-K hand-off area: per pair (at most 74), room for 16 ready flags (one
+// per CTA and epilogue warp) and a 512 x 256 fp32 partial tile.
 constexpr int kSkPairs = 74;
 constexpr int kSkFlagWords = kSkPairs * 16;
 constexpr int64_t kSlotFloats = 512 * 256;
@@ -47,7 +47,7 @@ struct TcParams {
     int64_t dp_tiles;      // tiles t < dp_tiles run data-parallel, the rest stream-K
     uint64_t wait_ns;
     unsigned kernel_id;
-    int out_v8;            // out and ldo allow 32-byte stores of 64-column segments
+    int out_v4;            // out and ldo allow 16-byte stores of 8-column chunks
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {

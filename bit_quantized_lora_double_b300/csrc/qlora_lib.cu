@@ -791,7 +791,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     prm.mean = w->absmax_mean;
     prm.out = static_cast<uint16_t *>(Y);
     prm.ldo = N;
-    prm.out_v8 = (reinterpret_cast<uintptr_t>(Y) & 31) == 0 && (N & 15) == 0;
+    prm.out_v4 = (reinterpret_cast<uintptr_t>(Y) & 15) == 0 && (N & 7) == 0;
     prm.flags = f.sk.flags;
     prm.slots = f.sk.slots;
     prm.wait_ns = wait_ns();
@@ -962,7 +962,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     prm.mean = w->absmax_mean;
     prm.out = static_cast<uint16_t *>(dX);
     prm.ldo = K;
-    prm.out_v8 = (reinterpret_cast<uintptr_t>(dX) & 31) == 0 && (K & 15) == 0;
+    prm.out_v4 = (reinterpret_cast<uintptr_t>(dX) & 15) == 0 && (K & 7) == 0;
     prm.flags = b.sk.flags;
     prm.slots = b.sk.slots;
     prm.wait_ns = wait_ns();
