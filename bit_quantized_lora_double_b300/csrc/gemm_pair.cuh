@@ -324,6 +324,23 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         prefetch_tmap(&tm_codes);
         prefetch_tmap(&tm_lact);
         prefetch_tmap(&tm_lw);
+        // the first steps' activation and code tiles into L2 while the
+        // preceding kernel finishes (L2 stays coherent with its writes)
+        SegWalk sw = seg_walk(pl, pair_id);
+        PairSeg w;
+        if (seg_next(p, pl, sw, w)) {
+            const int64_t rowA0 = w.m0 + (int64_t)rank * C::SUB;
+            const int64_t ch = w.c0 + (int64_t)rank * C::HN;
+            for (int64_t it = 0; it < w.nmain && it < C::STAGES; ++it) {
+                const int32_t k = (int32_t)((w.kbeg + it) * C::BK);
+                tma_prefetch_2d(&tm_act, k, (int32_t)rowA0);
+                if (w.two) tma_prefetch_2d(&tm_act, k, (int32_t)(rowA0 + 256));
+                if (MODE == kFwd)
+                    tma_prefetch_2d(&tm_codes, k / 2, (int32_t)ch);
+                else
+                    tma_prefetch_2d(&tm_codes, (int32_t)(ch / 2), k);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();

@@ -212,6 +212,17 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(tm_a);
         prefetch_tmap(tm_b);
+        // the first stages' streamed tiles into L2 while the preceding kernel
+        // finishes (L2 stays coherent with its writes)
+        for (int64_t it = 0; it < nsteps && it < 4; ++it) {
+            const int32_t l = (int32_t)(l0 + it * C::BK);
+            if (A_MN) {
+                tma_prefetch_2d(tm_a, (int32_t)row0, l);
+                tma_prefetch_2d(tm_a, (int32_t)(row0 + 64), l);
+            } else {
+                tma_prefetch_2d(tm_a, l, (int32_t)row0);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -357,7 +368,9 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
             }
         }
         __syncwarp();
-        cluster_sync_all();  // the partials stay alive until the sums are read
+        // the partials stay alive until every remote read has returned (the
+        // sums are already stored: no ordering of memory needed here)
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
     }
     __syncthreads();
     if (warp == 1) {

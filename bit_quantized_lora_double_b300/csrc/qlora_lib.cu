@@ -321,13 +321,14 @@ int64_t gemm_pairs_resident() {
 // pairs: data-parallel when the tiles fill the pairs' rounds well enough
 // (at most one round, a whole number of rounds, or a last round at least half
 // full); stream-K over every tile when there are fewer tiles than half the
-// pairs; otherwise data-parallel rounds with the last one-and-a-fraction
-// rounds stream-K.
+// pairs (on at most three pairs per tile: each more partial to add back
+// costs the finishing pair more than the shorter share saves); otherwise
+// data-parallel rounds with the last one-and-a-fraction rounds stream-K.
 struct GemmSched {
     int64_t dp_tiles, pairs;
 };
 GemmSched gemm_sched(int64_t T, int64_t S, int64_t P) {
-    if (2 * T < P) return {0, std::min(P, T * S)};
+    if (2 * T < P) return {0, std::min({P, T * S, 3 * T})};
     if (T <= P || T % P == 0 || 2 * (T % P) >= P) return {T, std::min(P, T)};
     return {(T / P - 1) * P, P};
 }
