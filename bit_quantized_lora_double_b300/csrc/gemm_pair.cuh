@@ -219,14 +219,14 @@ __device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &p
     PairSeg w;
     w.t = g / pl.S;
     const int64_t k0 = g - w.t * pl.S, k1 = min(pl.S, k0 + (end - g));
-    w.m0 = (w.t % pl.mt) * PairCfg::PAIR_M;
+    w.m0 = (w.t % pl.mt) * p.tile_rows;
     w.c0 = (w.t / pl.mt) * PairCfg::BN;
     w.kbeg = k0;
     w.nmain = max((int64_t)0, min(k1, p.nk_main) - k0);
     w.lbeg = max(k0, p.nk_main) - p.nk_main;
     w.nk = k1 - k0;
     w.role = k0 == 0 ? (k1 == pl.S ? kSegFull : kSegHead) : kSegPart;
-    w.two = w.m0 + 256 < p.M;
+    w.two = p.tile_rows == PairCfg::PAIR_M && w.m0 + 256 < p.M;
     return w;
 }
 
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     const uint32_t peer = rank ^ 1u;
     const uint32_t peer_abort = mapa_u32(smem_u32((const void *)abort_flag), peer);
     PairPlan pl;
-    pl.mt = (p.M + C::PAIR_M - 1) / C::PAIR_M;
+    pl.mt = (p.M + p.tile_rows - 1) / p.tile_rows;
     pl.S = p.nk_main + p.lora_steps;
     pl.T = pl.mt * ((p.Nd + C::BN - 1) / C::BN);
     pl.dpt = min(p.dp_tiles, pl.T);

@@ -45,6 +45,7 @@ struct TcParams {
     uint32_t *flags;
     float *slots;
     int64_t dp_tiles;      // tiles t < dp_tiles run data-parallel, the rest stream-K
+    int tile_rows;         // rows per tile: 512 (two 256-row sub-tiles) or 256 (one)
     uint64_t wait_ns;
     unsigned kernel_id;
     int out_v4;            // out and ldo allow 16-byte stores of 8-column chunks

@@ -341,8 +341,13 @@ qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUt
                          TcParams prm, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    const GemmSched sc = gemm_sched(cdiv(prm.Nd, PairCfg::BN) * cdiv(prm.M, PairCfg::PAIR_M),
-                                    prm.nk_main + prm.lora_steps, gemm_pairs_resident<MODE>());
+    // Very few tiles of 512 rows (fewer than a quarter of the pairs): tiles
+    // of 256 rows instead, twice as many for the pairs to share (the decoded
+    // weight tile then feeds only 256 rows per k-step, so this pays only
+    // when the pairs would otherwise sit mostly idle).
+    const int64_t P = gemm_pairs_resident<MODE>(), nt = cdiv(prm.Nd, PairCfg::BN);
+    prm.tile_rows = 4 * nt * cdiv(prm.M, PairCfg::PAIR_M) < P ? PairCfg::PAIR_M / 2 : PairCfg::PAIR_M;
+    const GemmSched sc = gemm_sched(nt * cdiv(prm.M, (int64_t)prm.tile_rows), prm.nk_main + prm.lora_steps, P);
     prm.dp_tiles = sc.dp_tiles;
     const int64_t pairs = sc.pairs;
     cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);

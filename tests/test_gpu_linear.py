@@ -70,6 +70,10 @@ def run_and_check(g, oracle, M, N, K, r, scale, seed, **kw):
     (70, 100, 192, 8, 2.0),        # tensor-core forward, CUDA-core backward (N % 8 != 0)
     (32, 2048, 1024, 16, 2.0),     # largest few-token forward (four 8-token tiles)
     (24, 512, 14336, 16, 2.0),     # few tokens, longest K of the table
+    # fused-GEMM schedules on 74 CTA pairs (tiles of 512 x 256):
+    (2048, 9728, 128, 16, 2.0),    # forward: 152 tiles, one data-parallel round + stream-K over 78
+    (2048, 128, 9728, 16, 2.0),    # dX: the same split on the backward
+    (2148, 4000, 192, 8, 1.0),     # stream-K over 80 tiles, 100-row last row tile, ragged N
 ])
 def test_fwd_bwd_parity(g, oracle, M, N, K, r, scale):
     run_and_check(g, oracle, M, N, K, r, scale, seed=3000 + M + N + r)
