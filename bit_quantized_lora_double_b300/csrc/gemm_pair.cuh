@@ -50,19 +50,23 @@ struct PairCfg {
     static constexpr int W_BYTES = HN * BK * 2;   // 16 KB: this CTA's half of W' (or adapter)
     static constexpr int C_BYTES = HN * BK / 2;   // 4 KB: this CTA's half of the codes
     static constexpr int STAGE_BYTES = W_BYTES + 2 * A_BYTES + C_BYTES;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 4 * 4096 + 1024;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int NFIX = 6;                // 8 KB partial pieces in flight per epilogue warp when finishing
     static constexpr int GROUP_WARPS = 4;         // decode warps per group
     static constexpr int DEC_GROUPS = 2;          // groups take alternate k-steps
     static constexpr int EPI_WARPS = 4;           // one per TMEM lane quarter
-    static constexpr int EPI_OFF = STAGES * STAGE_BYTES + BAR_BYTES;  // per epilogue warp: 4 KB output staging
+    // per epilogue warp: 4 KB output staging, 1 KB aligned (128-byte swizzle)
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES + 1024;
+    static constexpr int SMEM_BYTES = EPI_OFF + 4 * 4096 + 1024;
     static constexpr int NBATCH = 8;              // 64-column batches per warp and tile (2 sub-tiles x 4)
     static constexpr int THREADS = 64 + 32 * (GROUP_WARPS * DEC_GROUPS + EPI_WARPS);
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int MAX_PAIRS = 74;
 };
 static_assert(PairCfg::MAX_PAIRS == kSkPairs, "one stream-K slot and flag set per pair");
-static_assert(PairCfg::EPI_WARPS * 16384 <= PairCfg::STAGES * PairCfg::STAGE_BYTES,
+static_assert(PairCfg::SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(PairCfg::BAR_BYTES <= 1024 && PairCfg::EPI_OFF % 1024 == 0, "barriers before the staging tiles");
+static_assert(PairCfg::EPI_WARPS * PairCfg::NFIX * 8192 <= PairCfg::STAGES * PairCfg::STAGE_BYTES,
               "finishing buffers live in the stage ring");
 
 // ---- cta_group::2 wrappers -------------------------------------------------
@@ -270,7 +274,7 @@ template <int MODE>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                 const __grid_constant__ CUtensorMap tm_lact, const __grid_constant__ CUtensorMap tm_lw,
-                const TcParams p) {
+                const __grid_constant__ CUtensorMap tm_out, const TcParams p) {
     using C = PairCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     uint64_t *tfull = bar + 3 * C::STAGES;      // accumulators complete (commit from the even CTA)
     uint64_t *tempty = bar + 3 * C::STAGES + 1; // even CTA: accumulators drained (8 warp arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * C::STAGES + 2);
-    uint64_t *fixbar = bar + 16;                // 2 per epilogue warp: partial tiles fetched for finishing
+    uint64_t *fixbar = bar + 16;                // NFIX per epilogue warp: partial pieces fetched for finishing
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     auto wtile = [&](int s) { return smem + s * C::STAGE_BYTES; };
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         }
         mbar_init(tfull, 1);
         mbar_init(tempty, 2 * C::EPI_WARPS);
-        for (int i = 0; i < 2 * C::EPI_WARPS; ++i) mbar_init(&fixbar[i], 1);
+        for (int i = 0; i < C::NFIX * C::EPI_WARPS; ++i) mbar_init(&fixbar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -324,6 +328,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         prefetch_tmap(&tm_codes);
         prefetch_tmap(&tm_lact);
         prefetch_tmap(&tm_lw);
+        if (p.out_v4) prefetch_tmap(&tm_out);
         // the first steps' activation and code tiles into L2 while the
         // preceding kernel finishes (L2 stays coherent with its writes)
         SegWalk sw = seg_walk(pl, pair_id);
@@ -565,13 +570,13 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         // [CTA][warp][batch][8-column chunk][lane][8 fp32], so every store
         // instruction writes 1 KB of consecutive bytes. Finishing a tile, the
         // warp fetches the matching 8 KB pieces of the contributors' slots
-        // into the (now idle) stage buffers with bulk copies, two in flight,
+        // into the (now idle) stage buffers with bulk copies, NFIX in flight,
         // and adds them in pair order.
         const int ew = warp - (2 + C::GROUP_WARPS * C::DEC_GROUPS);  // 0..3
         const int quarter = warp & 3;
         uint8_t *stg = smem + C::EPI_OFF + ew * 4096;
         const uint32_t tempty_addr0 = mapa_u32(smem_u32(tempty), 0);
-        uint8_t *fixbuf = smem + ew * 16384;  // two 8 KB buffers of this warp
+        uint8_t *fixbuf = smem + ew * (C::NFIX * 8192);  // NFIX 8 KB buffers of this warp
         int fx_issued = 0, fx_waited = 0;     // pieces fetched / consumed (one head segment at most)
         int64_t tl = 0;
         SegWalk sw = seg_walk(pl, pair_id);
@@ -597,9 +602,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 const int64_t q = pair_id + 1 + i % nq;
                 const float *src =
                     p.slots + q * kSlotFloats + (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
-                uint64_t *fb = &fixbar[ew * 2 + (i & 1)];
+                uint64_t *fb = &fixbar[ew * C::NFIX + i % C::NFIX];
                 mbar_arrive_expect_tx(fb, 8192);
-                bulk_g2s(fixbuf + (i & 1) * 8192, src, 8192, fb);
+                bulk_g2s(fixbuf + (i % C::NFIX) * 8192, src, 8192, fb);
             };
             if (nq > 0) {
                 bool ok = true;
@@ -611,8 +616,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                fetch_piece(0);
-                fetch_piece(1);
+                for (int i = 0; i < C::NFIX; ++i) fetch_piece(i);
             }
             bool alive = true;
             for (int sub = 0; sub < 2 && alive; ++sub) {
@@ -649,13 +653,13 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                     }
                     for (int qi = 0; qi < nq; ++qi) {
                         const int i = b * nq + qi;
-                        if (!pair_wait(&fixbar[ew * 2 + (i & 1)], (uint32_t)(i >> 1) & 1, p.wait_ns,
+                        if (!pair_wait(&fixbar[ew * C::NFIX + i % C::NFIX], (uint32_t)(i / C::NFIX) & 1, p.wait_ns,
                                        (p.kernel_id << 16) | 8, abort_flag, peer_abort)) {
                             alive = false;
                             break;
                         }
                         fx_waited = i + 1;
-                        const float *src = reinterpret_cast<const float *>(fixbuf + (i & 1) * 8192);
+                        const float *src = reinterpret_cast<const float *>(fixbuf + (i % C::NFIX) * 8192);
 #pragma unroll
                         for (int jc = 0; jc < 8; ++jc) {
                             const float4 a0 = *reinterpret_cast<const float4 *>(src + (jc * 32 + lane) * 8);
@@ -666,12 +670,16 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                                 v[8 * jc + e] = __float_as_uint(__uint_as_float(v[8 * jc + e]) + add[e]);
                         }
                         __syncwarp();  // every lane has read the buffer before it is refilled
-                        fetch_piece(i + 2);
+                        fetch_piece(i + C::NFIX);
                     }
                     if (!alive) break;
                     const int64_t ncol = p.Nd - (w.c0 + col);  // valid columns from here
-                    if (ncol >= 64 && p.out_v4) {
-                        // row `lane` into the staging buffer: chunk c (8 columns) at c ^ (lane & 7)
+                    if (p.out_v4) {
+                        // the previous batch's store has read the staging tile
+                        if (lane == 0) bulk_wait_read<0>();
+                        __syncwarp();
+                        // row `lane` into the staging tile: chunk c (8 columns)
+                        // at c ^ (lane & 7), the tensor map's 128-byte swizzle
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             uint4 pk;
@@ -681,17 +689,14 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                             pk.w = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
                             *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = pk;
                         }
+                        fence_proxy_async_smem();
                         __syncwarp();
-                        // 8 lanes per row, 4 rows per instruction: whole lines
-                        const int ch = lane & 7;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int rr = j * 4 + (lane >> 3);
-                            const uint4 val = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
-                            if (rbase + rr < p.M)
-                                *reinterpret_cast<uint4 *>(p.out + (rbase + rr) * p.ldo + w.c0 + col + ch * 8) = val;
+                        // one TMA store of the 32 x 64 box; rows and columns
+                        // past the output's edge are clipped by the unit
+                        if (lane == 0 && rbase < p.M) {
+                            tma_store_2d(&tm_out, stg, (int32_t)(w.c0 + col), (int32_t)rbase);
+                            bulk_commit();
                         }
-                        __syncwarp();  // the buffer is read before the next batch refills it
                         continue;
                     }
                     if (row >= p.M) continue;
@@ -711,12 +716,14 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 }
             }
         }
+        // the output stores complete before the CTA leaves
+        if (lane == 0) bulk_wait_all();
         // after an abort: let the fetches still in flight land before the
         // shared memory is given up
         if (lane == 0) {
             for (int i = fx_waited; i < fx_issued; ++i) {
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(&fixbar[ew * 2 + (i & 1)], (uint32_t)(i >> 1) & 1))
+                while (!mbar_try_wait(&fixbar[ew * C::NFIX + i % C::NFIX], (uint32_t)(i / C::NFIX) & 1))
                     if (globaltimer() - t0 > p.wait_ns) break;
             }
         }

@@ -48,7 +48,7 @@ struct TcParams {
     int tile_rows;         // rows per tile: 512 (two 256-row sub-tiles) or 256 (one)
     uint64_t wait_ns;
     unsigned kernel_id;
-    int out_v4;            // out and ldo allow 16-byte stores of 8-column chunks
+    int out_v4;            // out is 16-byte aligned and ldo % 8 == 0: stores through the output tensor map
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {

@@ -339,6 +339,15 @@ GemmSched gemm_sched(int64_t T, int64_t S, int64_t P) {
 template <int MODE>
 qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUtensorMap &tl, const CUtensorMap &tw,
                          TcParams prm, cudaStream_t s) {
+    // output tiles leave through a tensor map (32 x 64 boxes, 128-byte
+    // swizzle) when its row pitch and base allow one
+    CUtensorMap to;
+    memset(&to, 0, sizeof to);
+    if (prm.out_v4) {
+        const qlora_status st = make_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, prm.out, prm.Nd, prm.M,
+                                         prm.ldo * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B, "output");
+        if (st) return st;
+    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     // Very few tiles of 512 rows (fewer than a quarter of the pairs): tiles
@@ -365,7 +374,7 @@ qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUt
     cudaError_t e;
     {
         ProfScope ps(MODE == kFwd ? QLORA_KERNEL_FWD_GEMM : QLORA_KERNEL_DX_GEMM, s);
-        e = cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE>, ta, tc, tl, tw, prm);
+        e = cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE>, ta, tc, tl, tw, to, prm);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
