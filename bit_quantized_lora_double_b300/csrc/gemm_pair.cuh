@@ -152,8 +152,9 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64
 }
 
 // Work schedule: data-parallel waves, then a stream-K remainder. The T
-// output tiles of 512 x 256 are numbered with the row tiles of a column tile
-// adjacent; each is S = nk_main + lora_steps k-steps deep. Tiles t < dp_tiles
+// output tiles of 512 x 256 are numbered band by band (kRowBand row tiles per
+// band), with the row tiles of a column tile adjacent inside a band; each is
+// S = nk_main + lora_steps k-steps deep. Tiles t < dp_tiles
 // go data-parallel: pair q of the P pairs computes tiles q, q + P, ... whole,
 // all pairs in step (neighbouring pairs share weight and activation tiles
 // through L2 at the same k). The remaining tiles form one line of
@@ -183,8 +184,13 @@ struct PairSeg {
     bool two;       // the tile has a second 256-row sub-tile
 };
 
+// Row tiles per band of the tile order: the pairs working at the same time
+// touch at most this many row tiles (4096 activation rows at 512-row tiles),
+// so the activations they stream stay in L2 while every column tile passes.
+constexpr int kRowBand = 8;
+
 struct PairPlan {
-    int64_t mt, S, T, dpt, P;
+    int64_t mt, nt, S, T, dpt, P;
     int64_t base, W;  // stream-K line: steps [base, base + W)
     __device__ __forceinline__ int64_t begin(int64_t q) const { return base + W * q / P; }
 };
@@ -223,8 +229,13 @@ __device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &p
     PairSeg w;
     w.t = g / pl.S;
     const int64_t k0 = g - w.t * pl.S, k1 = min(pl.S, k0 + (end - g));
-    w.m0 = (w.t % pl.mt) * p.tile_rows;
-    w.c0 = (w.t / pl.mt) * PairCfg::BN;
+    // tile t -> (row tile, column tile): bands of kRowBand row tiles, the
+    // row tiles of a column tile adjacent inside a band
+    const int64_t band = w.t / (kRowBand * pl.nt);
+    const int64_t rows_in = min((int64_t)kRowBand, pl.mt - band * kRowBand);
+    const int64_t rb = w.t - band * kRowBand * pl.nt;
+    w.m0 = (band * kRowBand + rb % rows_in) * p.tile_rows;
+    w.c0 = (rb / rows_in) * PairCfg::BN;
     w.kbeg = k0;
     w.nmain = max((int64_t)0, min(k1, p.nk_main) - k0);
     w.lbeg = max(k0, p.nk_main) - p.nk_main;
@@ -299,7 +310,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     PairPlan pl;
     pl.mt = (p.M + p.tile_rows - 1) / p.tile_rows;
     pl.S = p.nk_main + p.lora_steps;
-    pl.T = pl.mt * ((p.Nd + C::BN - 1) / C::BN);
+    pl.nt = (p.Nd + C::BN - 1) / C::BN;
+    pl.T = pl.mt * pl.nt;
     pl.dpt = min(p.dp_tiles, pl.T);
     pl.P = gridDim.x >> 1;
     pl.base = pl.dpt * pl.S;

@@ -74,6 +74,7 @@ def run_and_check(g, oracle, M, N, K, r, scale, seed, **kw):
     (2048, 9728, 128, 16, 2.0),    # forward: 152 tiles, one data-parallel round + stream-K over 78
     (2048, 128, 9728, 16, 2.0),    # dX: the same split on the backward
     (2148, 4000, 192, 8, 1.0),     # stream-K over 80 tiles, 100-row last row tile, ragged N
+    (4708, 2048, 128, 8, 1.0),     # ten row tiles: two bands of the tile order, the second partial
 ])
 def test_fwd_bwd_parity(g, oracle, M, N, K, r, scale):
     run_and_check(g, oracle, M, N, K, r, scale, seed=3000 + M + N + r)
