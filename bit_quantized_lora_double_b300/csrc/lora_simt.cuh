@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(256) k_lora_down(const uint16_t *__restrict__ 
                                                    const uint16_t *__restrict__ Q, int r, float s,
                                                    uint16_t *__restrict__ U, int ldu, uint16_t *__restrict__ sU,
                                                    int lds) {
+    // a forward launched as a programmatic dependent (the few-token kernel)
+    // may start streaming its weights now; it waits for U before using it
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t o = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (o >= M * lds) return;

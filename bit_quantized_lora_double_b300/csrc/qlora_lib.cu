@@ -755,9 +755,26 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         {
             ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
             auto kern = nt == 1 ? k_fwd_small<1> : (nt == 2 ? k_fwd_small<2> : k_fwd_small<4>);
-            kern<<<grid, SmallCfg::THREADS, 0, s>>>(tmC, X16, M, K, w->absmax_q, w->absmax_scale, w->absmax_mean, N,
-                                                    f.sU, rp, static_cast<const uint16_t *>(B), r,
-                                                    static_cast<uint16_t *>(Y), wait_ns());
+            // a programmatic dependent of k_lora_down: the weights stream
+            // while U is computed
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(grid);
+            cfg.blockDim = dim3(SmallCfg::THREADS);
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmC, (const uint16_t *)X16, M, K,
+                                                     (const int8_t *)w->absmax_q, (const float *)w->absmax_scale,
+                                                     (const float *)w->absmax_mean, N, (const uint16_t *)f.sU, rp,
+                                                     static_cast<const uint16_t *>(B), r, static_cast<uint16_t *>(Y),
+                                                     wait_ns());
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return fail(QLORA_ERR_CUDA, "k_fwd_small: launch failed: %s", cudaGetErrorString(e));
+            }
         }
         if ((st = launch_check("k_fwd_small"))) return st;
         return ok();

@@ -17,7 +17,8 @@
 // bf16(L[code]) * a' instead of bf16(L[code] * a'): the two differ by at most
 // one bf16 rounding of the weight. The four warps' partial sums meet in
 // shared memory, in warp order, where the LoRA term is added and Y is
-// written as bf16.
+// written as bf16. The kernel is launched as a programmatic dependent of the
+// LoRA down-projection and waits for it only before that last step.
 // Sources: ashishsrivastav.com "QLoRA: Fine-Tuning a 70B on One GPU", section
 // "Double Quantization" (dequantize on the fly); xingyuzhitong.com
 // "Fine-Tuning Memory Requirements", section "QLoRA: quantize the frozen base
@@ -221,6 +222,9 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
         }
     }
     __syncthreads();
+    // launched as a programmatic dependent of the kernel that writes sU:
+    // everything above ran alongside it, its output is visible from here on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // the 16 x M outputs: warp sums in warp order, then the LoRA term
     // sum_j sU[m, j] B[n, j]
     for (int o = threadIdx.x; o < 16 * M; o += C::THREADS) {
