@@ -189,11 +189,37 @@ struct PairSeg {
 // so the activations they stream stay in L2 while every column tile passes.
 constexpr int kRowBand = 8;
 
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
 struct PairPlan {
     int64_t mt, nt, S, T, dpt, P;
     int64_t base, W;  // stream-K line: steps [base, base + W)
-    __device__ __forceinline__ int64_t begin(int64_t q) const { return base + W * q / P; }
+    __host__ __device__ __forceinline__ int64_t begin(int64_t q) const { return base + W * q / P; }
 };
+
+// The schedule of one launch on P pairs (tile_rows and dp_tiles set by the host).
+__host__ __device__ __forceinline__ PairPlan make_plan(const TcParams &p, int64_t P) {
+    PairPlan pl;
+    pl.mt = (p.M + p.tile_rows - 1) / p.tile_rows;
+    pl.S = p.nk_main + p.lora_steps;
+    pl.nt = (p.Nd + PairCfg::BN - 1) / PairCfg::BN;
+    pl.T = pl.mt * pl.nt;
+    pl.dpt = min64(p.dp_tiles, pl.T);
+    pl.P = P;
+    pl.base = pl.dpt * pl.S;
+    pl.W = (pl.T - pl.dpt) * pl.S;
+    return pl;
+}
+
+// The pair finishing tile t (its head, pair q) adds the tails computed by
+// pairs q + 1 .. head_contrib_end(...) - 1: those whose ranges start inside t.
+__host__ __device__ __forceinline__ int64_t head_contrib_end(const PairPlan &pl, int64_t q, int64_t t) {
+    const int64_t tend = (t + 1) * pl.S;
+    int64_t e = q + 1;
+    while (e < pl.P && pl.begin(e) < tend) ++e;
+    return e;
+}
 
 // Walks one pair's segments: its data-parallel tiles, then its stream-K range.
 struct SegWalk {
@@ -202,16 +228,17 @@ struct SegWalk {
     int64_t end;  // end of this pair's stream-K range
 };
 
-__device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &pl, int64_t g, int64_t end);
+__host__ __device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &pl, int64_t g,
+                                                     int64_t end);
 
-__device__ __forceinline__ SegWalk seg_walk(const PairPlan &pl, int64_t q) {
+__host__ __device__ __forceinline__ SegWalk seg_walk(const PairPlan &pl, int64_t q) {
     SegWalk sw;
     sw.dp = q;
     sw.g = pl.begin(q);
     sw.end = pl.begin(q + 1);
     return sw;
 }
-__device__ __forceinline__ bool seg_next(const TcParams &p, const PairPlan &pl, SegWalk &sw, PairSeg &w) {
+__host__ __device__ __forceinline__ bool seg_next(const TcParams &p, const PairPlan &pl, SegWalk &sw, PairSeg &w) {
     if (sw.dp < pl.dpt) {
         w = pair_seg(p, pl, sw.dp * pl.S, sw.dp * pl.S + pl.S);
         sw.dp += pl.P;
@@ -225,20 +252,21 @@ __device__ __forceinline__ bool seg_next(const TcParams &p, const PairPlan &pl, 
     return false;
 }
 
-__device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &pl, int64_t g, int64_t end) {
+__host__ __device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const PairPlan &pl, int64_t g,
+                                                     int64_t end) {
     PairSeg w;
     w.t = g / pl.S;
-    const int64_t k0 = g - w.t * pl.S, k1 = min(pl.S, k0 + (end - g));
+    const int64_t k0 = g - w.t * pl.S, k1 = min64(pl.S, k0 + (end - g));
     // tile t -> (row tile, column tile): bands of kRowBand row tiles, the
     // row tiles of a column tile adjacent inside a band
     const int64_t band = w.t / (kRowBand * pl.nt);
-    const int64_t rows_in = min((int64_t)kRowBand, pl.mt - band * kRowBand);
+    const int64_t rows_in = min64(kRowBand, pl.mt - band * kRowBand);
     const int64_t rb = w.t - band * kRowBand * pl.nt;
     w.m0 = (band * kRowBand + rb % rows_in) * p.tile_rows;
     w.c0 = (rb / rows_in) * PairCfg::BN;
     w.kbeg = k0;
-    w.nmain = max((int64_t)0, min(k1, p.nk_main) - k0);
-    w.lbeg = max(k0, p.nk_main) - p.nk_main;
+    w.nmain = max64(0, min64(k1, p.nk_main) - k0);
+    w.lbeg = max64(k0, p.nk_main) - p.nk_main;
     w.nk = k1 - k0;
     w.role = k0 == 0 ? (k1 == pl.S ? kSegFull : kSegHead) : kSegPart;
     w.two = p.tile_rows == PairCfg::PAIR_M && w.m0 + 256 < p.M;
@@ -307,15 +335,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     const uint32_t rank = pair_rank();
     const uint32_t peer = rank ^ 1u;
     const uint32_t peer_abort = mapa_u32(smem_u32((const void *)abort_flag), peer);
-    PairPlan pl;
-    pl.mt = (p.M + p.tile_rows - 1) / p.tile_rows;
-    pl.S = p.nk_main + p.lora_steps;
-    pl.nt = (p.Nd + C::BN - 1) / C::BN;
-    pl.T = pl.mt * pl.nt;
-    pl.dpt = min(p.dp_tiles, pl.T);
-    pl.P = gridDim.x >> 1;
-    pl.base = pl.dpt * pl.S;
-    pl.W = (pl.T - pl.dpt) * pl.S;
+    const PairPlan pl = make_plan(p, gridDim.x >> 1);
     const int64_t pair_id = blockIdx.x >> 1;
 
     if (threadIdx.x == 0) {
@@ -599,11 +619,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             tc_fence_after();
             const int nb = w.two ? C::NBATCH : C::NBATCH / 2;
             // contributors of a head segment: pairs pair_id + 1 .. qend - 1
-            int64_t qend = pair_id + 1;
-            if (w.role == kSegHead) {
-                const int64_t tend = (w.t + 1) * pl.S;
-                while (qend < pl.P && pl.begin(qend) < tend) ++qend;
-            }
+            const int64_t qend = w.role == kSegHead ? head_contrib_end(pl, pair_id, w.t) : pair_id + 1;
             const int nq = (int)(qend - pair_id - 1);
             const int nitems = nq * nb;
             auto fetch_piece = [&](int i) {

@@ -333,6 +333,19 @@ GemmSched gemm_sched(int64_t T, int64_t S, int64_t P) {
     return {(T / P - 1) * P, P};
 }
 
+// Sets prm.tile_rows and prm.dp_tiles for P resident pairs; returns the pairs
+// to launch. Very few tiles of 512 rows (fewer than a quarter of the pairs):
+// tiles of 256 rows instead, twice as many for the pairs to share (the
+// decoded weight tile then feeds only 256 rows per k-step, so this pays only
+// when the pairs would otherwise sit mostly idle).
+int64_t gemm_schedule(TcParams &prm, int64_t P) {
+    const int64_t nt = cdiv(prm.Nd, PairCfg::BN);
+    prm.tile_rows = 4 * nt * cdiv(prm.M, PairCfg::PAIR_M) < P ? PairCfg::PAIR_M / 2 : PairCfg::PAIR_M;
+    const GemmSched sc = gemm_sched(nt * cdiv(prm.M, (int64_t)prm.tile_rows), prm.nk_main + prm.lora_steps, P);
+    prm.dp_tiles = sc.dp_tiles;
+    return sc.pairs;
+}
+
 // Launches the fused GEMM (forward or dX): a persistent grid of CTA pairs (no
 // more than the device holds at once) on the schedule above, launched as a
 // programmatic dependent of the preceding kernel.
@@ -350,15 +363,7 @@ qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUt
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    // Very few tiles of 512 rows (fewer than a quarter of the pairs): tiles
-    // of 256 rows instead, twice as many for the pairs to share (the decoded
-    // weight tile then feeds only 256 rows per k-step, so this pays only
-    // when the pairs would otherwise sit mostly idle).
-    const int64_t P = gemm_pairs_resident<MODE>(), nt = cdiv(prm.Nd, PairCfg::BN);
-    prm.tile_rows = 4 * nt * cdiv(prm.M, PairCfg::PAIR_M) < P ? PairCfg::PAIR_M / 2 : PairCfg::PAIR_M;
-    const GemmSched sc = gemm_sched(nt * cdiv(prm.M, (int64_t)prm.tile_rows), prm.nk_main + prm.lora_steps, P);
-    prm.dp_tiles = sc.dp_tiles;
-    const int64_t pairs = sc.pairs;
+    const int64_t pairs = gemm_schedule(prm, gemm_pairs_resident<MODE>());
     cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
     cfg.blockDim = dim3(PairCfg::THREADS);
     cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
@@ -516,6 +521,42 @@ qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsig
 extern "C" {
 
 const char *qlora_version(void) { return "qlora-b300 0.1 (sm_103a)"; }
+
+int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lora_steps, int pairs_resident,
+                                  int64_t *out, int64_t cap) {
+    if (M < 1 || Nd < 1 || nk_main < 0 || lora_steps < 0 || nk_main + lora_steps < 1 || pairs_resident < 1 ||
+        pairs_resident > PairCfg::MAX_PAIRS || !out)
+        return -2;
+    if (cap < 4) return -1;
+    TcParams prm{};
+    prm.M = M;
+    prm.Nd = Nd;
+    prm.nk_main = nk_main;
+    prm.lora_steps = lora_steps;
+    const int64_t pairs = gemm_schedule(prm, pairs_resident);
+    const PairPlan pl = make_plan(prm, pairs);
+    out[0] = prm.tile_rows;
+    out[1] = prm.dp_tiles;
+    out[2] = pairs;
+    out[3] = pl.T;
+    int64_t n = 4;
+    for (int64_t q = 0; q < pairs; ++q) {
+        SegWalk sw = seg_walk(pl, q);
+        PairSeg w;
+        while (seg_next(prm, pl, sw, w)) {
+            if (n + 8 > cap) return -1;
+            out[n++] = q;
+            out[n++] = w.t;
+            out[n++] = w.m0;
+            out[n++] = w.c0;
+            out[n++] = w.kbeg;
+            out[n++] = w.nk;
+            out[n++] = w.role;
+            out[n++] = w.role == kSegHead ? head_contrib_end(pl, q, w.t) : -1;
+        }
+    }
+    return (n - 4) / 8;
+}
 
 const char *qlora_last_error(void) { return t_last_error.c_str(); }
 

@@ -30,7 +30,7 @@ EXPORTS = [
     "qlora_nf4_dequantize",
     "qlora_linear_fwd_workspace", "qlora_linear_bwd_workspace", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_last_error", "qlora_check_device_status", "qlora_set_wait_limit", "qlora_version",
-    "qlora_profile_start", "qlora_profile_stop",
+    "qlora_profile_start", "qlora_profile_stop", "qlora_debug_gemm_segments",
 ]
 
 KERNEL_KINDS = ["quantize", "dequant", "lora_pre", "fwd_gemm", "fwd_simt", "dx_gemm", "dx_simt", "grads"]
@@ -89,6 +89,8 @@ def lib():
         L.qlora_profile_start.argtypes = []
         L.qlora_profile_stop.restype = i32
         L.qlora_profile_stop.argtypes = [vp, vp]
+        L.qlora_debug_gemm_segments.restype = i64
+        L.qlora_debug_gemm_segments.argtypes = [i64, i64, i64, i32, i32, vp, i64]
         _lib = L
     return _lib
 
@@ -227,6 +229,24 @@ def qlora_set_wait_limit(spins: int):
 
 def qlora_version() -> str:
     return lib().qlora_version().decode()
+
+
+def qlora_debug_gemm_segments(M: int, Nd: int, nk_main: int, lora_steps: int, pairs_resident: int):
+    """The fused GEMM's work schedule (host computation, no GPU): returns
+    (tile_rows, dp_tiles, pairs, tiles, records), records an int64 array of
+    rows (pair, tile, row0, col0, kbeg, nk, role, contrib_end); see the C
+    header for the fields. Raises QloraError(QLORA_ERR_SHAPE) on bad input."""
+    import numpy as np
+    cap = 4 + 8 * 4096
+    while True:
+        out = np.zeros(cap, np.int64)
+        n = lib().qlora_debug_gemm_segments(int(M), int(Nd), int(nk_main), int(lora_steps), int(pairs_resident),
+                                            out.ctypes.data, cap)
+        if n >= 0:
+            return int(out[0]), int(out[1]), int(out[2]), int(out[3]), out[4:4 + 8 * n].reshape(n, 8).copy()
+        if n != -1:
+            raise QloraError(2, "qlora_debug_gemm_segments: invalid arguments")
+        cap *= 4
 
 
 def qlora_profile_start():

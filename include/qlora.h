@@ -238,6 +238,25 @@ int qlora_profile_stop(double ms_per_kind[QLORA_KERNEL_KINDS], int launches_per_
 /* Library version string. */
 const char *qlora_version(void);
 
+/* Diagnostic, host only (no device access): the work schedule the fused
+ * tensor-core GEMM would run for an output of M rows and Nd columns with
+ * nk_main main 64-deep k-steps and lora_steps LoRA k-steps (forward: Nd = N,
+ * nk_main = K / 64; dX: Nd = K, nk_main = ceil(N / 64); lora_steps =
+ * ceil(r / 64)) on a device holding `pairs_resident` (1..74) CTA pairs at
+ * once. Writes to out[0..3] the tile height in rows (512 or 256), the number
+ * of tiles run data-parallel, the pairs launched and the number of tiles T;
+ * then one record of 8 values per segment, pair by pair in the order each pair
+ * runs them: pair, tile, first output row, first output column, first k-step,
+ * k-steps, role (0 whole tile, 1 head: the pair finishes the tile, 2 tail: the
+ * pair's fp32 partial goes to its slot) and, for a head, one past the last
+ * pair whose tail it adds (-1 otherwise). Returns the number of records, -1
+ * when `cap` (values available in out) is too small, -2 for invalid
+ * arguments.
+ * Tiles are 256 output columns wide; a tile's k-steps are the main steps then
+ * the LoRA steps. */
+int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lora_steps, int pairs_resident,
+                                  int64_t *out, int64_t cap);
+
 #ifdef __cplusplus
 }
 #endif
