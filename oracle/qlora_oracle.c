@@ -319,7 +319,12 @@ void oracle_linear_fwd(const uint16_t *X, int64_t M, const uint16_t *Wdq, int64_
  *   dA[j, k] = s * sum_m V[m,j] X[m,k]                           (columns k listed)
  * No gradient for the frozen W. A NULL list means every index (and its count
  * is then M, N or K); outputs are packed in list order: dX is nr x K, dB is
- * nn x r, dA is r x nk. */
+ * nn x r, dA is r x nk.
+ * Every sum runs over its contraction index in increasing order (n for dX, m
+ * for dB and dA). The loops keep a row of running sums per output row (or a
+ * chunk of outputs) so that W', dY and X are read along their rows; this does
+ * not change the order in which any single sum is formed. */
+#define ORACLE_CHUNK 256
 void oracle_linear_bwd(const uint16_t *dY, const uint16_t *X, int64_t M, const uint16_t *Wdq,
                        int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, int r,
                        float scale, const int64_t *rows, int64_t nr, const int64_t *ncols,
@@ -332,35 +337,66 @@ void oracle_linear_bwd(const uint16_t *dY, const uint16_t *X, int64_t M, const u
     if (!rows) nr = M;
     if (!ncols) nn = N;
     if (!kcols) nk = K;
-#pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < nr; ++i) {
-        int64_t m = rows ? rows[i] : i;
-        for (int64_t k = 0; k < K; ++k) {
-            double base = 0.0;
-            for (int64_t n = 0; n < N; ++n)
-                base += (double)bf16_to_f32(dY[m * N + n]) * (double)bf16_to_f32(Wdq[n * K + k]);
-            double lora = 0.0;
-            for (int j = 0; j < r; ++j) lora += V[m * r + j] * (double)bf16_to_f32(A[(int64_t)j * K + k]);
-            dX[i * K + k] = base + (double)scale * lora;
+    /* dX: for row m, base[k] = sum over n = 0..N-1 of dY[m,n] W'[n,k] */
+#pragma omp parallel
+    {
+        double *base = (double *)malloc((size_t)K * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t i = 0; i < nr; ++i) {
+            int64_t m = rows ? rows[i] : i;
+            for (int64_t k = 0; k < K; ++k) base[k] = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double g = (double)bf16_to_f32(dY[m * N + n]);
+                const uint16_t *w = Wdq + n * K;
+                for (int64_t k = 0; k < K; ++k) base[k] += g * (double)bf16_to_f32(w[k]);
+            }
+            for (int64_t k = 0; k < K; ++k) {
+                double lora = 0.0;
+                for (int j = 0; j < r; ++j) lora += V[m * r + j] * (double)bf16_to_f32(A[(int64_t)j * K + k]);
+                dX[i * K + k] = base[k] + (double)scale * lora;
+            }
         }
+        free(base);
     }
-#pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < nn; ++i) {
-        int64_t n = ncols ? ncols[i] : i;
-        for (int j = 0; j < r; ++j) {
-            double acc = 0.0;
-            for (int64_t m = 0; m < M; ++m) acc += (double)bf16_to_f32(dY[m * N + n]) * U[m * r + j];
-            dB[i * r + j] = (double)scale * acc;
+    /* dB[n, j] = s * sum over m = 0..M-1 of dY[m,n] U[m,j], ORACLE_CHUNK listed n at a time */
+    int64_t nchunks = (nn + ORACLE_CHUNK - 1) / ORACLE_CHUNK;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)ORACLE_CHUNK * (size_t)r * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t c = 0; c < nchunks; ++c) {
+            int64_t i0 = c * ORACLE_CHUNK, i1 = i0 + ORACLE_CHUNK < nn ? i0 + ORACLE_CHUNK : nn;
+            for (int64_t t = 0; t < (i1 - i0) * r; ++t) acc[t] = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                for (int64_t i = i0; i < i1; ++i) {
+                    int64_t n = ncols ? ncols[i] : i;
+                    double g = (double)bf16_to_f32(dY[m * N + n]);
+                    for (int j = 0; j < r; ++j) acc[(i - i0) * r + j] += g * U[m * r + j];
+                }
+            for (int64_t i = i0; i < i1; ++i)
+                for (int j = 0; j < r; ++j) dB[i * r + j] = (double)scale * acc[(i - i0) * r + j];
         }
+        free(acc);
     }
-#pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < nk; ++i) {
-        int64_t k = kcols ? kcols[i] : i;
-        for (int j = 0; j < r; ++j) {
-            double acc = 0.0;
-            for (int64_t m = 0; m < M; ++m) acc += V[m * r + j] * (double)bf16_to_f32(X[m * K + k]);
-            dA[(int64_t)j * nk + i] = (double)scale * acc;
+    /* dA[j, k] = s * sum over m = 0..M-1 of V[m,j] X[m,k], ORACLE_CHUNK listed k at a time */
+    nchunks = (nk + ORACLE_CHUNK - 1) / ORACLE_CHUNK;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)ORACLE_CHUNK * (size_t)r * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t c = 0; c < nchunks; ++c) {
+            int64_t i0 = c * ORACLE_CHUNK, i1 = i0 + ORACLE_CHUNK < nk ? i0 + ORACLE_CHUNK : nk;
+            for (int64_t t = 0; t < (i1 - i0) * r; ++t) acc[t] = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                for (int64_t i = i0; i < i1; ++i) {
+                    int64_t k = kcols ? kcols[i] : i;
+                    double x = (double)bf16_to_f32(X[m * K + k]);
+                    for (int j = 0; j < r; ++j) acc[(i - i0) * r + j] += V[m * r + j] * x;
+                }
+            for (int64_t i = i0; i < i1; ++i)
+                for (int j = 0; j < r; ++j) dA[(int64_t)j * nk + i] = (double)scale * acc[(i - i0) * r + j];
         }
+        free(acc);
     }
     free(U);
     free(V);

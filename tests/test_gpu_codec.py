@@ -80,3 +80,20 @@ def test_codec_full_size(g, oracle):
     qw = oracle.nf4_quantize(W)
     assert_quant_equal(w, qw)
     assert np.array_equal(g.dequantize(w), oracle.nf4_dequantize(qw))
+
+
+def test_dq_half_way_ties(g, oracle):
+    # Blocks whose absmax puts c / s2 exactly half-way between int8 codes
+    # (2.5, 0.5, -0.5 ...): the GPU's int8 step must round half to even as
+    # the oracle does. Block b holds its absmax once and zeros elsewhere.
+    from tests.test_oracle_dq import _tie_absmax
+    a, _ = _tie_absmax()
+    W = np.zeros((a.size, 64), np.uint16)
+    W[:, 0] = synth.f32_to_bf16_bits(a)
+    assert np.array_equal(synth.bf16_bits_to_f32(W[:, 0]), a)  # the absmax values are bf16 numbers
+    W = W.reshape(8, -1)
+    w = g.quantize(W)
+    qw = oracle.nf4_quantize(W)
+    assert_quant_equal(w, qw)
+    assert list(w.absmax_q.cpu().numpy()[:6]) == [127, 2, 0, 2, 4, 0]
+    assert np.array_equal(g.dequantize(w), oracle.nf4_dequantize(qw))

@@ -124,3 +124,34 @@ def test_zero_block_decodes_to_zero(oracle):
     qw = oracle.nf4_quantize(W)
     Wd = oracle.nf4_dequantize(qw)
     assert np.all(synth.bf16_bits_to_f32(Wd[0, :64]) == 0)
+
+
+def _tie_absmax():
+    """Absmax values whose int8 step lands exactly half-way between codes.
+
+    With s2 = 2^-10 and mean = s2 / 2, group 0 holds c / s2 = 127 (which fixes
+    s2 exactly), 2.5, 0.5, 1.5, 3.5 and -0.5; group 1 only balances the sum so
+    that the mean is exactly s2 / 2. Every value is a small dyadic number, so
+    the pairwise sum, the mean, c and c / s2 are all exact, and every absmax
+    is a bf16 number (at most 8 significant bits), so a weight block can carry
+    it.
+    """
+    s2 = 2.0 ** -10
+    c0 = [127.0, 2.5, 0.5, 1.5, 3.5] + [-0.5] * 251      # sum 9.5
+    c1 = [-0.5] * 19 + [0.0] * 237                       # sum -9.5
+    a = (np.array(c0 + c1) + 0.5) * s2
+    return a.astype(np.float32), s2
+
+
+def test_dq_half_way_ties_round_to_even(oracle):
+    # The int8 step rounds half to even (C rint): 2.5 -> 2, 0.5 -> 0,
+    # -0.5 -> 0, 1.5 -> 2, 3.5 -> 4. Rounding half away from zero would give
+    # 3, 1, -1 for the first three, so a round() in place of rint() fails here.
+    a, s2 = _tie_absmax()
+    q, s, mean = oracle.dq_encode(a)
+    assert mean == np.float32(s2 / 2)
+    assert s[0] == np.float32(s2)
+    assert list(q[:6]) == [127, 2, 0, 2, 4, 0]
+    assert np.all(q[6:256] == 0)
+    # decode: a' = q * s2 + mean, exact here
+    assert oracle.dq_decode(2, s2, mean) == np.float32(2.5 * s2)
