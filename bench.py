@@ -1,16 +1,21 @@
 """Benchmark of the NF4 + double-quantized LoRA linear layer on one B300.
 
 One step = forward + backward of all seven NF4-LoRA projections of a
-Llama-3.1-8B-shaped decoder layer (q, k, v, o, gate, up, down; r = 16,
-alpha = 32, M = 2048 tokens), inputs resident in HBM. The line also carries
-the standalone codec measurement (14336 x 4096 quantize once + dequantize
-x100), the roofline of the dominant kernel, an end-to-end figure through the
-C ABI with host buffers, and the CPU oracle timed on a bounded token sample.
+Llama-70B-shaped decoder layer (q, k, v, o, gate, up, down with d_model 8192,
+KV width 1024, FFN 28672; LoRA r = 64, alpha = 16; M = 4096 tokens), inputs
+resident in HBM. The same JSON line carries: the roofline of the step's
+dominant kernel kind; an end-to-end figure through the C ABI with host buffers;
+the Llama-3.1-8B-shaped layer (M = 2048, r = 16) and the single 1024 x 1024
+layer (M = 256, r = 8); the standalone codec (14336 x 4096 quantize once +
+dequantize x100); the token sweep on the gate projection; and the CPU oracle
+timed on bounded samples.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun (N > 1) every rank runs its own M tokens (weak scaling, data
-parallel) and the adapter gradients are all-reduced over NCCL each step.
+Every input follows the seeded numpy recipe of synth.py, the same bytes the
+parity tests give the oracle. Under torchrun (N > 1) every rank runs its own
+M tokens (weak scaling, data parallel) and the adapter gradients are
+all-reduced over NCCL each step.
 """
 from __future__ import annotations
 
@@ -30,9 +35,12 @@ sys.path.insert(0, ROOT)
 
 from bit_quantized_lora_double_b300 import dp, synth  # noqa: E402
 
-WORKLOAD = 1          # Llama-3.1-8B-shaped layer, M = 2048, r = 16
+WORKLOAD = 3          # Llama-70B-shaped projections, M = 4096, r = 64
+LAYER8B = 1           # Llama-3.1-8B-shaped layer, M = 2048, r = 16
+SINGLE = 0            # single 1024 x 1024 layer, M = 256, r = 8
 CODEC_WORKLOAD = 2    # 14336 x 4096 codec
-CPU_SAMPLE_TOKENS = 96
+SWEEP = 4             # gate 4096 -> 14336 token sweep
+CPU_SAMPLE_TOKENS = 24
 METRIC = "QLoRA linear fwd+bwd TFLOP/s and % bf16 peak; NF4 dequant GB/s and % HBM"
 
 
@@ -75,36 +83,51 @@ def step_flops(M, projections, r):
     return sum(4 * M * n * k + 6 * M * r * (n + k) for _, n, k in projections)
 
 
-def fwd_gemm_flops(M, n, k, r):
-    # one forward main-kernel launch: X W'^T plus the LoRA up-projection
-    return 2 * M * n * k + 2 * M * n * r
-
-
-def dx_gemm_flops(M, n, k, r):
-    return 2 * M * n * k + 2 * M * k * r
+# algorithmic flops per kernel kind and projection (the LoRA terms that run
+# inside the fused GEMMs count with them; U, V, dA, dB are the side path)
+KIND_FLOPS = {
+    "fwd_gemm": lambda M, n, k, r: 2 * M * n * k + 2 * M * n * r,
+    "fwd_simt": lambda M, n, k, r: 2 * M * n * k + 2 * M * n * r,
+    "dx_gemm": lambda M, n, k, r: 2 * M * n * k + 2 * M * k * r,
+    "dx_simt": lambda M, n, k, r: 2 * M * n * k + 2 * M * k * r,
+}
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons; `summary` keeps
+    the samples taken between mark_start() and mark_end()."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval_ms=50):
         self.gpu = gpu_index
+        self.interval = interval_ms
         self.proc = None
         self.f = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            # wait for the first sample so the sampler covers the region
+            t_end = time.time() + 5
+            while time.time() < t_end and os.path.getsize(self.f.name) == 0:
+                time.sleep(0.02)
         except Exception:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(2 * self.interval / 1000)
 
     def __exit__(self, *a):
         if self.proc:
@@ -117,113 +140,86 @@ class Clocks:
     def summary(self):
         if not self.f:
             return None
+        import datetime
         self.f.flush()
         rows = []
         with open(self.f.name) as fh:
             for line in fh:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                rows.append((ts, parts[1:]))
         os.unlink(self.f.name)
-        if not rows:
+        inside = [p for ts, p in rows if self.t0 is not None and self.t0 - 0.05 <= ts <= (self.t1 or ts) + 0.05]
+        use = inside if inside else [p for _, p in rows]
+        if not use:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[1]) for r in use if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "interval_ms": self.interval}
 
 
-def cpu_baseline(M_tokens, projections, r, scale):
-    """The CPU oracle, as it stands, on a bounded token sample of the step."""
-    from oracle import oracle
-    tot_t, tot_f = 0.0, 0
-    for p, (name, n, k) in enumerate(projections):
-        X, W, A, B, dY, s = synth.layer_inputs(WORKLOAD, p, M=M_tokens)
-        qw = oracle.nf4_quantize(W)
-        Wdq = oracle.nf4_dequantize(qw)
-        t = time.perf_counter()
-        oracle.linear_fwd(X, Wdq, A, B, s)
-        oracle.linear_bwd(dY, X, Wdq, A, B, s)
-        tot_t += time.perf_counter() - t
-        tot_f += 4 * M_tokens * n * k + 6 * M_tokens * r * (n + k)
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    threads = int(os.environ.get("OMP_NUM_THREADS", cores))
-    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{M_tokens} tokens of each of the 7 projections, forward + backward (fp64 C loops, "
-                      f"OpenMP); {tot_t:.1f} s"}
+def load_layer(qlora, torch, dev, wl_id, pinned=False):
+    """Seeded inputs of every projection of a workload (synth recipe, numpy),
+    copied to the device; weights quantized on the GPU; outputs and one
+    workspace per projection; pinned host copies of X and dY for the
+    end-to-end leg when asked."""
+    wl = synth.WORKLOADS[wl_id]
+    M, r = wl["M"], wl["r"]
+    P = []
+    for p, (name, n, k) in enumerate(wl["projections"]):
+        X, W, A, B, dY, s = synth.layer_inputs(wl_id, p)
+        dv = lambda h: torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
+        w = qlora.alloc_nf4_weight(n, k, dev)
+        Wd = dv(W)
+        del W
+        wsq = qlora.workspace(qlora.qlora_nf4_quantize_workspace(n, k), dev)
+        qlora.qlora_nf4_quantize(Wd, w, wsq)
+        torch.cuda.synchronize()
+        del Wd, wsq
+        d = dict(name=name, n=n, k=k, s=s, w=w, X=dv(X), A=dv(A), B=dv(B), dY=dv(dY),
+                 Y=torch.empty((M, n), dtype=torch.bfloat16, device=dev),
+                 U=torch.empty((M, r), dtype=torch.bfloat16, device=dev),
+                 dX=torch.empty((M, k), dtype=torch.bfloat16, device=dev),
+                 dA=torch.empty((r, k), dtype=torch.float32, device=dev),
+                 dB=torch.empty((n, r), dtype=torch.float32, device=dev))
+        if pinned:
+            d["hX"] = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).pin_memory()
+            d["hdY"] = torch.from_numpy(dY.view(np.int16)).view(torch.bfloat16).pin_memory()
+        d["ws"] = qlora.workspace(max(qlora.qlora_linear_fwd_workspace(M, w, r),
+                                      qlora.qlora_linear_bwd_workspace(M, w, r)), dev)
+        P.append(d)
+    torch.cuda.synchronize()
+    return wl, P
 
 
-def run_reference(args, rank, world):
-    """Reference arm: the CPU oracle timed on the host cores, per step a bounded
-    sample (one token of one projection, round robin)."""
-    if rank != 0:
-        return
-    from oracle import oracle
-    w = synth.WORKLOADS[WORKLOAD]
-    projs, r = w["projections"], w["r"]
-    prep = []
-    for p in range(len(projs)):
-        X, W, A, B, dY, s = synth.layer_inputs(WORKLOAD, p, M=1)
-        qw = oracle.nf4_quantize(W)
-        prep.append((X, oracle.nf4_dequantize(qw), A, B, dY, s, projs[p]))
-
-    def one(i):
-        X, Wdq, A, B, dY, s, (_, n, k) = prep[i % len(prep)]
-        t = time.perf_counter()
-        oracle.linear_fwd(X, Wdq, A, B, s)
-        oracle.linear_bwd(dY, X, Wdq, A, B, s)
-        return time.perf_counter() - t, 4 * n * k + 6 * r * (n + k)
-
-    for i in range(args.warmup):
-        one(i)
-    tt, ff = 0.0, 0
-    for i in range(args.steps):
-        t, f = one(args.warmup + i)
-        tt += t
-        ff += f
-    v = ff / tt / 1e12
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w["name"], "M": w["M"], "r": r, "sample": "1 token of one projection per step"},
-        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "1 token of one projection (round robin over q,k,v,o,gate,up,down) per step"},
-        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }), flush=True)
+def make_step(qlora, P, M, r, world):
+    def step():
+        for d in P:
+            qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"])
+        for d in reversed(P):
+            qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
+                                   d["dB"], d["ws"])
+            if world > 1:
+                dp.allreduce_adapter_grads([d["dA"], d["dB"]])
+    return step
 
 
-def device_projection(qlora, torch, dev, gen, n, k, M, r, w_std, b_std, copies=1):
-    """Seeded device-side inputs of one projection (torch Philox generator,
-    the same distributions as the parity inputs): the NF4 weight (and
-    `copies` - 1 extra copies of it), X, dY ~ N(0, 1), A ~ N(0, 1/K),
-    B ~ N(0, b_std); output buffers and one workspace."""
-    bf = torch.bfloat16
-
-    def normal(shape, std):
-        return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * std).to(bf)
-
-    W = normal((n, k), w_std)
-    w = qlora.alloc_nf4_weight(n, k, dev)
-    qlora.qlora_nf4_quantize(W, w, qlora.workspace(qlora.qlora_nf4_quantize_workspace(n, k), dev))
-    del W
-    ws_ = [w]
-    for _ in range(copies - 1):
-        x = qlora.alloc_nf4_weight(n, k, dev)
-        x.codes.copy_(w.codes); x.absmax_q.copy_(w.absmax_q)
-        x.absmax_scale.copy_(w.absmax_scale); x.absmax_mean.copy_(w.absmax_mean)
-        ws_.append(x)
-    d = dict(n=n, k=k, w=ws_, X=normal((M, k), 1.0), dY=normal((M, n), 1.0), A=normal((r, k), 1.0 / k),
-             B=normal((n, r), b_std), Y=torch.empty((M, n), dtype=bf, device=dev),
-             U=torch.empty((M, r), dtype=bf, device=dev), dX=torch.empty((M, k), dtype=bf, device=dev),
-             dA=torch.empty((r, k), dtype=torch.float32, device=dev),
-             dB=torch.empty((n, r), dtype=torch.float32, device=dev))
-    d["ws"] = qlora.workspace(max(qlora.qlora_linear_fwd_workspace(M, w, r),
-                                  qlora.qlora_linear_bwd_workspace(M, w, r)), dev)
-    return d
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    return g
 
 
 def graph_time(torch, fn, steps, warmup):
@@ -231,11 +227,7 @@ def graph_time(torch, fn, steps, warmup):
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        fn()
-    g.replay()
-    torch.cuda.synchronize()
+    g = capture(torch, fn)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(steps):
@@ -245,248 +237,56 @@ def graph_time(torch, fn, steps, warmup):
     return a.elapsed_time(b) / steps
 
 
-def bench_llama70b(qlora, torch, dev, pk, steps):
-    """The Llama-70B-shaped projections at M = 4096, r = 64: forward +
-    backward of all seven, TFLOP/s."""
-    wl = synth.WORKLOADS[3]
-    M, r, scale = wl["M"], wl["r"], wl["scale"]
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(synth.seed_for(3, "X"))
-    P = [device_projection(qlora, torch, dev, gen, n, k, M, r, wl["w_std"], wl["b_std"])
-         for _, n, k in wl["projections"]]
-
-    def step():
-        for d in P:
-            qlora.qlora_linear_fwd(d["X"], M, d["w"][0], d["A"], d["B"], r, scale, d["Y"], d["U"], d["ws"])
-        for d in reversed(P):
-            qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"][0], d["A"], d["B"], r, scale, d["dX"],
-                                   d["dA"], d["dB"], d["ws"])
-
-    ms = graph_time(torch, step, steps, 2)
-    flops = step_flops(M, wl["projections"], r)
-    out = {"workload": wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=64 alpha=16", "M": M, "r": r,
-           "ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "pct_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16"],
-           "pct_bf16_peak_sustained": flops / (ms * 1e-3) / 1e12 / pk["bf16_sus"]}
-    del P
-    torch.cuda.empty_cache()
-    return out
-
-
-def bench_sweep(qlora, torch, dev, pk):
-    """Token-count sweep on the gate projection 4096 -> 14336 (r = 16): the
-    forward at every M, the backward for M >= 128. For M <= 16 the forward
-    reads six rotating copies of the packed weight (more than L2 holds) and
-    is reported as GB/s against the HBM roofline."""
-    wl = synth.WORKLOADS[4]
-    _, n, k = wl["projections"][0]
-    r, scale = wl["r"], wl["scale"]
-    rows = []
-    for M in wl["M_sweep"]:
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(synth.seed_for(4, "X") + M)
-        copies = 6 if M <= 16 else 1
-        d = device_projection(qlora, torch, dev, gen, n, k, M, r, wl["w_std"], wl["b_std"], copies)
-        it = [0]
-
-        def fwd():
-            w = d["w"][it[0] % copies]
-            it[0] += 1
-            qlora.qlora_linear_fwd(d["X"], M, w, d["A"], d["B"], r, scale, d["Y"], d["U"], d["ws"])
-
-        reps = max(3, min(200, int(2e11 / max(1, M * n * k * 2))))
-        if copies > 1:
-            # eager launches (the rotation over weight copies is host-side)
-            for _ in range(5):
-                fwd()
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            for _ in range(reps):
-                fwd()
-            b.record()
-            torch.cuda.synchronize()
-            f_ms = a.elapsed_time(b) / reps
-        else:
-            f_ms = graph_time(torch, fwd, reps, 3)
-        f_fl = 2 * M * n * k + 2 * M * r * (n + k)
-        row = {"M": M, "fwd_ms": f_ms, "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12}
-        if M <= 16:
-            wbytes = n * k // 2 + n * k // 64 + 4 * ((n * k // 64 + 255) // 256) + 4
-            byts = wbytes + 2 * (M * k + M * n + r * k + n * r)
-            gbs = byts / (f_ms * 1e-3) / 1e9
-            row.update({"fwd_gbs": gbs, "fwd_pct_hbm": gbs / pk["hbm"], "fwd_bytes": byts,
-                        "l2": "6 rotating weight copies (> L2)"})
-        if M >= 128:
-            def bwd():
-                qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"][0], d["A"], d["B"], r, scale, d["dX"],
-                                       d["dA"], d["dB"], d["ws"])
-            b_ms = graph_time(torch, bwd, reps, 3)
-            b_fl = 2 * M * n * k + 4 * M * r * (n + k)
-            row.update({"bwd_ms": b_ms, "bwd_tflops": b_fl / (b_ms * 1e-3) / 1e12,
-                        "fwd_bwd_tflops": (4 * M * n * k + 6 * M * r * (n + k)) / ((f_ms + b_ms) * 1e-3) / 1e12})
-        rows.append(row)
-        del d
-        torch.cuda.empty_cache()
-    return {"workload": wl["name"] + ": gate 4096->14336 NF4+DQ, LoRA r=16 alpha=32", "rows": rows}
-
-
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--prof-steps", type=int, default=20)
-    ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the 70B-shaped layer and the M sweep")
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-
-    if args.impl == "reference":
-        return run_reference(args, rank, world)
-
-    import torch
-    import torch.distributed as dist
-    from bit_quantized_lora_double_b300 import qlora
-
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    pk = peaks()
-
-    wl = synth.WORKLOADS[WORKLOAD]
-    projs, M, r = wl["projections"], wl["M"], wl["r"]
-
-    def dev_bf16(h):
-        return torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    # ---- setup: quantize the seven weights on the GPU, inputs resident -----
-    P = []
-    for p, (name, n, k) in enumerate(projs):
-        X, W, A, B, dY, s = synth.layer_inputs(WORKLOAD, p)
-        w = qlora.alloc_nf4_weight(n, k, dev)
-        wsq = qlora.workspace(qlora.qlora_nf4_quantize_workspace(n, k), dev)
-        qlora.qlora_nf4_quantize(dev_bf16(W), w, wsq)
-        del wsq
-        d = dict(name=name, n=n, k=k, s=s, w=w, X=dev_bf16(X), A=dev_bf16(A), B=dev_bf16(B), dY=dev_bf16(dY),
-                 hX=torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).pin_memory(),
-                 hdY=torch.from_numpy(dY.view(np.int16)).view(torch.bfloat16).pin_memory(),
-                 Y=torch.empty((M, n), dtype=torch.bfloat16, device=dev),
-                 U=torch.empty((M, r), dtype=torch.bfloat16, device=dev),
-                 dX=torch.empty((M, k), dtype=torch.bfloat16, device=dev),
-                 dA=torch.empty((r, k), dtype=torch.float32, device=dev),
-                 dB=torch.empty((n, r), dtype=torch.float32, device=dev))
-        d["ws"] = qlora.workspace(max(qlora.qlora_linear_fwd_workspace(M, w, r),
-                                      qlora.qlora_linear_bwd_workspace(M, w, r)), dev)
-        P.append(d)
+def profile_kinds(qlora, torch, step, n):
+    """Per kernel kind: summed device ms per step and launches per step, from
+    CUDA events the library records around each launch on its launch stream
+    during n eager steps."""
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-
-    def step():
-        for d in P:
-            qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"])
-        for d in reversed(P):
-            qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
-                                   d["dB"], d["ws"])
-            if world > 1:
-                dp.allreduce_adapter_grads([d["dA"], d["dB"]])
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    for _ in range(args.warmup):
-        step()
-    qlora.qlora_check_device_status(stream)
-    barrier()
-
-    # The timed region replays one CUDA graph of the step (captured after the
-    # warm-up; the library's calls allocate and synchronize nothing, so they
-    # capture as they are), or launches the step eagerly with --no-graph.
-    graph = None
-    if not args.no_graph and world == 1:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        graph.replay()
-        barrier()
-        qlora.qlora_check_device_status(stream)
-    run_step = graph.replay if graph is not None else step
-
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
-        barrier()
-        ev0.record()
-        for _ in range(args.steps):
-            run_step()
-        ev1.record()
-        barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    qlora.qlora_check_device_status(stream)
-    clocks = clk.summary()
-
-    flops = step_flops(M, projs, r)
-    ms_step = ms / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
-
-    # Per-kernel device times: the same step launched eagerly with the
-    # library's profiling hooks (a CUDA event pair around every launch, on the
-    # launch stream), right after the timed region.
-    prof_steps = max(1, min(args.steps, args.prof_steps))
     qlora.qlora_profile_start()
-    barrier()
-    for _ in range(prof_steps):
+    for _ in range(n):
         step()
-    barrier()
-    prof_ms, prof_n, _ = qlora.qlora_profile_stop()
-    launches = sum(prof_n.values()) // prof_steps * args.steps
+    torch.cuda.synchronize()
+    ms, cnt, _ = qlora.qlora_profile_stop()
+    return ({k: v / n for k, v in ms.items() if cnt[k]}, {k: v // n for k, v in cnt.items() if v})
 
-    # dominant kernel of the step and its roofline: per kind, the summed
-    # device time of its launches in the timed region against the algorithmic
-    # flops of those launches (a kind's split-reduction launches count with it)
-    kinds = {k: v for k, v in prof_ms.items() if prof_n[k] > 0}
-    dom = max(kinds, key=kinds.get)
-    gemm_flops = {"fwd_gemm": sum(fwd_gemm_flops(M, n, k, r) for _, n, k in projs),
-                  "fwd_simt": sum(fwd_gemm_flops(M, n, k, r) for _, n, k in projs),
-                  "dx_gemm": sum(dx_gemm_flops(M, n, k, r) for _, n, k in projs),
-                  "dx_simt": sum(dx_gemm_flops(M, n, k, r) for _, n, k in projs)}
-    roof = None
-    if dom in gemm_flops:
-        ms_kind = prof_ms[dom] / prof_steps
-        ach = gemm_flops[dom] / (ms_kind * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_sus"], "traffic": measured_traffic(dom),
-                "traffic_note": "DRAM read+write bytes per launch (average over the step's launches) from "
-                                "profiles/roofline_traffic.json",
-                "peak_note": f"bf16 dense sustained ({pk['src']}); a kernel timed inside a long step",
-                "flops_per_launch": gemm_flops[dom] / len(projs),
-                "launches_per_step": prof_n[dom] / prof_steps, "ms_per_step": ms_kind,
-                "timing": f"CUDA events around each launch, {prof_steps} eager profiled steps after the timed region"}
 
-    # ---- end to end through the C ABI with host buffers ----------------------
+def roofline_of(kind_ms, kind_n, graph_ms, M, projections, r, pk, clocks):
+    """Roofline of the dominant kernel kind. Its per-launch device times come
+    from the eager profiled steps; they are scaled by (graph step time / sum of
+    the kinds' eager times) so that the kinds add up to the timed step, which
+    charges any idle time of the graph step to the kernels (a lower bound on
+    the rate)."""
+    dom = max(kind_ms, key=kind_ms.get)
+    if dom not in KIND_FLOPS:
+        return None
+    scale = graph_ms / sum(kind_ms.values())
+    ms_kind = kind_ms[dom] * scale
+    fl = sum(KIND_FLOPS[dom](M, n, k, r) for _, n, k in projections)
+    ach = fl / (ms_kind * 1e-3) / 1e12
+    capped = clocks is not None and "sw_power_cap" in clocks.get("reasons", [])
+    return {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+            "frac": ach / pk["bf16"], "frac_of_sustained_peak": ach / pk["bf16_sus"],
+            "traffic": measured_traffic(dom),
+            "traffic_note": "DRAM read+write bytes per launch (mean over the step's launches of this kind), "
+                            "from profiles/roofline_traffic.json; null when the kernels changed since",
+            "peak_note": f"bf16 dense burst ({pk['src']}); the sustained figure is {pk['bf16_sus']} TFLOP/s"
+                         + ("; sw_power_cap was active during the timed region" if capped else ""),
+            "flops_per_step": fl, "launches_per_step": kind_n[dom], "ms_per_step": ms_kind,
+            "ms_per_step_eager": kind_ms[dom], "scale_to_graph_step": scale,
+            "timing": "CUDA events around each launch on its stream during eager profiled steps, scaled so "
+                      "that the kinds sum to the graph-timed ms_per_step"}
+
+
+def e2e_leg(qlora, torch, dev, P, M, r, world, steps, flops):
+    """Same step through the C ABI with pinned host buffers: per step the H2D
+    copy of every X and dY and the D2H copy of Y, dX, dA and dB, on two copy
+    streams overlapping the compute stream."""
     hY = {d["name"]: torch.empty(d["Y"].shape, dtype=torch.bfloat16, pin_memory=True) for d in P}
     hdX = {d["name"]: torch.empty(d["dX"].shape, dtype=torch.bfloat16, pin_memory=True) for d in P}
     hdA = {d["name"]: torch.empty(d["dA"].shape, dtype=torch.float32, pin_memory=True) for d in P}
     hdB = {d["name"]: torch.empty(d["dB"].shape, dtype=torch.float32, pin_memory=True) for d in P}
     h2d = sum(d["hX"].numel() * 2 + d["hdY"].numel() * 2 for d in P)
     d2h = sum(d["Y"].numel() * 2 + d["dX"].numel() * 2 + d["dA"].numel() * 4 + d["dB"].numel() * 4 for d in P)
-
-    # Host copies run on two copy streams beside the compute stream: the inputs
-    # of projection p+1 travel while projection p computes, and each result
-    # goes back as soon as its kernel is done.
     s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     comp = torch.cuda.current_stream()
 
@@ -496,7 +296,6 @@ def main():
                 d["X"].copy_(d["hX"], non_blocking=True)
                 d["ev_x"] = torch.cuda.Event()
                 d["ev_x"].record(s_h2d)
-            with torch.cuda.stream(s_h2d):
                 d["dY"].copy_(d["hdY"], non_blocking=True)
                 d["ev_dy"] = torch.cuda.Event()
                 d["ev_dy"].record(s_h2d)
@@ -521,79 +320,398 @@ def main():
                 hdX[d["name"]].copy_(d["dX"], non_blocking=True)
                 hdA[d["name"]].copy_(d["dA"], non_blocking=True)
                 hdB[d["name"]].copy_(d["dB"], non_blocking=True)
-        # the step ends when every result is on the host
         ev = torch.cuda.Event()
         ev.record(s_d2h)
         comp.wait_event(ev)
 
     e2e_step()
-    barrier()
-    ev0.record(comp)
-    for _ in range(args.e2e_steps):
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    for _ in range(steps):
         e2e_step()
-    ev1.record(comp)
-    barrier()
-    e2e_ms = ev0.elapsed_time(ev1) / args.e2e_steps
-    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "note": "pinned host buffers; H2D of all inputs and D2H of Y, dX, dA, dB on two copy streams "
-                   "overlapping the compute stream"}
+    b.record(comp)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "note": "pinned host buffers; H2D of every X and dY and D2H of Y, dX, dA, dB on two copy streams "
+                    "overlapping the compute stream"}
 
-    # ---- codec: 14336 x 4096 quantize once + dequantize x100 -----------------
+
+def bench_layer(qlora, torch, dev, pk, wl_id, steps):
+    """A whole layer step (graph-timed) of another workload, with its own
+    per-kind times."""
+    wl, P = load_layer(qlora, torch, dev, wl_id)
+    M, r = wl["M"], wl["r"]
+    step = make_step(qlora, P, M, r, 1)
+    ms = graph_time(torch, step, steps, 3)
+    kms, kn = profile_kinds(qlora, torch, step, 3)
+    flops = step_flops(M, wl["projections"], r)
+    v = flops / (ms * 1e-3) / 1e12
+    out = {"workload": wl["name"], "M": M, "r": r, "alpha": wl["alpha"], "ms_per_step": ms, "value": v,
+           "unit": "TFLOP/s", "pct_bf16_peak": v / pk["bf16"], "pct_bf16_peak_sustained": v / pk["bf16_sus"],
+           "flops_per_step": flops, "kernels_ms_per_step_eager": kms, "kernels_launches_per_step": kn,
+           "roofline": roofline_of(kms, kn, ms, M, wl["projections"], r, pk, None)}
+    del P
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_codec(qlora, torch, dev, pk):
+    """14336 x 4096 quantize once + dequantize x100 (rotating over 6 copies of
+    the packed weight, more than L2 holds, so reads come from HBM)."""
     _, cn, ck = synth.WORKLOADS[CODEC_WORKLOAD]["projections"][0]
-    Wc = dev_bf16(synth.gaussian_bf16((cn, ck), 0.02, synth.seed_for(CODEC_WORKLOAD, "W")))
+    Wc = torch.from_numpy(synth.gaussian_bf16((cn, ck), 0.02, synth.seed_for(CODEC_WORKLOAD, "W")).view(np.int16))
+    Wc = Wc.view(torch.bfloat16).to(dev)
     wc = qlora.alloc_nf4_weight(cn, ck, dev)
     wsc = qlora.workspace(qlora.qlora_nf4_quantize_workspace(cn, ck), dev)
     outc = torch.empty((cn, ck), dtype=torch.bfloat16, device=dev)
     for _ in range(3):
         qlora.qlora_nf4_quantize(Wc, wc, wsc)
         qlora.qlora_nf4_dequantize(wc, outc)
-    barrier()
-    ev0.record(stream)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
     qlora.qlora_nf4_quantize(Wc, wc, wsc)
-    ev1.record(stream)
-    barrier()
-    q_ms = ev0.elapsed_time(ev1)
-    # rotate over copies of the packed weight larger than L2 in total, so the
-    # dequantize reads come from HBM
+    b.record()
+    torch.cuda.synchronize()
+    q_ms = a.elapsed_time(b)
     ncopy = 6
     wcs = [wc] + [qlora.alloc_nf4_weight(cn, ck, dev) for _ in range(ncopy - 1)]
     for x in wcs[1:]:
         x.codes.copy_(wc.codes); x.absmax_q.copy_(wc.absmax_q)
         x.absmax_scale.copy_(wc.absmax_scale); x.absmax_mean.copy_(wc.absmax_mean)
-    outs = [outc] + [torch.empty_like(outc) for _ in range(1)]
+    outs = [outc, torch.empty_like(outc)]
     qlora.qlora_profile_start()
-    barrier()
-    ev0.record(stream)
+    torch.cuda.synchronize()
+    a.record()
     for i in range(100):
         qlora.qlora_nf4_dequantize(wcs[i % ncopy], outs[i % 2])
-    ev1.record(stream)
-    barrier()
+    b.record()
+    torch.cuda.synchronize()
     dq_prof_ms, dq_prof_n, _ = qlora.qlora_profile_stop()
-    dq_ms = ev0.elapsed_time(ev1) / 100
+    dq_ms = a.elapsed_time(b) / 100
     dq_kernel_ms = dq_prof_ms["dequant"] / max(1, dq_prof_n["dequant"])
     nel = cn * ck
     dq_bytes = nel // 2 + nel // 64 + 4 * ((nel // 64 + 255) // 256) + 4 + 2 * nel
     q_bytes = 2 * nel + nel // 2 + nel // 64 + 4 * ((nel // 64 + 255) // 256) + 4
     dq_gbs = dq_bytes / (dq_kernel_ms * 1e-3) / 1e9
-    codec = {"workload": "nf4 codec 14336x4096 bf16 N(0,0.02)",
-             "dequant": {"value": dq_gbs, "unit": "GB/s", "pct_hbm": dq_gbs / pk["hbm"],
-                         "bytes_per_pass": dq_bytes, "ms_per_pass": dq_kernel_ms, "ms_per_call": dq_ms,
-                         "l2": f"{ncopy} rotating copies of the packed weight (> L2)",
-                         "roofline": {"bound": "hbm", "achieved": dq_gbs, "peak": pk["hbm"], "unit": "GB/s",
-                                      "frac": dq_gbs / pk["hbm"], "traffic": measured_traffic("dequant"),
-                                      "peak_note": f"HBM copy, {pk['src']}"}},
-             "quantize": {"value": q_bytes / (q_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": q_ms,
-                          "bytes": q_bytes}}
+    return {"workload": "nf4 codec 14336x4096 bf16 N(0,0.02)",
+            "dequant": {"value": dq_gbs, "unit": "GB/s", "pct_hbm": dq_gbs / pk["hbm"],
+                        "bytes_per_pass": dq_bytes, "ms_per_pass": dq_kernel_ms, "ms_per_call": dq_ms,
+                        "l2": f"{ncopy} rotating copies of the packed weight (> L2)",
+                        "roofline": {"bound": "hbm", "achieved": dq_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                                     "frac": dq_gbs / pk["hbm"], "traffic": measured_traffic("dequant"),
+                                     "peak_note": f"HBM copy, {pk['src']}"}},
+            "quantize": {"value": q_bytes / (q_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": q_ms, "bytes": q_bytes,
+                         "pct_hbm": q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm"]}}
+
+
+def bench_sweep(qlora, torch, dev, pk):
+    """Token-count sweep on the gate projection 4096 -> 14336 (r = 16): the
+    forward at every M, the backward for M >= 128. For M <= 16 the forward
+    reads six rotating copies of the packed weight (more than L2 holds) and
+    is reported as GB/s against the HBM roofline."""
+    wl = synth.WORKLOADS[SWEEP]
+    _, n, k = wl["projections"][0]
+    r, scale = wl["r"], wl["scale"]
+    dv = lambda h: torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
+    _, W, A, B, _, _ = synth.layer_inputs(SWEEP, 0, M=1)
+    w0 = qlora.alloc_nf4_weight(n, k, dev)
+    qlora.qlora_nf4_quantize(dv(W), w0, qlora.workspace(qlora.qlora_nf4_quantize_workspace(n, k), dev))
+    Ad, Bd = dv(A), dv(B)
+    del W
+    rows = []
+    for M in wl["M_sweep"]:
+        # the same draws as synth.layer_inputs(SWEEP, 0, M) for X and dY
+        X = synth.gaussian_bf16((M, k), 1.0, synth.seed_for(SWEEP, "X"))
+        dY = synth.gaussian_bf16((M, n), 1.0, synth.seed_for(SWEEP, "dY")) if M >= 128 else None
+        copies = 6 if M <= 16 else 1
+        ws_ = [w0]
+        for _ in range(copies - 1):
+            x = qlora.alloc_nf4_weight(n, k, dev)
+            x.codes.copy_(w0.codes); x.absmax_q.copy_(w0.absmax_q)
+            x.absmax_scale.copy_(w0.absmax_scale); x.absmax_mean.copy_(w0.absmax_mean)
+            ws_.append(x)
+        Xd = dv(X)
+        Y = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        U = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+        wsb = qlora.workspace(max(qlora.qlora_linear_fwd_workspace(M, w0, r),
+                                  qlora.qlora_linear_bwd_workspace(M, w0, r)), dev)
+        it = [0]
+
+        def fwd():
+            w = ws_[it[0] % copies]
+            it[0] += 1
+            qlora.qlora_linear_fwd(Xd, M, w, Ad, Bd, r, scale, Y, U, wsb)
+
+        reps = max(3, min(200, int(2e11 / max(1, M * n * k * 2))))
+        if copies > 1:
+            # eager launches (the rotation over weight copies is host-side)
+            for _ in range(5):
+                fwd()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            qlora.qlora_profile_start()
+            a.record()
+            for _ in range(reps):
+                fwd()
+            b.record()
+            torch.cuda.synchronize()
+            pms, pn, _ = qlora.qlora_profile_stop()
+            f_ms = a.elapsed_time(b) / reps
+        else:
+            f_ms = graph_time(torch, fwd, reps, 3)
+        f_fl = 2 * M * n * k + 2 * M * r * (n + k)
+        row = {"M": M, "fwd_ms": f_ms, "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12}
+        if M <= 16:
+            wbytes = n * k // 2 + n * k // 64 + 4 * ((n * k // 64 + 255) // 256) + 4
+            byts = wbytes + 2 * (M * k + M * n + r * k + n * r)
+            gbs = byts / (f_ms * 1e-3) / 1e9
+            row.update({"fwd_gbs": gbs, "fwd_pct_hbm": gbs / pk["hbm"], "fwd_bytes": byts,
+                        "kernels_ms_per_call": {kk: v / reps for kk, v in pms.items() if pn[kk]},
+                        "l2": "6 rotating weight copies (> L2)"})
+        if M >= 128:
+            dYd = dv(dY)
+            dX = torch.empty((M, k), dtype=torch.bfloat16, device=dev)
+            dA = torch.empty((r, k), dtype=torch.float32, device=dev)
+            dB = torch.empty((n, r), dtype=torch.float32, device=dev)
+
+            def bwd():
+                qlora.qlora_linear_bwd(dYd, Xd, U, M, w0, Ad, Bd, r, scale, dX, dA, dB, wsb)
+            b_ms = graph_time(torch, bwd, reps, 3)
+            b_fl = 2 * M * n * k + 4 * M * r * (n + k)
+            row.update({"bwd_ms": b_ms, "bwd_tflops": b_fl / (b_ms * 1e-3) / 1e12,
+                        "fwd_bwd_tflops": (4 * M * n * k + 6 * M * r * (n + k)) / ((f_ms + b_ms) * 1e-3) / 1e12})
+            del dYd, dX
+        rows.append(row)
+        del Xd, ws_[1:], wsb
+        torch.cuda.empty_cache()
+    return {"workload": wl["name"] + ": gate 4096->14336 NF4+DQ, LoRA r=16 alpha=32", "rows": rows}
+
+
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_baseline():
+    """The CPU oracle, as it stands, on bounded samples: the headline layer on
+    CPU_SAMPLE_TOKENS tokens of every projection (all host cores, and one
+    projection token on one thread), the codec, and the gate sweep at
+    M <= 128. Rates need no extrapolation; the full-step time at M = 4096 is
+    extrapolated linearly in the tokens and labelled so."""
+    from oracle import oracle
+    cores = host_cores()
+    oracle.set_threads(cores)
+    wl = synth.WORKLOADS[WORKLOAD]
+    projs, r, M_full = wl["projections"], wl["r"], wl["M"]
+    T = CPU_SAMPLE_TOKENS
+    tot_t, tot_f = 0.0, 0
+    one_thread = None
+    for p, (name, n, k) in enumerate(projs):
+        X, W, A, B, dY, s = synth.layer_inputs(WORKLOAD, p, M=T)
+        Wdq = oracle.nf4_dequantize(oracle.nf4_quantize(W))
+        del W
+        t = time.perf_counter()
+        oracle.linear_fwd(X, Wdq, A, B, s)
+        oracle.linear_bwd(dY, X, Wdq, A, B, s)
+        tot_t += time.perf_counter() - t
+        tot_f += 4 * T * n * k + 6 * T * r * (n + k)
+        if name == "gate":
+            oracle.set_threads(1)
+            t = time.perf_counter()
+            oracle.linear_fwd(X[:1], Wdq, A, B, s)
+            oracle.linear_bwd(dY[:1], X[:1], Wdq, A, B, s)
+            t1 = time.perf_counter() - t
+            oracle.set_threads(cores)
+            one_thread = {"value": (4 * n * k + 6 * r * (n + k)) / t1 / 1e12, "unit": "TFLOP/s", "threads": 1,
+                          "sample": "1 token of the 28672 x 8192 gate projection, forward + backward",
+                          "seconds": t1}
+    rate = tot_f / tot_t / 1e12
+    full_flops = step_flops(M_full, projs, r)
+    # codec: 14336 x 4096 quantize + dequantize
+    _, cn, ck = synth.WORKLOADS[CODEC_WORKLOAD]["projections"][0]
+    Wc = synth.gaussian_bf16((cn, ck), 0.02, synth.seed_for(CODEC_WORKLOAD, "W"))
+    t = time.perf_counter()
+    qw = oracle.nf4_quantize(Wc)
+    tq = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.nf4_dequantize(qw)
+    tdq = time.perf_counter() - t
+    nel = cn * ck
+    dq_bytes = nel // 2 + nel // 64 + 4 * ((nel // 64 + 255) // 256) + 4 + 2 * nel
+    q_bytes = 2 * nel + nel // 2 + nel // 64 + 4 * ((nel // 64 + 255) // 256) + 4
+    del Wc, qw
+    # gate sweep at M <= 128 (the full problem at those token counts)
+    sw = synth.WORKLOADS[SWEEP]
+    _, n, k = sw["projections"][0]
+    rs = sw["r"]
+    X, W, A, B, dY, s = synth.layer_inputs(SWEEP, 0, M=128)
+    Wdq = oracle.nf4_dequantize(oracle.nf4_quantize(W))
+    sweep = []
+    for M in (1, 16, 128):
+        t = time.perf_counter()
+        oracle.linear_fwd(X[:M], Wdq, A, B, s)
+        tf = time.perf_counter() - t
+        row = {"M": M, "fwd_tflops": (2 * M * n * k + 2 * M * rs * (n + k)) / tf / 1e12, "fwd_s": tf}
+        if M == 128:
+            t = time.perf_counter()
+            oracle.linear_bwd(dY, X, Wdq, A, B, s)
+            tb = time.perf_counter() - t
+            row.update({"bwd_tflops": (2 * M * n * k + 4 * M * rs * (n + k)) / tb / 1e12, "bwd_s": tb})
+        sweep.append(row)
+    return {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{T} tokens of each of the 7 Llama-70B-shaped projections (r = 64), forward + backward "
+                      f"(fp64 C loops, OpenMP on {cores} threads); {tot_t:.1f} s",
+            "ms_per_step_extrapolated": 1e3 * full_flops / (rate * 1e12),
+            "extrapolation": f"time of the full M = {M_full} step extrapolated linearly in the tokens "
+                             f"from the {T}-token sample",
+            "one_thread": one_thread,
+            "codec": {"quantize_gbs": q_bytes / tq / 1e9, "dequant_gbs": dq_bytes / tdq / 1e9,
+                      "quantize_s": tq, "dequant_s": tdq, "sample": "the full 14336 x 4096 codec workload"},
+            "gate_sweep_M_le_128": sweep}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle timed on the host cores on this arm's
+    workload (the Llama-70B-shaped layer), each step a bounded sample: one
+    token of one projection, forward + backward, round robin over the seven."""
+    if rank != 0:
+        return
+    from oracle import oracle
+    cores = host_cores()
+    oracle.set_threads(cores)
+    w = synth.WORKLOADS[WORKLOAD]
+    projs, r = w["projections"], w["r"]
+    prep = []
+    for p in range(len(projs)):
+        X, W, A, B, dY, s = synth.layer_inputs(WORKLOAD, p, M=1)
+        prep.append((X, oracle.nf4_dequantize(oracle.nf4_quantize(W)), A, B, dY, s, projs[p]))
+        del W
+
+    def one(i):
+        X, Wdq, A, B, dY, s, (_, n, k) = prep[i % len(prep)]
+        t = time.perf_counter()
+        oracle.linear_fwd(X, Wdq, A, B, s)
+        oracle.linear_bwd(dY, X, Wdq, A, B, s)
+        return time.perf_counter() - t, 4 * n * k + 6 * r * (n + k)
+
+    for i in range(args.warmup):
+        one(i)
+    tt, ff = 0.0, 0
+    for i in range(args.steps):
+        t, f = one(args.warmup + i)
+        tt += t
+        ff += f
+    v = ff / tt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["name"], "M": w["M"], "r": r,
+                   "sample": "1 token of one projection per step (round robin over q,k,v,o,gate,up,down)"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "1 token of one projection (round robin over q,k,v,o,gate,up,down) per step"},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--prof-steps", type=int, default=3)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other layers, the codec and the M sweep")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    from bit_quantized_lora_double_b300 import qlora
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    props = torch.cuda.get_device_properties(dev)
+
+    wl, P = load_layer(qlora, torch, dev, WORKLOAD, pinned=True)
+    projs, M, r = wl["projections"], wl["M"], wl["r"]
+    stream = torch.cuda.current_stream()
+    step = make_step(qlora, P, M, r, world)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    qlora.qlora_check_device_status(stream)
+    barrier()
+
+    # The timed region replays one CUDA graph of the step (the library's calls
+    # allocate and synchronize nothing, so they capture as they are), or
+    # launches the step eagerly with --no-graph.
+    graph = capture(torch, step) if not args.no_graph and world == 1 else None
+    if graph is not None:
+        qlora.qlora_check_device_status(stream)
+    run_step = graph.replay if graph is not None else step
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        clk.mark_start()
+        ev0.record()
+        for _ in range(args.steps):
+            run_step()
+        ev1.record()
+        barrier()
+        clk.mark_end()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    qlora.qlora_check_device_status(stream)
+    clocks = clk.summary()
+
+    flops = step_flops(M, projs, r)
+    ms_step = ms / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    kind_ms, kind_n = profile_kinds(qlora, torch, step, max(1, args.prof_steps))
+    launches = sum(kind_n.values()) * args.steps
+    roof = roofline_of(kind_ms, kind_n, ms_step, M, projs, r, pk, clocks)
+    e2e = e2e_leg(qlora, torch, dev, P, M, r, world, args.e2e_steps, flops)
+    timed_region = "CUDA graph of one step replayed" if graph is not None else "eager launches"
+    del P, graph
+    torch.cuda.empty_cache()
 
     extra = {}
     if rank == 0 and world == 1 and not args.no_extra:
-        extra["llama70b_layer"] = bench_llama70b(qlora, torch, dev, pk, 5)
+        extra["llama8b_layer"] = bench_layer(qlora, torch, dev, pk, LAYER8B, 100)
+        extra["single_layer"] = bench_layer(qlora, torch, dev, pk, SINGLE, 200)
+        extra["codec"] = bench_codec(qlora, torch, dev, pk)
         extra["gate_sweep"] = bench_sweep(qlora, torch, dev, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(CPU_SAMPLE_TOKENS, projs, r, wl["scale"])
+        cpu = cpu_baseline()
 
     if rank == 0:
         line = {
@@ -601,19 +719,19 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "pct_bf16_peak": value / world / pk["bf16"], "pct_bf16_peak_sustained": value / world / pk["bf16_sus"],
-            "config": {"workload": wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=16 alpha=32",
-                       "M": M, "r": r, "projections": [[n_, k_] for _, n_, k_ in projs],
+            "config": {"workload": wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=64 alpha=16",
+                       "M": M, "r": r, "alpha": wl["alpha"], "projections": [[n_, k_] for _, n_, k_ in projs],
                        "flops_per_step": flops, "parallelism": f"dp{world}",
-                       "l2": "inputs larger than L2 (about 0.5 GB touched per step)"},
+                       "l2": "inputs larger than L2 (several GB touched per step)",
+                       "l2_cache_bytes": int(props.L2_cache_size), "sm_count": props.multi_processor_count},
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
-            "kernels_ms_per_step": {k: v / prof_steps for k, v in prof_ms.items() if prof_n[k]},
-            "kernels_launches_per_step": {k: v // prof_steps for k, v in prof_n.items() if v},
-            "timed_region": "CUDA graph of one step replayed" if graph is not None else "eager launches",
+            "kernels_ms_per_step_eager": kind_ms,
+            "kernels_launches_per_step": kind_n,
+            "timed_region": timed_region,
             "clocks": clocks,
-            "codec": codec,
             **extra,
         }
         print(json.dumps(line), flush=True)

@@ -99,6 +99,13 @@ __device__ __forceinline__ void tc_commit2_both(uint64_t *bar) {
         "h"((uint16_t)0x3)
         : "memory");
 }
+// Arrive once on this CTA's barrier `bar` when all tcgen05 operations issued
+// so far by this thread complete.
+__device__ __forceinline__ void tc_commit2_self(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
 __device__ __forceinline__ uint32_t pair_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -324,6 +331,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     uint64_t *tfull = bar + 3 * C::STAGES;      // accumulators complete (commit from the even CTA)
     uint64_t *tempty = bar + 3 * C::STAGES + 1; // even CTA: accumulators drained (8 warp arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * C::STAGES + 2);
+    uint64_t *mdrain = bar + 3 * C::STAGES + 3; // even CTA: every MMA issued has completed
     uint64_t *fixbar = bar + 16;                // NFIX per epilogue warp: partial pieces fetched for finishing
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -346,6 +354,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         }
         mbar_init(tfull, 1);
         mbar_init(tempty, 2 * C::EPI_WARPS);
+        mbar_init(mdrain, 1);
         for (int i = 0; i < C::NFIX * C::EPI_WARPS; ++i) mbar_init(&fixbar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -434,9 +443,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             for (int s = 0; s < C::STAGES; ++s) {
                 if (g <= s) break;
                 const int64_t last = g - 1 - ((g - 1 - s) % C::STAGES);
-                const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(&full[s], (uint32_t)(last / C::STAGES) & 1))
-                    if (globaltimer() - t0 > p.wait_ns) break;
+                drain_wait(&full[s], (uint32_t)(last / C::STAGES) & 1);
             }
         }
     } else if (warp == 1) {
@@ -476,6 +483,13 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                     tc_commit2_both(&empty[s]);
                 }
                 tc_commit2_both(tfull);
+            }
+            // every MMA issued (also after an abort, when the epilogue may not
+            // have waited for the last ones) completes before the pair gives
+            // up its operand tiles and TMEM
+            if (g > 0) {
+                tc_commit2_self(mdrain);
+                drain_wait(mdrain, 0);
             }
         }
     } else if (warp < 2 + C::GROUP_WARPS * C::DEC_GROUPS) {
@@ -749,11 +763,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         // after an abort: let the fetches still in flight land before the
         // shared memory is given up
         if (lane == 0) {
-            for (int i = fx_waited; i < fx_issued; ++i) {
-                const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(&fixbar[ew * C::NFIX + i % C::NFIX], (uint32_t)(i / C::NFIX) & 1))
-                    if (globaltimer() - t0 > p.wait_ns) break;
-            }
+            for (int i = fx_waited; i < fx_issued; ++i)
+                drain_wait(&fixbar[ew * C::NFIX + i % C::NFIX], (uint32_t)(i / C::NFIX) & 1);
         }
     }
     tc_fence_before();

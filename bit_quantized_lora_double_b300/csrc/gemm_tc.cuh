@@ -57,6 +57,21 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Limit of the waits that drain a kernel's own asynchronous work (bulk copies
+// and tensor-core operations it issued) before it gives up shared memory or
+// TMEM. That work always completes, so these waits are independent of the
+// adjustable limit of the pipeline waits (which a test may set very low).
+constexpr uint64_t kDrainNs = 2000000000ull;
+
+// Waits (at most kDrainNs) for phase `parity` of `bar`; false if it did not
+// complete in that time.
+__device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kDrainNs) return false;
+    return true;
+}
+
 // Wait for phase `parity` of `bar` with a time limit; false (and the error
 // word recorded) when the limit runs out or another role already aborted.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns, unsigned code,

@@ -24,6 +24,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "gemm_tc.cuh"
 
 namespace qlora {
 
@@ -266,9 +267,7 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
             for (int s = 0; s < C::STAGES; ++s) {
                 if (issued <= s) break;
                 const int64_t last = issued - 1 - ((issued - 1 - s) % C::STAGES);
-                const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(&full[s], (uint32_t)(last / C::STAGES) & 1))
-                    if (globaltimer() - t0 > p.wait_ns) break;
+                drain_wait(&full[s], (uint32_t)(last / C::STAGES) & 1);
             }
         }
     } else if (warp == 1) {
@@ -292,6 +291,9 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
                 tc_commit(&empty[s]);
             }
             tc_commit(accfull);
+            // every MMA issued has completed before TMEM is given up (after an
+            // abort the epilogue does not wait for this commit)
+            drain_wait(accfull, 0);
         }
     } else {
         // -------------------- warps 2..5: one output row per thread ----

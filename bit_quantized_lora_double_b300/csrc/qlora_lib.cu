@@ -8,6 +8,7 @@
 #include <string>
 #include <vector>
 #include <algorithm>
+#include <array>
 
 #include "qlora.h"
 
@@ -81,6 +82,30 @@ qlora_status launch_check(const char *what) {
     return QLORA_OK;
 }
 
+// Sets a kernel's dynamic shared memory limit once per (kernel, device): the
+// attribute belongs to the device that is current when it is set.
+std::mutex g_attr_mu;
+std::vector<std::pair<const void *, int>> g_attr_done;
+
+template <class Kern>
+cudaError_t smem_attr(Kern kern, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const void *key = reinterpret_cast<const void *>(kern);
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    for (const auto &d : g_attr_done)
+        if (d.first == key && d.second == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_attr_done.push_back({key, dev});
+    return e;
+}
+
+int current_device() {
+    int dev = 0;
+    return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
 bool valid_dims(int64_t rows, int64_t cols) {
     return rows >= 0 && cols > 0 && cols % kBlock == 0 && rows < kMaxDim && cols < kMaxDim;
 }
@@ -126,6 +151,49 @@ size_t quantize_ws(int64_t rows, int64_t cols, float **absmax, double **gsum, do
     if (buf0) *buf0 = b0;
     if (buf1) *buf1 = b1;
     return c.off;
+}
+
+// The quantizer's launch sequence on a carved scratch area (the caller's
+// workspace or the built-in array): encode with the exact absmax and the
+// group sums of the pairwise tree, the tree's upper levels 256 values at a
+// time down to the mean, then the int8 codes and group scales.
+qlora_status quantize_launch(const void *W, qlora_nf4_weight *out, float *absmax, double *gsum, double *b0,
+                             double *b1, cudaStream_t s) {
+    const int64_t nb = out->rows * out->cols / kBlock, ng = cdiv(nb, kGroup);
+    qlora_status st;
+    {
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_nf4_encode<<<(unsigned)ng, 256, 0, s>>>(static_cast<const uint4 *>(W), nb,
+                                                 reinterpret_cast<uint32_t *>(out->codes), absmax, gsum);
+    }
+    if ((st = launch_check("k_nf4_encode"))) return st;
+    const double *cur = gsum;
+    int64_t n = ng;
+    double *bufs[2] = {b0, b1};
+    int flip = 0;
+    while (n > 256) {
+        const int64_t chunks = cdiv(n, 256);
+        {
+            ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+            k_pairwise_reduce<<<(unsigned)cdiv(chunks, 8), 256, 0, s>>>(cur, n, bufs[flip], nullptr, nb);
+        }
+        if ((st = launch_check("k_pairwise_reduce"))) return st;
+        cur = bufs[flip];
+        flip ^= 1;
+        n = chunks;
+    }
+    {
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_pairwise_reduce<<<1, 256, 0, s>>>(cur, n, nullptr, out->absmax_mean, nb);
+    }
+    if ((st = launch_check("k_pairwise_reduce(mean)"))) return st;
+    {
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_dq_encode<<<(unsigned)cdiv(ng, 8), 256, 0, s>>>(absmax, nb, out->absmax_mean, out->absmax_q,
+                                                          out->absmax_scale);
+    }
+    if ((st = launch_check("k_dq_encode"))) return st;
+    return ok();
 }
 
 // ---- linear workspaces
@@ -282,22 +350,24 @@ qlora_status tc_device_ok() {
 
 template <int MODE>
 qlora_status tc_setup() {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(k_gemm_pair<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   PairCfg::SMEM_BYTES);
-    });
+    const cudaError_t err = smem_attr(k_gemm_pair<MODE>, PairCfg::SMEM_BYTES);
     if (err != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(err));
     return QLORA_OK;
 }
 
-// Pairs of the persistent fused GEMM that the device holds at once.
+// Pairs of the persistent fused GEMM that the current device holds at once
+// (queried once per device; the kernel's attribute is set by tc_setup first).
 template <int MODE>
 int64_t gemm_pairs_resident() {
-    static std::once_flag once;
-    static int n = 0;
-    std::call_once(once, [] {
+    static std::mutex mu;
+    static std::vector<std::pair<int, int>> cache;  // (device, clusters)
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lock(mu);
+    int n = -1;
+    for (const auto &c : cache)
+        if (c.first == dev) n = c.second;
+    if (n < 0) {
+        n = 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(PairCfg::THREADS);
@@ -313,7 +383,8 @@ int64_t gemm_pairs_resident() {
             cudaGetLastError();
             n = 0;
         }
-    });
+        cache.push_back({dev, n});
+    }
     return n > 0 ? std::min<int64_t>(n, PairCfg::MAX_PAIRS) : PairCfg::MAX_PAIRS;
 }
 
@@ -428,8 +499,17 @@ SkParams sk_params(const SkJob &j, int r, unsigned id) {
 template <int A_MN, int B_MN>
 int skinny_max_clusters(int c) {
     static std::mutex mu;
-    static int cache[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    static std::vector<std::pair<int, std::array<int, 9>>> caches;  // per device
+    const int dev = current_device();
     std::lock_guard<std::mutex> g(mu);
+    std::array<int, 9> *cachep = nullptr;
+    for (auto &d : caches)
+        if (d.first == dev) cachep = &d.second;
+    if (!cachep) {
+        caches.push_back({dev, {-1, -1, -1, -1, -1, -1, -1, -1, -1}});
+        cachep = &caches.back().second;
+    }
+    std::array<int, 9> &cache = *cachep;
     if (cache[c] < 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, (unsigned)c, 1);
@@ -467,12 +547,7 @@ int64_t skinny_chunks(int64_t clusters, int64_t steps) {
 template <int A_MN, int B_MN>
 qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsigned id, uint32_t *zero = nullptr,
                         int nzero = 0) {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(k_lora_skinny<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   SkCfg::SMEM_BYTES);
-    });
+    const cudaError_t err = smem_attr(k_lora_skinny<A_MN, B_MN>, SkCfg::SMEM_BYTES);
     if (err != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(err));
     SkJob j1v = j1p ? *j1p : j0;
     const SkJob *j1 = j1p ? &j1v : nullptr;
@@ -601,66 +676,55 @@ qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, 
     const size_t need = quantize_ws(rows, cols, &absmax, &gsum, &b0, &b1, ws);
     if (ws_bytes < need)
         return fail(QLORA_ERR_WORKSPACE, "quantize workspace %zu < %zu bytes", ws_bytes, need);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t nb = rows * cols / kBlock, ng = cdiv(nb, kGroup);
-    {
-        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
-        k_nf4_encode<<<(unsigned)ng, 256, 0, s>>>(static_cast<const uint4 *>(W), nb,
-                                                 reinterpret_cast<uint32_t *>(out->codes), absmax, gsum);
-    }
-    if ((st = launch_check("k_nf4_encode"))) return st;
-    // continue the pairwise tree over the group sums, 256 per warp
-    const double *cur = gsum;
-    int64_t n = ng;
-    double *bufs[2] = {b0, b1};
-    int flip = 0;
-    while (n > 256) {
-        const int64_t chunks = cdiv(n, 256);
-        {
-            ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
-            k_pairwise_reduce<<<(unsigned)cdiv(chunks, 8), 256, 0, s>>>(cur, n, bufs[flip], nullptr, nb);
-        }
-        if ((st = launch_check("k_pairwise_reduce"))) return st;
-        cur = bufs[flip];
-        flip ^= 1;
-        n = chunks;
-    }
-    {
-        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
-        k_pairwise_reduce<<<1, 256, 0, s>>>(cur, n, nullptr, out->absmax_mean, nb);
-    }
-    if ((st = launch_check("k_pairwise_reduce(mean)"))) return st;
-    {
-        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
-        k_dq_encode<<<(unsigned)cdiv(ng, 8), 256, 0, s>>>(absmax, nb, out->absmax_mean, out->absmax_q,
-                                                          out->absmax_scale);
-    }
-    if ((st = launch_check("k_dq_encode"))) return st;
-    return ok();
+    return quantize_launch(W, out, absmax, gsum, b0, b1, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---- quantize without a caller workspace ------------------------------------
 // The scratch lives in this file-scope device array. In host code its name is
-// only a host-side stand-in, so the device address is looked up with
-// cudaGetSymbolAddress, once per device, with that device current.
+// only a host-side stand-in, so its device address is looked up with
+// cudaGetSymbolAddress. A __device__ array has one instance per CUDA context,
+// so the address is cached per context (the current one at the call), which
+// covers a host that drives the same GPU through several contexts.
 static __device__ __align__(256) unsigned char g_quantize_scratch[QLORA_NF4_NOALLOC_SCRATCH_BYTES];
 static std::mutex g_scratch_mu;
-static void *g_scratch_ptr[128] = {};
+static std::vector<std::pair<CUcontext, void *>> g_scratch_ptr;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+static CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    });
+    return fn;
+}
 
 static qlora_status quantize_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= 128) return fail(QLORA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    if (!get) return fail(QLORA_ERR_UNSUPPORTED, "cuCtxGetCurrent is not available from the driver");
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return fail(QLORA_ERR_CUDA, "cannot read the current CUDA context");
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_quantize_scratch);
-        if (e != cudaSuccess || !p)
-            return fail(QLORA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
+    if (ctx) {
+        for (const auto &c : g_scratch_ptr)
+            if (c.first == ctx) {
+                *out = c.second;
+                return QLORA_OK;
+            }
     }
-    *out = g_scratch_ptr[dev];
+    // first call in this context (with no context current yet, the runtime
+    // binds the current device's primary context here)
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_quantize_scratch);
+    if (e != cudaSuccess || !p) return fail(QLORA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx)) return fail(QLORA_ERR_CUDA, "no current CUDA context");
+    g_scratch_ptr.push_back({ctx, p});
+    *out = p;
     return QLORA_OK;
 }
 
@@ -682,29 +746,7 @@ qlora_status qlora_nf4_quantize_noalloc(const void *W, qlora_nf4_weight *out, ql
     float *absmax;
     double *gsum, *b0, *b1;
     quantize_ws(rows, cols, &absmax, &gsum, &b0, &b1, scratch);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t nb = rows * cols / kBlock, ng = cdiv(nb, kGroup);
-    k_nf4_encode<<<(unsigned)ng, 256, 0, s>>>(static_cast<const uint4 *>(W), nb,
-                                             reinterpret_cast<uint32_t *>(out->codes), absmax, gsum);
-    if ((st = launch_check("k_nf4_encode"))) return st;
-    const double *cur = gsum;
-    int64_t n = ng;
-    double *bufs[2] = {b0, b1};
-    int flip = 0;
-    while (n > 256) {
-        const int64_t chunks = cdiv(n, 256);
-        k_pairwise_reduce<<<(unsigned)cdiv(chunks, 8), 256, 0, s>>>(cur, n, bufs[flip], nullptr, nb);
-        if ((st = launch_check("k_pairwise_reduce"))) return st;
-        cur = bufs[flip];
-        flip ^= 1;
-        n = chunks;
-    }
-    k_pairwise_reduce<<<1, 256, 0, s>>>(cur, n, nullptr, out->absmax_mean, nb);
-    if ((st = launch_check("k_pairwise_reduce(mean)"))) return st;
-    k_dq_encode<<<(unsigned)cdiv(ng, 8), 256, 0, s>>>(absmax, nb, out->absmax_mean, out->absmax_q,
-                                                      out->absmax_scale);
-    if ((st = launch_check("k_dq_encode"))) return st;
-    return ok();
+    return quantize_launch(W, out, absmax, gsum, b0, b1, reinterpret_cast<cudaStream_t>(stream));
 }
 
 qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream) {
@@ -715,11 +757,7 @@ qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_st
     if (w->rows == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t nb = w->rows * w->cols / kBlock;
-    static std::once_flag once;
-    static cudaError_t aerr = cudaSuccess;
-    std::call_once(once, [] {
-        aerr = cudaFuncSetAttribute(k_nf4_dequant, cudaFuncAttributeMaxDynamicSharedMemorySize, kDeqSmem);
-    });
+    const cudaError_t aerr = smem_attr(k_nf4_dequant, kDeqSmem);
     if (aerr != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
     // the output viewed as [blocks, 64] bf16 rows of 128 bytes
     CUtensorMap tmO;

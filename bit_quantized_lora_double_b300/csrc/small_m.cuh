@@ -111,9 +111,11 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
     }
     __syncthreads();
 
+    float acc[NT][4];
     if (warp == 4) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
+            int64_t issued = nstages < C::STAGES ? nstages : C::STAGES;
             for (int64_t st = C::STAGES; st < nstages; ++st) {
                 const int s = (int)(st % C::STAGES);
                 const uint32_t u = (uint32_t)(st / C::STAGES);
@@ -122,6 +124,13 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
                 tma_load_2d(ring[s], &tm_codes, &full[s], (int32_t)(st * C::STAGE_BLOCKS * 32), (int32_t)n0);
                 tma_load_2d(ring[s] + 2048, &tm_codes, &full[s], (int32_t)(st * C::STAGE_BLOCKS * 32 + 128),
                             (int32_t)n0);
+                issued = st + 1;
+            }
+            // every load issued has landed before the ring is reused for the
+            // partial sums (after an abort some were never consumed)
+            for (int s = 0; s < C::STAGES && s < issued; ++s) {
+                const int64_t last = issued - 1 - ((issued - 1 - s) % C::STAGES);
+                drain_wait(&full[s], (uint32_t)(last / C::STAGES) & 1);
             }
         }
     } else {
@@ -155,7 +164,6 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
             load_x(i, 0, xbuf[i][0]);
             load_x(i, 1, xbuf[i][1]);
         }
-        float acc[NT][4];
 #pragma unroll
         for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
         bool alive = true;
@@ -212,7 +220,12 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
                 load_x(st + P, 1, xbuf[i][1]);
             }
         }
+    }
+    // the producer's loads have all landed: the ring is free for the partials
+    __syncthreads();
+    if (warp < 4) {
         // partial sums of this warp: rows g, g + 8; tokens 8 j + 2 t, + 1
+        const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             red[warp][g][8 * j + 2 * t] = acc[j][0];
@@ -240,15 +253,6 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
         for (int jj = 0; jj < r; ++jj)
             l = fmaf(bf16lo_to_f32(sU[(int64_t)m * ldu + jj]), bf16lo_to_f32(B[n * r + jj]), l);
         Y[(int64_t)m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y + l));
-    }
-    // the producer's last loads have landed before the CTA exits
-    if (warp == 4 && lane == 0) {
-        for (int s = 0; s < C::STAGES && s < nstages; ++s) {
-            const int64_t last = nstages - 1 - ((nstages - 1 - s) % C::STAGES);
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(&full[s], (uint32_t)(last / C::STAGES) & 1))
-                if (globaltimer() - t0 > wait_ns) break;
-        }
     }
 }
 

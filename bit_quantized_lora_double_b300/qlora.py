@@ -223,8 +223,8 @@ def qlora_check_device_status(stream=None):
     _check(lib().qlora_check_device_status(_stream(stream)))
 
 
-def qlora_set_wait_limit(spins: int):
-    lib().qlora_set_wait_limit(int(spins))
+def qlora_set_wait_limit(microseconds: int):
+    lib().qlora_set_wait_limit(int(microseconds))
 
 
 def qlora_version() -> str:

@@ -143,9 +143,9 @@ qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, 
  *    (qlora_nf4_quantize_workspace) exceeds that size is rejected with
  *    QLORA_ERR_WORKSPACE and nothing is launched (16 MiB covers about
  *    2.6e8 weights, e.g. 28672 x 8192).
- *  - The first call on each device (with that device current) looks up the
- *    array's device address once; make that first call before any stream
- *    capture.
+ *  - The first call in each CUDA context (on each device, with that device
+ *    current) looks up the array's device address once and caches it for
+ *    that context; make that first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents;
  *    nothing in it needs to start at zero. Calls that can overlap on the GPU
  *    (different streams without ordering between them) race on it: order
@@ -207,11 +207,13 @@ const char *qlora_last_error(void);
  * names the kernel and wait) or QLORA_ERR_CUDA. */
 qlora_status qlora_check_device_status(qlora_stream_t stream);
 
-/* Test hook: sets the iteration limit of the bounded waits in pipelined
- * kernels (0 restores the default). A limit of 1 makes any wait that is not
- * already satisfied run out at once. Host-side setting, applies to later
- * launches on all streams. */
-void qlora_set_wait_limit(int64_t spins);
+/* Test hook: sets the time limit, in microseconds, of the bounded pipeline
+ * waits in the kernels (0 or less restores the default of 2 s). A limit of 1
+ * makes a wait that is not satisfied within about 1 us (plus the hardware's
+ * own suspend interval, up to about 80 us) run out. The kernels' waits for
+ * their own copies and tensor-core work before they exit are not affected.
+ * Host-side setting, applies to later launches on all streams. */
+void qlora_set_wait_limit(int64_t microseconds);
 
 /* Profiling of the library's own kernels, for benchmarks. Between
  * qlora_profile_start() and qlora_profile_stop(), every kernel launch is

@@ -45,6 +45,10 @@ def lib():
         if _lib is None:
             L = ctypes.CDLL(build())
             i64, vp, f32, f64, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_double, ctypes.c_int
+            L.oracle_set_threads.restype = None
+            L.oracle_set_threads.argtypes = [i32]
+            L.oracle_max_threads.restype = i32
+            L.oracle_max_threads.argtypes = []
             L.oracle_norm_ppf.restype = f64
             L.oracle_norm_ppf.argtypes = [f64]
             L.oracle_norm_cdf.restype = f64
@@ -72,6 +76,17 @@ def lib():
                                             vp, i64, vp, i64, vp, i64, vp, vp, vp]
             _lib = L
     return _lib
+
+
+# -------------------------------------------------------------- threads ----
+
+def set_threads(n: int) -> None:
+    """Number of OpenMP threads the oracle's loops use from now on."""
+    lib().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
 
 
 # ---------------------------------------------------------------- table ----

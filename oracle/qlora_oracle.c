@@ -66,6 +66,17 @@ static uint16_t f32_to_bf16_rne(float f) {
 }
 
 uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+
+/* Thread count of the OpenMP loops below (for timing the oracle on a given
+ * number of host cores; no effect on any result). */
+#ifdef _OPENMP
+#include <omp.h>
+void oracle_set_threads(int n) { if (n > 0) omp_set_num_threads(n); }
+int oracle_max_threads(void) { return omp_get_max_threads(); }
+#else
+void oracle_set_threads(int n) { (void)n; }
+int oracle_max_threads(void) { return 1; }
+#endif
 float oracle_bf16_to_f32(uint16_t h) { return bf16_to_f32(h); }
 
 /* ------------------------------------------------------------------------ */
