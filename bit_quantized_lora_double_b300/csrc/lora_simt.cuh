@@ -27,14 +27,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 // (m, j), lanes striding over K in 8-element (16-byte) chunks, then a warp
 // reduction. Writes U (bf16, stride ldu, may be null) and sU = bf16(s * U)
 // (stride lds); the warps of the outputs (m, j) with r <= j < lds write the
-// zero padding of sU.
+// zero padding of sU. Block 0 also sets zero[0 .. nzero) to 0 (the following
+// kernel's arrival counters; zero may be null).
 __global__ void __launch_bounds__(256) k_lora_down(const uint16_t *__restrict__ P, int64_t M, int64_t K,
                                                    const uint16_t *__restrict__ Q, int r, float s,
                                                    uint16_t *__restrict__ U, int ldu, uint16_t *__restrict__ sU,
-                                                   int lds) {
+                                                   int lds, uint32_t *__restrict__ zero = nullptr, int nzero = 0) {
     // a forward launched as a programmatic dependent (the few-token kernel)
     // may start streaming its weights now; it waits for U before using it
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (zero && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
     const int lane = threadIdx.x & 31;
     const int64_t o = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (o >= M * lds) return;

@@ -19,6 +19,7 @@
 #include "gemm_pair.cuh"
 #include "lora_tc.cuh"
 #include "small_m.cuh"
+#include "fwd_few.cuh"
 
 using namespace qlora;
 
@@ -241,15 +242,51 @@ SkArea take_sk_area(Carve &c) {
     return a;
 }
 
+// The few-token forward (k_fwd_few) serves M <= 16 when K is a multiple of
+// its 1024-deep stages; other few-token shapes take k_fwd_small.
+inline bool few_path(int64_t M, int64_t K) { return M <= 8 * FewCfg::MAX_NT && K % FewCfg::KSTAGE == 0; }
+
+// Its grid: one CTA per SM, more when a CTA's share of the slices would touch
+// more row groups than its shared memory holds sums for.
+struct FewPlan {
+    int64_t grid, slices, spg, groups;
+};
+FewPlan few_plan(int64_t N, int64_t K) {
+    FewPlan f;
+    f.groups = cdiv(N, FewCfg::ROWS);
+    f.spg = K / FewCfg::KSTAGE;
+    f.slices = f.groups * f.spg * FewCfg::WARPS;
+    int64_t G = std::min<int64_t>(FewCfg::GRID, f.slices);
+    while (true) {
+        int64_t worst = 0;
+        for (int64_t c = 0; c < G; ++c) {
+            int64_t g0, ng;
+            few_groups(c, G, f.slices, f.spg, g0, ng);
+            worst = std::max(worst, ng);
+        }
+        if (worst <= FewCfg::MAX_GROUPS || G >= f.slices) break;
+        G = std::min(f.slices, G + FewCfg::GRID);
+    }
+    f.grid = G;
+    return f;
+}
+
 struct FwdWs {
     uint16_t *sU, *Bp;
+    float *few_slots;
+    uint32_t *few_counters;
     SkArea sk;
 };
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     const bool tc = M > kSmallMaxM || K > kSmallMaxK;
     Carve c(ws);
     FwdWs f{};
-    if (!tc) {
+    if (few_path(M, K)) {
+        const FewPlan fp = few_plan(N, K);
+        f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
+        f.few_slots = c.take<float>((size_t)fp.grid * 2 * FewCfg::SUM_FLOATS);
+        f.few_counters = c.take<uint32_t>((size_t)fp.groups);
+    } else if (!tc) {
         f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
     } else {
         const int rs = lora_rs(r);
@@ -815,6 +852,68 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     const int rp = lora_pad(r);
     const uint16_t *X16 = static_cast<const uint16_t *>(X);
     uint16_t *U16 = static_cast<uint16_t *>(U_save);
+
+    if (few_path(M, K)) {
+        // few tokens, K a multiple of 1024: persistent HBM-bound kernel
+        if ((st = tc_device_ok())) return st;
+        const cudaError_t aerr = smem_attr(k_fwd_few<1>, FewCfg::SMEM_BYTES);
+        const cudaError_t aerr2 = smem_attr(k_fwd_few<2>, FewCfg::SMEM_BYTES);
+        if (aerr != cudaSuccess || aerr2 != cudaSuccess)
+            return fail(QLORA_ERR_CUDA, "setting shared memory size: %s",
+                        cudaGetErrorString(aerr != cudaSuccess ? aerr : aerr2));
+        const FewPlan fp = few_plan(N, K);
+        {
+            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+            k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
+                                                              U16, r, f.sU, rp, f.few_counters, (int)fp.groups);
+        }
+        if ((st = launch_check("k_lora_down"))) return st;
+        CUtensorMap tmC, tmQ;
+        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 64, FewCfg::ROWS,
+                           CU_TENSOR_MAP_SWIZZLE_64B, "codes")) ||
+            (st = make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->absmax_q, K / kBlock, N, K / kBlock, 16,
+                           FewCfg::ROWS, CU_TENSOR_MAP_SWIZZLE_NONE, "absmax codes")))
+            return st;
+        FewParams prm{};
+        prm.X = X16;
+        prm.M = M;
+        prm.N = N;
+        prm.K = K;
+        prm.s2 = w->absmax_scale;
+        prm.mean = w->absmax_mean;
+        prm.sU = f.sU;
+        prm.ldu = rp;
+        prm.B = static_cast<const uint16_t *>(B);
+        prm.r = r;
+        prm.Y = static_cast<uint16_t *>(Y);
+        prm.slots = f.few_slots;
+        prm.counters = f.few_counters;
+        prm.slices = fp.slices;
+        prm.spg = fp.spg;
+        prm.wait_ns = wait_ns();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)fp.grid);
+        cfg.blockDim = dim3(FewCfg::THREADS);
+        cfg.dynamicSmemBytes = FewCfg::SMEM_BYTES;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e;
+        {
+            ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
+            e = M <= 8 ? cudaLaunchKernelEx(&cfg, k_fwd_few<1>, tmC, tmQ, prm)
+                       : cudaLaunchKernelEx(&cfg, k_fwd_few<2>, tmC, tmQ, prm);
+        }
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(QLORA_ERR_CUDA, "k_fwd_few: launch failed: %s", cudaGetErrorString(e));
+        }
+        if ((st = launch_check("k_fwd_few"))) return st;
+        return ok();
+    }
 
     if (M <= kSmallMaxM && K <= kSmallMaxK) {
         // few tokens: HBM-bound path (mma.sync over the decoded weight rows)
