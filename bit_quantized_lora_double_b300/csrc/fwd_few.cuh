@@ -54,12 +54,16 @@ struct FewCfg {
     static constexpr int STAGES = 5;
     static constexpr int MAX_NT = 2;                    // 8-token tiles: up to 16 tokens
     static constexpr int SUM_FLOATS = ROWS * 8 * MAX_NT;  // one row group's sums [32][16]
-    static constexpr int MAX_GROUPS = 24;               // row groups one CTA may touch
+    static constexpr int MAX_GROUPS = 16;               // row groups one CTA may touch
+    static constexpr int B_BYTES = 32768;               // the CTA's rows of the LoRA B (bf16)
+    static constexpr int SU_FLOATS = 16 * 128;          // s*U [M <= 16][r <= 128] as fp32
     static constexpr int TABLE_WORDS = 256 * 32;        // 256 entries x 32 lane copies
     static constexpr int OFF_RING = TABLE_WORDS * 4;
     static constexpr int OFF_RED = OFF_RING + STAGES * STAGE_BYTES;
     static constexpr int OFF_SUM = OFF_RED + 2 * WARPS * SUM_FLOATS * 4;
-    static constexpr int OFF_BAR = OFF_SUM + MAX_GROUPS * SUM_FLOATS * 4;
+    static constexpr int OFF_B = OFF_SUM + MAX_GROUPS * SUM_FLOATS * 4;
+    static constexpr int OFF_SU = OFF_B + B_BYTES;
+    static constexpr int OFF_BAR = OFF_SU + SU_FLOATS * 4;
     static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr int GRID = 148;                    // CTAs before the row-group cap (one per SM)
 };
@@ -93,6 +97,12 @@ __host__ __device__ __forceinline__ int64_t few_cta_of(int64_t x, int64_t G, int
     while (c > 0 && few_begin(c, G, T) > x) --c;
     return c;
 }
+
+// 16-byte global -> shared copy that does not block the thread
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Row groups CTA c touches (first, count); count 0 for an empty range.
 __host__ __device__ __forceinline__ void few_groups(int64_t c, int64_t G, int64_t T, int64_t spg, int64_t &g0,
@@ -144,7 +154,7 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *empty = full + C::STAGES;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + C::STAGES);
-    volatile int *bcast = reinterpret_cast<volatile int *>(empty + C::STAGES) + 1;
+    volatile int *bcast = reinterpret_cast<volatile int *>(empty + C::STAGES) + 1;  // two words
     constexpr int SF = C::ROWS * 8 * NT;  // floats of one row group's sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,6 +171,20 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
+    }
+    // this CTA's rows of B (rows of its row groups, contiguous in B) start
+    // coming in now; they are needed only when the outputs are finished
+    int64_t g0, ng;
+    few_groups(c, G, T, spg, g0, ng);
+    const int64_t nB0 = g0 * C::ROWS, nB1 = p.N < (g0 + ng) * C::ROWS ? p.N : (g0 + ng) * C::ROWS;
+    uint16_t *sB = reinterpret_cast<uint16_t *>(smem + C::OFF_B);
+    {
+        const int64_t nbytes = nB1 > nB0 ? (nB1 - nB0) * p.r * 2 : 0;  // <= B_BYTES (host plan)
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.B + nB0 * p.r);  // 16-byte aligned: nB0 % 32 == 0
+        for (int64_t i = threadIdx.x; i < nbytes / 16; i += C::THREADS)
+            cp_async16(reinterpret_cast<uint8_t *>(sB) + 16 * i, src + 16 * i);
+        for (int64_t i = (nbytes / 16) * 8 + threadIdx.x; i < nbytes / 2; i += C::THREADS)
+            sB[i] = p.B[nB0 * p.r + i];
     }
     __syncthreads();
 
@@ -385,58 +409,71 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     // launched as a programmatic dependent of the kernel that writes sU and
     // zeroes the counters: everything above ran alongside it
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    int64_t g0, ng;
-    few_groups(c, G, T, spg, g0, ng);
-    for (int rl = 0; rl < ng; ++rl) {
-        const int64_t rg = g0 + rl;
-        const int64_t cf = few_cta_of(rg * 8 * spg, G, T), cl = few_cta_of((rg + 1) * 8 * spg - 1, G, T);
-        const float *mine = gsum + rl * SF;
-        bool finish = true;
-        if (cl > cf) {
-            // shared group: this CTA's partial to its slot (0: its first
-            // group, 1: its last), then the arrival count
-            float *slot = p.slots + (c * 2 + (rl == 0 ? 0 : 1)) * C::SUM_FLOATS;
+    float *sUf = reinterpret_cast<float *>(smem + C::OFF_SU);
+    for (int i = threadIdx.x; i < p.M * p.r; i += C::THREADS) {
+        const int m = i / p.r, jj = i - m * p.r;
+        sUf[i] = bf16lo_to_f32(p.sU[(int64_t)m * p.ldu + jj]);
+    }
+    // Row groups shared with other CTAs (only the first and the last can
+    // be): this CTA's partial goes to its slot (0: its first group, 1: its
+    // last), then one arrival per group; the last CTA to arrive finishes it.
+    int64_t cf[2] = {0, 0}, cl[2] = {0, 0};
+    bool split[2] = {false, false};
+    for (int e = 0; e < 2 && e < ng; ++e) {
+        const int64_t rg = e == 0 ? g0 : g0 + ng - 1;
+        cf[e] = few_cta_of(rg * 8 * spg, G, T);
+        cl[e] = few_cta_of((rg + 1) * 8 * spg - 1, G, T);
+        split[e] = cl[e] > cf[e];
+        if (split[e]) {
+            const float *mine = gsum + (e == 0 ? 0 : ng - 1) * SF;
+            float *slot = p.slots + (c * 2 + e) * C::SUM_FLOATS;
             for (int i = threadIdx.x; i < SF; i += C::THREADS) __stcg(slot + i, mine[i]);
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) *bcast = (int)atomicAdd(p.counters + rg, 1u);
-            __syncthreads();
-            finish = *bcast == (int)(cl - cf);
-            if (finish) __threadfence();
         }
-        if (finish) {
-            const int64_t n0 = rg * C::ROWS;
-            for (int o = threadIdx.x; o < C::ROWS * p.M; o += C::THREADS) {
-                const int row = o & (C::ROWS - 1);
-                const int m = o >> 5;
-                const int64_t n = n0 + row;
-                if (n >= p.N) continue;
-                const int idx = row * 8 * NT + m;
-                float v;
-                if (cl > cf) {
-                    // partials in CTA order (this CTA's from shared memory)
-                    v = 0.0f;
-                    for (int64_t cc = cf; cc <= cl; ++cc) {
-                        float part;
-                        if (cc == c) {
-                            part = mine[idx];
-                        } else {
-                            int64_t h0, hn;
-                            few_groups(cc, G, T, spg, h0, hn);
-                            part = __ldcg(p.slots + (cc * 2 + (rg == h0 ? 0 : 1)) * C::SUM_FLOATS + idx);
-                        }
-                        v = cc == cf ? part : v + part;
-                    }
+    }
+    __threadfence();
+    cp_async_wait_all();
+    __syncthreads();
+    if (threadIdx.x == 0 && split[0]) bcast[0] = (int)atomicAdd(p.counters + g0, 1u);
+    if (threadIdx.x == 32 && split[1]) bcast[1] = (int)atomicAdd(p.counters + g0 + ng - 1, 1u);
+    __syncthreads();
+    const bool fin0 = !split[0] || bcast[0] == (int)(cl[0] - cf[0]);
+    const bool fin1 = !split[1] || bcast[1] == (int)(cl[1] - cf[1]);
+    if (split[0] || split[1]) __threadfence();
+    // every output this CTA finishes, all groups at once
+    const int per = C::ROWS * (int)p.M;
+    for (int64_t o = threadIdx.x; o < ng * per; o += C::THREADS) {
+        const int rl = (int)(o / per);
+        const int rem = (int)(o - (int64_t)rl * per);
+        const int m = rem >> 5, row = rem & (C::ROWS - 1);
+        const int64_t rg = g0 + rl, n = rg * C::ROWS + row;
+        if (n >= p.N) continue;
+        const int e = rl == 0 ? 0 : (rl == ng - 1 ? 1 : -1);
+        const bool shared = e >= 0 && split[e];
+        if (shared && !(e == 0 ? fin0 : fin1)) continue;
+        const int idx = row * 8 * NT + m;
+        float v;
+        if (shared) {
+            // partials in CTA order (this CTA's from shared memory)
+            v = 0.0f;
+            for (int64_t cc = cf[e]; cc <= cl[e]; ++cc) {
+                float part;
+                if (cc == c) {
+                    part = gsum[rl * SF + idx];
                 } else {
-                    v = mine[idx];
+                    int64_t h0, hn;
+                    few_groups(cc, G, T, spg, h0, hn);
+                    part = __ldcg(p.slots + (cc * 2 + (rg == h0 ? 0 : 1)) * C::SUM_FLOATS + idx);
                 }
-                float l = 0.0f;
-                for (int jj = 0; jj < p.r; ++jj)
-                    l = fmaf(bf16lo_to_f32(p.sU[(int64_t)m * p.ldu + jj]), bf16lo_to_f32(p.B[n * p.r + jj]), l);
-                p.Y[(int64_t)m * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v + l));
+                v = cc == cf[e] ? part : v + part;
             }
+        } else {
+            v = gsum[rl * SF + idx];
         }
-        __syncthreads();
+        float l = 0.0f;
+        const uint16_t *brow = sB + (n - nB0) * p.r;
+        const float *urow = sUf + m * p.r;
+        for (int jj = 0; jj < p.r; ++jj) l = fmaf(urow[jj], bf16lo_to_f32(brow[jj]), l);
+        p.Y[(int64_t)m * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v + l));
     }
 }
 

@@ -23,28 +23,32 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// U[m, j] = sum_k P[m, k] Q[j, k] (fp32) for j < r: one warp per output
-// (m, j), lanes striding over K in 8-element (16-byte) chunks, then a warp
-// reduction. Writes U (bf16, stride ldu, may be null) and sU = bf16(s * U)
-// (stride lds); the warps of the outputs (m, j) with r <= j < lds write the
-// zero padding of sU. Block 0 also sets zero[0 .. nzero) to 0 (the following
-// kernel's arrival counters; zero may be null).
-__global__ void __launch_bounds__(256) k_lora_down(const uint16_t *__restrict__ P, int64_t M, int64_t K,
-                                                   const uint16_t *__restrict__ Q, int r, float s,
-                                                   uint16_t *__restrict__ U, int ldu, uint16_t *__restrict__ sU,
-                                                   int lds, uint32_t *__restrict__ zero = nullptr, int nzero = 0) {
+// U[m, j] = sum_k P[m, k] Q[j, k] (fp32) for j < r: one block of
+// kDownThreads per output (m, j), threads striding over K in 8-element
+// (16-byte) chunks, then a warp reduction and the warps' sums in warp order.
+// Writes U (bf16, stride ldu, may be null) and sU = bf16(s * U) (stride lds);
+// the blocks of the outputs (m, j) with r <= j < lds write the zero padding of
+// sU. Block 0 also sets zero[0 .. nzero) to 0 (the following kernel's arrival
+// counters; zero may be null). Grid: M * lds blocks.
+constexpr int kDownThreads = 128;
+__global__ void __launch_bounds__(kDownThreads) k_lora_down(const uint16_t *__restrict__ P, int64_t M, int64_t K,
+                                                            const uint16_t *__restrict__ Q, int r, float s,
+                                                            uint16_t *__restrict__ U, int ldu,
+                                                            uint16_t *__restrict__ sU, int lds,
+                                                            uint32_t *__restrict__ zero = nullptr, int nzero = 0) {
     // a forward launched as a programmatic dependent (the few-token kernel)
     // may start streaming its weights now; it waits for U before using it
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (zero && blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
-    const int lane = threadIdx.x & 31;
-    const int64_t o = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (o >= M * lds) return;
+    __shared__ float wsum[kDownThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t o = blockIdx.x;
     const int64_t m = o / lds;
     const int j = (int)(o % lds);
+    if (m >= M) return;
     if (j >= r) {
-        if (lane == 0) sU[m * lds + j] = 0;
+        if (threadIdx.x == 0) sU[m * lds + j] = 0;
         return;
     }
     float acc = 0.0f;
@@ -53,7 +57,7 @@ __global__ void __launch_bounds__(256) k_lora_down(const uint16_t *__restrict__ 
         const uint4 *pr = reinterpret_cast<const uint4 *>(P + m * K);
         const uint4 *qr = reinterpret_cast<const uint4 *>(Q + (int64_t)j * K);
 #pragma unroll 4
-        for (int64_t c = lane; c < K / 8; c += 32) {
+        for (int64_t c = threadIdx.x; c < K / 8; c += kDownThreads) {
             const uint4 x = __ldg(pr + c), a = __ldg(qr + c);
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, as[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
@@ -63,13 +67,18 @@ __global__ void __launch_bounds__(256) k_lora_down(const uint16_t *__restrict__ 
             }
         }
     } else {
-        for (int64_t c = lane; c < K; c += 32)
+        for (int64_t c = threadIdx.x; c < K; c += kDownThreads)
             acc = fmaf(bf16lo_to_f32(P[m * K + c]), bf16lo_to_f32(Q[(int64_t)j * K + c]), acc);
     }
     acc = warp_sum(acc);
-    if (lane == 0) {
-        if (U) U[m * ldu + j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-        sU[m * lds + j] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, acc)));
+    if (lane == 0) wsum[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = wsum[0];
+#pragma unroll
+        for (int w = 1; w < kDownThreads / 32; ++w) t += wsum[w];
+        if (U) U[m * ldu + j] = __bfloat16_as_ushort(__float2bfloat16_rn(t));
+        sU[m * lds + j] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, t)));
     }
 }
 

@@ -247,11 +247,12 @@ SkArea take_sk_area(Carve &c) {
 inline bool few_path(int64_t M, int64_t K) { return M <= 8 * FewCfg::MAX_NT && K % FewCfg::KSTAGE == 0; }
 
 // Its grid: one CTA per SM, more when a CTA's share of the slices would touch
-// more row groups than its shared memory holds sums for.
+// more row groups than its shared memory holds sums (or rows of B) for.
 struct FewPlan {
     int64_t grid, slices, spg, groups;
 };
-FewPlan few_plan(int64_t N, int64_t K) {
+FewPlan few_plan(int64_t N, int64_t K, int r) {
+    const int64_t max_groups = std::min<int64_t>(FewCfg::MAX_GROUPS, FewCfg::B_BYTES / (FewCfg::ROWS * 2 * r));
     FewPlan f;
     f.groups = cdiv(N, FewCfg::ROWS);
     f.spg = K / FewCfg::KSTAGE;
@@ -264,7 +265,7 @@ FewPlan few_plan(int64_t N, int64_t K) {
             few_groups(c, G, f.slices, f.spg, g0, ng);
             worst = std::max(worst, ng);
         }
-        if (worst <= FewCfg::MAX_GROUPS || G >= f.slices) break;
+        if (worst <= max_groups || G >= f.slices) break;
         G = std::min(f.slices, G + FewCfg::GRID);
     }
     f.grid = G;
@@ -282,7 +283,7 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     Carve c(ws);
     FwdWs f{};
     if (few_path(M, K)) {
-        const FewPlan fp = few_plan(N, K);
+        const FewPlan fp = few_plan(N, K, r);
         f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
         f.few_slots = c.take<float>((size_t)fp.grid * 2 * FewCfg::SUM_FLOATS);
         f.few_counters = c.take<uint32_t>((size_t)fp.groups);
@@ -861,10 +862,10 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         if (aerr != cudaSuccess || aerr2 != cudaSuccess)
             return fail(QLORA_ERR_CUDA, "setting shared memory size: %s",
                         cudaGetErrorString(aerr != cudaSuccess ? aerr : aerr2));
-        const FewPlan fp = few_plan(N, K);
+        const FewPlan fp = few_plan(N, K, r);
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
+            k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
                                                               U16, r, f.sU, rp, f.few_counters, (int)fp.groups);
         }
         if ((st = launch_check("k_lora_down"))) return st;
@@ -920,7 +921,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         if ((st = tc_device_ok())) return st;
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
+            k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
                                                               U16, r, f.sU, rp);
         }
         if ((st = launch_check("k_lora_down"))) return st;
@@ -1046,7 +1047,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
         if ((st = launch_check("k_transpose"))) return st;
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, rp);
+            k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(dY16, M, N, b.Bt, r, scale, nullptr, 0, b.sV, rp);
         }
         if ((st = launch_check("k_lora_down(V)"))) return st;
         const uint16_t *U = static_cast<const uint16_t *>(U_saved);
@@ -1054,7 +1055,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
         if (!U) {
             {
                 ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-                k_lora_down<<<(unsigned)cdiv(M * rp, 8), 256, 0, s>>>(X16, M, K, A16, r, 1.0f, nullptr, 0, b.U, rp);
+                k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, A16, r, 1.0f, nullptr, 0, b.U, rp);
             }
             if ((st = launch_check("k_lora_down(U)"))) return st;
             U = b.U;
