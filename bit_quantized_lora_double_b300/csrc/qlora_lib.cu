@@ -243,8 +243,11 @@ SkArea take_sk_area(Carve &c) {
 }
 
 // The few-token forward (k_fwd_few) serves M <= 16 when K is a multiple of
-// its 1024-deep stages; other few-token shapes take k_fwd_small.
-inline bool few_path(int64_t M, int64_t K) { return M <= 8 * FewCfg::MAX_NT && K % FewCfg::KSTAGE == 0; }
+// its 1024-deep stages (and the block count fits 31 bits); other few-token
+// shapes take k_fwd_small.
+inline bool few_path(int64_t M, int64_t N, int64_t K) {
+    return M <= 8 * FewCfg::MAX_NT && K % FewCfg::KSTAGE == 0 && N * (K / kBlock) < (int64_t(1) << 31);
+}
 
 // Its grid: one CTA per SM, more when a CTA's share of the slices would touch
 // more row groups than its shared memory holds sums (or rows of B) for.
@@ -282,7 +285,7 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     const bool tc = M > kSmallMaxM || K > kSmallMaxK;
     Carve c(ws);
     FwdWs f{};
-    if (few_path(M, K)) {
+    if (few_path(M, N, K)) {
         const FewPlan fp = few_plan(N, K, r);
         f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
         f.few_slots = c.take<float>((size_t)fp.grid * 2 * FewCfg::SUM_FLOATS);
@@ -854,7 +857,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     const uint16_t *X16 = static_cast<const uint16_t *>(X);
     uint16_t *U16 = static_cast<uint16_t *>(U_save);
 
-    if (few_path(M, K)) {
+    if (few_path(M, N, K)) {
         // few tokens, K a multiple of 1024: persistent HBM-bound kernel
         if ((st = tc_device_ok())) return st;
         const cudaError_t aerr = smem_attr(k_fwd_few<1>, FewCfg::SMEM_BYTES);
@@ -865,13 +868,17 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         const FewPlan fp = few_plan(N, K, r);
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
-                                                              U16, r, f.sU, rp, f.few_counters, (int)fp.groups);
+            k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r,
+                                                                 scale, U16, r, f.sU, rp, f.few_counters,
+                                                                 (int)fp.groups);
         }
         if ((st = launch_check("k_lora_down"))) return st;
         CUtensorMap tmC, tmQ;
-        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 64, FewCfg::ROWS,
-                           CU_TENSOR_MAP_SWIZZLE_64B, "codes")) ||
+        // code boxes of 128 bytes x 32 rows (FewCfg::BOX_BYTES, what the kernel
+        // expects per box), 128-byte swizzle
+        static_assert(FewCfg::BOX_BYTES == 128 * FewCfg::ROWS, "code box");
+        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, FewCfg::ROWS,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "codes")) ||
             (st = make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->absmax_q, K / kBlock, N, K / kBlock, 16,
                            FewCfg::ROWS, CU_TENSOR_MAP_SWIZZLE_NONE, "absmax codes")))
             return st;
