@@ -20,6 +20,8 @@
 #include "lora_tc.cuh"
 #include "small_m.cuh"
 #include "fwd_few.cuh"
+#include "merge.cuh"
+#include "adamw.cuh"
 
 using namespace qlora;
 
@@ -788,6 +790,93 @@ qlora_status qlora_nf4_quantize_noalloc(const void *W, qlora_nf4_weight *out, ql
     double *gsum, *b0, *b1;
     quantize_ws(rows, cols, &absmax, &gsum, &b0, &b1, scratch);
     return quantize_launch(W, out, absmax, gsum, b0, b1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t qlora_lora_merge_workspace(int64_t rows, int64_t cols) {
+    if (!valid_dims(rows, cols) || rows == 0) return 0;
+    return up((size_t)(rows * cols) * 2, 256) + quantize_ws(rows, cols, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+qlora_status qlora_lora_merge_requantize(const qlora_nf4_weight *w, const void *A, const void *B, int r, float scale,
+                                         qlora_nf4_weight *out, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    qlora_status st = check_weight(w, false);
+    if (st) return st;
+    if ((st = check_weight(out, false))) return st;
+    if (out->rows != w->rows || out->cols != w->cols)
+        return fail(QLORA_ERR_SHAPE, "merged weight [%lld, %lld] differs from the base [%lld, %lld]",
+                    (long long)out->rows, (long long)out->cols, (long long)w->rows, (long long)w->cols);
+    if (r < 1 || r > 128) return fail(QLORA_ERR_RANK, "LoRA rank r = %d outside [1, 128]", r);
+    if (!A || !B) return fail(QLORA_ERR_NULL, "LoRA A or B is NULL");
+    if (!al16(A) || !al16(B)) return fail(QLORA_ERR_ALIGN, "LoRA A and B must be 16-byte aligned");
+    const int64_t N = w->rows, K = w->cols;
+    if (N == 0) return ok();
+    if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
+    if (!al16(ws)) return fail(QLORA_ERR_ALIGN, "workspace must be 16-byte aligned");
+    const size_t need = qlora_lora_merge_workspace(N, K);
+    if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "merge workspace %zu < %zu bytes", ws_bytes, need);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t *merged = static_cast<uint16_t *>(ws);
+    const int64_t chunks = N * K / 8;
+    {
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_lora_merge<<<(unsigned)cdiv(chunks, 256), 256, 0, s>>>(
+            reinterpret_cast<const uint32_t *>(w->codes), w->absmax_q, w->absmax_scale, w->absmax_mean, N, K,
+            static_cast<const uint16_t *>(A), static_cast<const uint16_t *>(B), r, scale,
+            reinterpret_cast<uint4 *>(merged));
+    }
+    if ((st = launch_check("k_lora_merge"))) return st;
+    float *absmax;
+    double *gsum, *b0, *b1;
+    quantize_ws(N, K, &absmax, &gsum, &b0, &b1, static_cast<char *>(ws) + up((size_t)(N * K) * 2, 256));
+    return quantize_launch(merged, out, absmax, gsum, b0, b1, s);
+}
+
+// A pointer the device can dereference: device or managed memory, or host
+// memory that is pinned (registered); pageable host memory is not.
+static bool device_reachable(const void *ptr) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+           (a.type == cudaMemoryTypeHost && a.devicePointer == ptr);
+}
+
+qlora_status qlora_adamw_step(float *param, uint16_t *param_bf16, const float *grad, float *m, float *v, int64_t n,
+                              float lr, float beta1, float beta2, float eps, float weight_decay, int64_t step,
+                              qlora_stream_t stream) {
+    if (n < 0) return fail(QLORA_ERR_SHAPE, "n = %lld < 0", (long long)n);
+    if (step < 1) return fail(QLORA_ERR_SHAPE, "step = %lld < 1", (long long)step);
+    if (n == 0) return ok();
+    if (!param || !grad || !m || !v) return fail(QLORA_ERR_NULL, "param, grad, m or v is NULL");
+    if (!al16(param) || !al16(grad) || !al16(m) || !al16(v) || (param_bf16 && (reinterpret_cast<uintptr_t>(param_bf16) & 7)))
+        return fail(QLORA_ERR_ALIGN, "param, grad, m, v must be 16-byte aligned, param_bf16 8-byte aligned");
+    if (!(beta1 >= 0.0f && beta1 < 1.0f && beta2 >= 0.0f && beta2 < 1.0f && eps > 0.0f))
+        return fail(QLORA_ERR_SHAPE, "need 0 <= beta1, beta2 < 1 and eps > 0");
+    const void *ptrs[5] = {param, grad, m, v, param_bf16};
+    for (int i = 0; i < 5; ++i)
+        if (ptrs[i] && !device_reachable(ptrs[i]))
+            return fail(QLORA_ERR_UNSUPPORTED, "pointer %d is not reachable from the device (pageable host memory?)", i);
+    AdamwParams h;
+    const double b1t = 1.0 - pow((double)beta1, (double)step), b2t = 1.0 - pow((double)beta2, (double)step);
+    h.decay = (float)(1.0 - (double)lr * (double)weight_decay);
+    h.b1 = beta1;
+    h.b2 = beta2;
+    h.one_m_b1 = 1.0f - beta1;
+    h.one_m_b2 = 1.0f - beta2;
+    h.step = (float)((double)lr / b1t);
+    h.c2 = (float)sqrt(b2t);
+    h.eps = eps;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const unsigned grid = (unsigned)std::min<int64_t>(std::max<int64_t>(1, cdiv(n / 4, 256)), 148 * 8);
+    {
+        ProfScope ps(QLORA_KERNEL_OPTIM, s);
+        k_adamw<<<grid, 256, 0, s>>>(param, param_bf16, grad, m, v, n, h);
+    }
+    qlora_status st = launch_check("k_adamw");
+    if (st) return st;
+    return ok();
 }
 
 qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream) {

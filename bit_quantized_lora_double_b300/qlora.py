@@ -31,9 +31,10 @@ EXPORTS = [
     "qlora_linear_fwd_workspace", "qlora_linear_bwd_workspace", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_last_error", "qlora_check_device_status", "qlora_set_wait_limit", "qlora_version",
     "qlora_profile_start", "qlora_profile_stop", "qlora_debug_gemm_segments",
+    "qlora_lora_merge_workspace", "qlora_lora_merge_requantize", "qlora_adamw_step",
 ]
 
-KERNEL_KINDS = ["quantize", "dequant", "lora_pre", "fwd_gemm", "fwd_simt", "dx_gemm", "dx_simt", "grads"]
+KERNEL_KINDS = ["quantize", "dequant", "lora_pre", "fwd_gemm", "fwd_simt", "dx_gemm", "dx_simt", "grads", "optim"]
 
 
 class QloraError(RuntimeError):
@@ -89,6 +90,12 @@ def lib():
         L.qlora_profile_start.argtypes = []
         L.qlora_profile_stop.restype = i32
         L.qlora_profile_stop.argtypes = [vp, vp]
+        L.qlora_lora_merge_workspace.restype = sz
+        L.qlora_lora_merge_workspace.argtypes = [i64, i64]
+        L.qlora_lora_merge_requantize.restype = i32
+        L.qlora_lora_merge_requantize.argtypes = [W, vp, vp, i32, f32, W, vp, sz, vp]
+        L.qlora_adamw_step.restype = i32
+        L.qlora_adamw_step.argtypes = [vp, vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, i64, vp]
         L.qlora_debug_gemm_segments.restype = i64
         L.qlora_debug_gemm_segments.argtypes = [i64, i64, i64, i32, i32, vp, i64]
         _lib = L
@@ -213,6 +220,24 @@ def qlora_linear_bwd(dY, X, U_saved, M, w: Nf4Weight, A, B, r, scale, dX, dA, dB
     _check(lib().qlora_linear_bwd(_ptr(dY), _ptr(X), _ptr(U_saved), M, ctypes.byref(d), _ptr(A), _ptr(B), r,
                                   float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws),
                                   0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qlora_lora_merge_workspace(rows, cols):
+    return lib().qlora_lora_merge_workspace(rows, cols)
+
+
+def qlora_lora_merge_requantize(w: Nf4Weight, A, B, r, scale, out: Nf4Weight, ws, stream=None):
+    """Merge the adapter into the base and quantize the merged weight into `out` (may be `w`)."""
+    dw, do = w.desc, out.desc
+    _check(lib().qlora_lora_merge_requantize(ctypes.byref(dw), _ptr(A), _ptr(B), r, float(scale), ctypes.byref(do),
+                                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qlora_adamw_step(param, param_bf16, grad, m, v, lr, beta1, beta2, eps, weight_decay, step, stream=None):
+    """One AdamW step on fp32 `param` (flat), state `m`, `v` anywhere the device can reach."""
+    _check(lib().qlora_adamw_step(_ptr(param), _ptr(param_bf16), _ptr(grad), _ptr(m), _ptr(v), param.numel(),
+                                  float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step),
+                                  _stream(stream)))
 
 
 def qlora_last_error() -> str:

@@ -161,6 +161,30 @@ qlora_status qlora_nf4_quantize_noalloc(const void *W, qlora_nf4_weight *out, ql
  * the fly to the compute type). */
 qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream);
 
+/* ---- deployment: merge the adapter, quantize again ---------------------- */
+
+/* Workspace bytes of qlora_lora_merge_requantize for a [rows, cols] weight
+ * (the merged bf16 weight plus the quantizer's workspace). */
+size_t qlora_lora_merge_workspace(int64_t rows, int64_t cols);
+
+/* Folds the adapter into the base weight and quantizes the result:
+ *   merged[n, k] = bf16_rne( w'[n, k] + scale * t[n, k] ),
+ *   t[n, k] = sum over j = 0 .. r-1 of B[n, j] * A[j, k],
+ * every step a separately rounded fp32 operation in that order (t starts at
+ * 0; no fused multiply-add), w' the dequantized base weight; then `out` gets
+ * the NF4 + double-quantized form of `merged`, exactly as qlora_nf4_quantize
+ * would produce it. A [r, K] and B [N, r] are bf16 (1 <= r <= 128); `out`
+ * has the same shape as `w` and may be `w` itself (in-place requantization:
+ * the merge reads `w` before the quantizer writes `out`). `ws` is a device
+ * workspace of qlora_lora_merge_workspace bytes; the merged bf16 weight is
+ * its first rows * cols * 2 bytes after the call.
+ * Source: xingyuzhitong.com "Fine-Tuning Memory Requirements", section
+ * "Choosing a method" (adapters merged into the base weights for
+ * deployment). */
+qlora_status qlora_lora_merge_requantize(const qlora_nf4_weight *w, const void *A, const void *B, int r,
+                                         float scale, qlora_nf4_weight *out, void *ws, size_t ws_bytes,
+                                         qlora_stream_t stream);
+
 /* ---- linear layer with LoRA ------------------------------------------- */
 
 /* Workspace bytes for qlora_linear_fwd / qlora_linear_bwd at these sizes. */
@@ -197,6 +221,32 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
                               float scale, void *dX, float *dA, float *dB, void *ws,
                               size_t ws_bytes, qlora_stream_t stream);
 
+/* ---- optimizer step for the adapters ----------------------------------- */
+
+/* One AdamW step on n fp32 parameters (the flattened adapter A or B master
+ * weights), with decoupled weight decay, in this order:
+ *   p = p * (1 - lr * weight_decay)
+ *   m = beta1 * m + (1 - beta1) * g ;  v = beta2 * v + (1 - beta2) * g^2
+ *   p = p - (lr / (1 - beta1^step)) * m / (sqrt(v) / sqrt(1 - beta2^step) + eps)
+ * computed in fp32 (the bias corrections in fp64 on the host). `grad` is the
+ * fp32 gradient qlora_linear_bwd wrote (dA or dB); `param_bf16`, if not NULL,
+ * receives bf16_rne(p), the adapter the next qlora_linear_fwd reads.
+ * "Paged" optimizer state: param, m and v may be device memory, managed
+ * memory (the driver pages it between host and device) or pinned host
+ * memory (read and written over the interconnect); pointers the device
+ * cannot reach (pageable host memory) are rejected with
+ * QLORA_ERR_UNSUPPORTED before anything is launched. step >= 1 counts the
+ * steps taken so far including this one. param, grad, m and v must be
+ * 16-byte aligned, param_bf16 8-byte aligned.
+ * Sources: inquiringlines.com note, mechanism paragraph (paged optimizers);
+ * ashishsrivastav.com, section "Paged Optimizers: Managing Fragmentation";
+ * addaly.com lesson "Fitting a fine-tune in 16 GB" (paged AdamW). The rule
+ * itself is the standard decoupled-decay AdamW the pages name but do not
+ * write out. */
+qlora_status qlora_adamw_step(float *param, uint16_t *param_bf16, const float *grad, float *m, float *v, int64_t n,
+                              float lr, float beta1, float beta2, float eps, float weight_decay, int64_t step,
+                              qlora_stream_t stream);
+
 /* ---- diagnostics ------------------------------------------------------- */
 
 /* Message for the last error on the calling thread ("" if none). */
@@ -232,7 +282,8 @@ enum {
     QLORA_KERNEL_DX_GEMM = 5,    /* fused dequant + tcgen05 dX GEMM */
     QLORA_KERNEL_DX_SIMT = 6,    /* small-M / CUDA-core dX */
     QLORA_KERNEL_GRADS = 7,      /* dA, dB reductions */
-    QLORA_KERNEL_KINDS = 8
+    QLORA_KERNEL_OPTIM = 8,      /* AdamW step of the adapters */
+    QLORA_KERNEL_KINDS = 9
 };
 void qlora_profile_start(void);
 int qlora_profile_stop(double ms_per_kind[QLORA_KERNEL_KINDS], int launches_per_kind[QLORA_KERNEL_KINDS]);

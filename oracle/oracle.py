@@ -74,6 +74,8 @@ def lib():
             L.oracle_linear_fwd.argtypes = [vp, i64, vp, i64, i64, vp, vp, i32, f32, vp, i64, vp, vp]
             L.oracle_linear_bwd.argtypes = [vp, vp, i64, vp, i64, i64, vp, vp, i32, f32,
                                             vp, i64, vp, i64, vp, i64, vp, vp, vp]
+            L.oracle_lora_merge.argtypes = [vp, i64, i64, vp, vp, i32, f32, vp]
+            L.oracle_adamw_step.argtypes = [vp, vp, vp, vp, i64, f64, f64, f64, f64, f64, i64]
             _lib = L
     return _lib
 
@@ -249,3 +251,31 @@ def linear_bwd(dY, X, Wdq, A, B, scale, rows=None, ncols=None, kcols=None):
                             None if ki is None else _p(ki), nk,
                             _p(dX), _p(dA), _p(dB))
     return dX, dA, dB
+
+
+# ---------------------------------------------------------------- merge ----
+
+def lora_merge(Wdq, A, B, scale):
+    """bf16 merged weight W' + s * B A (fixed fp32 order, see the C source)."""
+    Wdq, A, B = _u16(Wdq), _u16(A), _u16(B)
+    N, K = Wdq.shape
+    r = A.shape[0]
+    assert A.shape == (r, K) and B.shape == (N, r)
+    out = np.zeros((N, K), np.uint16)
+    lib().oracle_lora_merge(_p(Wdq), N, K, _p(A), _p(B), r, ctypes.c_float(scale), _p(out))
+    return out
+
+
+def merge_requantize(qw: dict, A, B, scale):
+    """The quantized weight of the merged layer: quantize(merge(dequant(qw)))."""
+    return nf4_quantize(lora_merge(nf4_dequantize(qw), A, B, scale))
+
+
+# ---------------------------------------------------------------- adamw ----
+
+def adamw_step(p, g, m, v, lr, beta1, beta2, eps, weight_decay, step):
+    """One AdamW step in fp64, in place on p, m, v (float64 arrays)."""
+    for a in (p, m, v):
+        assert a.dtype == np.float64 and a.flags.c_contiguous
+    g = np.ascontiguousarray(g, np.float64)
+    lib().oracle_adamw_step(_p(p), _p(g), _p(m), _p(v), p.size, lr, beta1, beta2, eps, weight_decay, step)

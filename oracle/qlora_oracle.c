@@ -412,3 +412,53 @@ void oracle_linear_bwd(const uint16_t *dY, const uint16_t *X, int64_t M, const u
     free(U);
     free(V);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Merge the adapter into the base and quantize again [QL-mem "Choosing a   */
+/* method": for deployment the adapters are merged into the base weights].  */
+/* ------------------------------------------------------------------------ */
+
+/* merged[n,k] = bf16_rne( w'[n,k] + s * t[n,k] ),  t[n,k] = sum_j B[n,j] A[j,k]
+ * with every operation a separately rounded fp32 operation: t starts at 0
+ * and adds the products for j = 0 .. r-1 in that order (a product of two
+ * bf16 numbers is exact in fp32), then s * t, then the add to w'. The
+ * merged weight is then quantized with oracle_nf4_quantize like any other
+ * bf16 weight. */
+void oracle_lora_merge(const uint16_t *Wdq, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B, int r,
+                       float s, uint16_t *merged) {
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            float t = 0.0f;
+            for (int j = 0; j < r; ++j) {
+                float prod = bf16_to_f32(B[n * r + j]) * bf16_to_f32(A[(int64_t)j * K + k]);
+                t = t + prod;
+            }
+            float st = s * t;
+            float m = bf16_to_f32(Wdq[n * K + k]) + st;
+            merged[n * K + k] = f32_to_bf16_rne(m);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* AdamW step for the adapters [QL-note: paged optimizers; QL-70B "Paged    */
+/* Optimizers": optimizer state that can live in host memory; the addaly    */
+/* lesson's paged_adamw]. The update rule is not on the pages; the reading  */
+/* is AdamW with decoupled weight decay (Loshchilov & Hutter), in the order */
+/* torch.optim.AdamW applies it, in fp64:                                   */
+/*   p = p * (1 - lr * wd)                                                  */
+/*   m = b1 m + (1 - b1) g ;  v = b2 v + (1 - b2) g^2                       */
+/*   p = p - (lr / (1 - b1^t)) * m / (sqrt(v) / sqrt(1 - b2^t) + eps)       */
+/* ------------------------------------------------------------------------ */
+void oracle_adamw_step(double *p, const double *g, double *m, double *v, int64_t n, double lr, double b1,
+                       double b2, double eps, double wd, int64_t t) {
+    double bias1 = 1.0 - pow(b1, (double)t), bias2 = 1.0 - pow(b2, (double)t);
+    double step_size = lr / bias1, bias2_sqrt = sqrt(bias2);
+    for (int64_t i = 0; i < n; ++i) {
+        p[i] = p[i] * (1.0 - lr * wd);
+        m[i] = b1 * m[i] + (1.0 - b1) * g[i];
+        v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];
+        double denom = sqrt(v[i]) / bias2_sqrt + eps;
+        p[i] = p[i] - step_size * m[i] / denom;
+    }
+}
