@@ -48,12 +48,14 @@ __device__ __forceinline__ uint32_t nf4_code(float x, const float *thr) {
     return c;
 }
 
+// tab: level table (kTableNF4 / kTableINT4); group_sum may be null (no
+// double quantization follows: the absmax values are the stored constants).
 __global__ void __launch_bounds__(256) k_nf4_encode(const uint4 *__restrict__ W, int64_t nb,
                                                     uint32_t *__restrict__ codes, float *__restrict__ absmax,
-                                                    double *__restrict__ group_sum) {
+                                                    double *__restrict__ group_sum, int tab) {
     __shared__ float s_thr[16];
     __shared__ float s_abs[kGroup];
-    if (threadIdx.x < 15) s_thr[threadIdx.x] = c_thresholds[threadIdx.x];
+    if (threadIdx.x < 15) s_thr[threadIdx.x] = c_thresholds_q4[tab][threadIdx.x];
     __syncthreads();
     const int64_t g = blockIdx.x;
     const int sub = threadIdx.x & 7;   // which 8-element slice of the block
@@ -95,6 +97,7 @@ __global__ void __launch_bounds__(256) k_nf4_encode(const uint4 *__restrict__ W,
             codes[b * 8 + sub] = word;
         }
     }
+    if (!group_sum) return;
     __syncthreads();
     if (threadIdx.x < 32) {
         double v[8];
@@ -173,18 +176,21 @@ constexpr int kDeqSmem = kDeqWarps * 2 * 32 * 128 + 1024;  // two 4 KB staging t
 // staging tile (conflict-free 16-byte stores) and one TMA store of the box
 // (64 bf16, 32 rows) of the output viewed as [blocks, 64] writes them.
 // The next chunk's loads are issued before the current chunk is decoded.
+// absmax_f32 (may be null): per-block fp32 absmax used in place of the
+// double-quantized q, scale, mean; tab: level table.
 __global__ void __launch_bounds__(kDeqWarps * 32) k_nf4_dequant(const __grid_constant__ CUtensorMap tm_out,
                                                                const uint4 *__restrict__ codes,
                                                                const int8_t *__restrict__ q,
                                                                const float *__restrict__ scale,
-                                                               const float *__restrict__ mean_p, int64_t nb) {
+                                                               const float *__restrict__ mean_p, int64_t nb,
+                                                               const float *__restrict__ absmax_f32, int tab) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *stage = smem + warp * 2 * 4096;
     const int64_t nchunks = (nb + 31) / 32;
     const int64_t nw = (int64_t)gridDim.x * kDeqWarps;
-    const float mean = *mean_p;
+    const float mean = absmax_f32 ? 0.0f : *mean_p;
     int64_t c = (int64_t)blockIdx.x * kDeqWarps + warp;
     uint4 cw0 = make_uint4(0, 0, 0, 0), cw1 = cw0;
     int qv = 0;
@@ -194,15 +200,19 @@ __global__ void __launch_bounds__(kDeqWarps * 32) k_nf4_dequant(const __grid_con
         if (ch < nchunks && b < nb) {
             cw0 = __ldg(codes + 2 * b);
             cw1 = __ldg(codes + 2 * b + 1);
-            qv = __ldg(q + b);
-            sv = __ldg(scale + (b >> 8));
+            if (absmax_f32) {
+                sv = __ldg(absmax_f32 + b);
+            } else {
+                qv = __ldg(q + b);
+                sv = __ldg(scale + (b >> 8));
+            }
         }
     };
     load(c);
     uint32_t it = 0;
     for (; c < nchunks; c += nw, ++it) {
         const uint32_t w[8] = {cw0.x, cw0.y, cw0.z, cw0.w, cw1.x, cw1.y, cw1.z, cw1.w};
-        const Nf4Table tab = make_table(dq_absmax((int8_t)qv, sv, mean));
+        const Nf4Table tbl = make_table(absmax_f32 ? sv : dq_absmax((int8_t)qv, sv, mean), tab);
         load(c + nw);
         uint8_t *buf = stage + (it & 1) * 4096;
         if (lane == 0) bulk_wait_read<1>();  // the store that last read this tile is done with it
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(kDeqWarps * 32) k_nf4_dequant(const __grid_con
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             uint32_t o[4];
-            decode8(tab, w[j], o);
+            decode8(tbl, w[j], o);
             *reinterpret_cast<uint4 *>(row + ((j ^ (lane & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();

@@ -18,8 +18,11 @@ namespace qlora {
 constexpr int kBlock = 64;    // weights per NF4 block (one absmax each)
 constexpr int kGroup = 256;   // blocks per second-level (fp32 scale) group
 
-__constant__ float c_levels[16] = QLORA_NF4_LEVELS;
-__constant__ float c_thresholds[15] = QLORA_NF4_THRESHOLDS;
+// Level tables: [0] NF4, [1] the INT4 baseline; the encode thresholds with
+// them. Kernels take the table id as a launch-uniform argument.
+enum { kTableNF4 = 0, kTableINT4 = 1 };
+__constant__ float c_levels_q4[2][16] = {QLORA_NF4_LEVELS, QLORA_INT4_LEVELS};
+__constant__ float c_thresholds_q4[2][15] = {QLORA_NF4_THRESHOLDS, QLORA_INT4_THRESHOLDS};
 
 // ---------------------------------------------------------------------------
 // Device error word: the first bounded wait that runs out records
@@ -240,11 +243,12 @@ __device__ __forceinline__ float dq_absmax(int8_t q, float s2, float mean) {
     return __fadd_rn(__fmul_rn(static_cast<float>(q), s2), mean);
 }
 
-__device__ __forceinline__ Nf4Table make_table(float a) {
+__device__ __forceinline__ Nf4Table make_table(float a, int tab = kTableNF4) {
+    const float *L = c_levels_q4[tab];
     uint32_t p[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(__fmul_rn(c_levels[2 * j], a), __fmul_rn(c_levels[2 * j + 1], a));
+        __nv_bfloat162 v = __floats2bfloat162_rn(__fmul_rn(L[2 * j], a), __fmul_rn(L[2 * j + 1], a));
         p[j] = *reinterpret_cast<uint32_t *>(&v);  // entry 2j in the low half
     }
     Nf4Table t;

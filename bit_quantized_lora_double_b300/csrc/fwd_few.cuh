@@ -151,10 +151,12 @@ __device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], const uint32_t (
 }
 
 // NT = number of 8-token tiles (M <= 8 * NT <= 16).
-template <int NT>
+// F32A: the block absmax is stored as fp32 (`absmax`, one per block) instead
+// of double-quantized; tab selects the level table (kTableNF4 / kTableINT4).
+template <int NT, bool F32A>
 __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     k_fwd_few(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_q,
-              const FewParams p) {
+              const FewParams p, const float *__restrict__ absmax, int tab) {
     using C = FewCfg;
     // the byte table: word (e * 32 + l) = bf16 pair (L[e >> 4] low, L[e & 15]
     // high); static, so its base is an immediate of every lookup
@@ -212,12 +214,13 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     auto issue = [&](int i, int s, int64_t rg, int64_t kc) {
         const int wa = i == 0 ? wfirst : 0, wb = i == nst - 1 ? wlast : C::WARPS;
         const int ba = wa >> 2, bb = (wb + 3) >> 2;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)((bb - ba) * C::BOX_BYTES + C::Q_BYTES));
+        const uint32_t qbytes = F32A ? 0u : (uint32_t)C::Q_BYTES;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)((bb - ba) * C::BOX_BYTES) + qbytes);
         __syncwarp();
         if (lane >= ba && lane < bb)
             tma_load_2d(ring + s * C::STAGE_BYTES + lane * C::BOX_BYTES, &tm_codes, &full[s],
                         (int32_t)(kc * 512 + 128 * lane), (int32_t)(rg * C::ROWS));
-        if (lane == 4)
+        if (lane == 4 && !F32A)
             tma_load_2d(qring + s * C::Q_BYTES, &tm_q, &full[s], (int32_t)(kc * 16), (int32_t)(rg * C::ROWS));
     };
     int64_t prg = (uint32_t)st0 / (uint32_t)spg, pkc = st0 - prg * spg;  // the producer's next stage
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     }
     for (int i = threadIdx.x; i < C::TABLE_WORDS; i += C::THREADS) {
         const int e = i >> 5;
-        s_table[i] = pack_bf16x2(c_levels[e >> 4], c_levels[e & 15]);
+        s_table[i] = pack_bf16x2(c_levels_q4[tab][e >> 4], c_levels_q4[tab][e & 15]);
     }
     __syncthreads();
 
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
         const int g = lane >> 2, t = lane & 3;
         const uint32_t lane4 = 4u * lane;
         const char *tab = reinterpret_cast<const char *>(s_table);
-        const float mean = *p.mean;
+        const float mean = F32A ? 0.0f : *p.mean;
         // this thread's 8 code bytes of rows g + 8 q of its block: block
         // column warp & 3 of box warp >> 2 (128-byte rows, 128-byte swizzle:
         // 16-byte chunk h of row r sits at h ^ (r & 7))
@@ -337,10 +340,16 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
                 sbase[i] = n < p.N ? (uint32_t)(n * kblocks) : 0u;
             }
         };
+        // (with fp32 absmax: the absmax of this warp's block of rows g + 8 i)
         auto load_s2 = [&](int64_t kc, float (&sv)[4]) {
             const uint32_t k16 = (uint32_t)kc * 16u;
+            if (F32A) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sv[i] = __ldg(p.s2 + ((sbase[i] + k16) >> 8));
+                for (int i = 0; i < 4; ++i) sv[i] = __ldg(absmax + sbase[i] + k16 + (uint32_t)warp);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sv[i] = __ldg(p.s2 + ((sbase[i] + k16) >> 8));
+            }
         };
         float acc[2][NT][4];
         auto zero_acc = [&]() {
@@ -436,7 +445,7 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
                     // block scale a' of rows g + 8 q
                     float ap[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) ap[q] = dq_absmax(qt[(g + 8 * q) * 16 + warp], sv[q], mean);
+                    for (int q = 0; q < 4; ++q) ap[q] = F32A ? sv[q] : dq_absmax(qt[(g + 8 * q) * 16 + warp], sv[q], mean);
 #pragma unroll
                     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll

@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         const int dw = warp - 2;
         const int grp = dw / C::GROUP_WARPS;
         const int dt = (dw % C::GROUP_WARPS) * 32 + lane;  // 0..127 within the group
-        const float mean = *p.mean;
+        const float mean = p.absmax ? 0.0f : *p.mean;
         const int64_t kblocks = p.w_cols / kBlock;
         const uint32_t ready_addr0 = mapa_u32(smem_u32(ready), 0);
         uint32_t dst[8], csrc[2];
@@ -553,8 +553,12 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             const int64_t kb = MODE == kFwd ? c.kbeg + c.it : ch / kBlock + b2;
             if (wrow >= p.w_rows || kb >= kblocks) return false;
             const int64_t bidx = wrow * kblocks + kb;
-            qv = __ldg(p.q + bidx);
-            sv = __ldg(p.s2 + (bidx >> 8));
+            if (p.absmax) {
+                sv = __ldg(p.absmax + bidx);
+            } else {
+                qv = __ldg(p.q + bidx);
+                sv = __ldg(p.s2 + (bidx >> 8));
+            }
             return true;
         };
         Cursor cur;
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 const uint8_t *ct = ctile(s);
                 uint32_t o[8][4];
                 if (valid) {
-                    const Nf4Table tab = make_table(dq_absmax((int8_t)qv, sv, mean));
+                    const Nf4Table tab = make_table(p.absmax ? sv : dq_absmax((int8_t)qv, sv, mean), p.tab);
                     uint4 cw[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) cw[h] = *reinterpret_cast<const uint4 *>(ct + csrc[h]);

@@ -37,6 +37,8 @@ struct TcParams {
     const int8_t *q;
     const float *s2;
     const float *mean;
+    const float *absmax;   // per-block fp32 absmax in place of q, s2, mean (null: double-quantized)
+    int tab;               // level table (kTableNF4 / kTableINT4)
     uint16_t *out;
     int64_t ldo;
     // Stream-K hand-off between pairs (zeroed flags before the launch):

@@ -164,11 +164,13 @@ constexpr int kSt = 64;
 
 // Decodes the 64 codes of block b (row n, columns k0..k0+63 of W') as fp32.
 // Thread `half` (0/1) decodes codes 32*half .. 32*half+31.
+// (absmax may be null: double-quantized q, s2, mean; tab: level table)
 __device__ __forceinline__ void decode_half_block(const uint8_t *__restrict__ codes, const int8_t *__restrict__ q,
-                                                  const float *__restrict__ s2, float mean, int64_t b, int half,
+                                                  const float *__restrict__ s2, float mean,
+                                                  const float *__restrict__ absmax, int tabid, int64_t b, int half,
                                                   float (&f)[32]) {
-    const float a = dq_absmax(q[b], s2[b / kGroup], mean);
-    const Nf4Table tab = make_table(a);
+    const float a = absmax ? absmax[b] : dq_absmax(q[b], s2[b / kGroup], mean);
+    const Nf4Table tab = make_table(a, tabid);
     const uint4 cw = reinterpret_cast<const uint4 *>(codes + b * 32)[half];
     const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
@@ -188,12 +190,13 @@ __global__ void __launch_bounds__(256) k_dx_simt(const uint16_t *__restrict__ dY
                                                  const uint8_t *__restrict__ codes, const int8_t *__restrict__ q,
                                                  const float *__restrict__ s2, const float *__restrict__ mean_p,
                                                  int64_t K, const uint16_t *__restrict__ sV, int ldv,
-                                                 const uint16_t *__restrict__ A, int r, uint16_t *__restrict__ dX) {
+                                                 const uint16_t *__restrict__ A, int r, uint16_t *__restrict__ dX,
+                                                 const float *__restrict__ absmax, int tab) {
     __shared__ float Ds[kSt][kSt + 1];  // [m][n]
     __shared__ float Ws[kSt][kSt + 1];  // [n][k]
     const int tid = threadIdx.x, tm = tid & 15, tk = tid >> 4;
     const int64_t m0 = (int64_t)blockIdx.y * kSt, k0 = (int64_t)blockIdx.x * kSt;
-    const float mean = *mean_p;
+    const float mean = absmax ? 0.0f : *mean_p;
     float acc[4][4] = {};
     for (int64_t n0 = 0; n0 < N; n0 += kSt) {
         for (int i = tid; i < kSt * kSt; i += 256) {
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(256) k_dx_simt(const uint16_t *__restrict__ dY
             const int64_t n = n0 + row;
             float f[32];
             if (n < N) {
-                decode_half_block(codes, q, s2, mean, (n * K + k0) / kBlock, half, f);
+                decode_half_block(codes, q, s2, mean, absmax, tab, (n * K + k0) / kBlock, half, f);
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) f[e] = 0.0f;

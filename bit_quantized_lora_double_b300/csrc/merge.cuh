@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) k_lora_merge(const uint32_t *__restrict__
     for (int e = 0; e < 8; ++e) {
         const uint32_t byte = (cw >> (8 * (e >> 1))) & 0xFFu;
         const uint32_t code = (e & 1) ? (byte & 15u) : (byte >> 4);
-        w[e] = bf16lo_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(c_levels[code], a))));
+        w[e] = bf16lo_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(c_levels_q4[kTableNF4][code], a))));
         t[e] = 0.0f;
     }
     for (int j = 0; j < r; ++j) {

@@ -113,17 +113,49 @@ bool valid_dims(int64_t rows, int64_t cols) {
     return rows >= 0 && cols > 0 && cols % kBlock == 0 && rows < kMaxDim && cols < kMaxDim;
 }
 
-qlora_status check_weight(const qlora_nf4_weight *w, bool need_rows) {
-    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
-    if (!valid_dims(w->rows, w->cols))
+// Internal view of a quantized weight, from either descriptor of the ABI:
+// the level table, and the block absmax either double-quantized (q, s2, mean)
+// or as fp32 (absmax; then q, s2, mean are null).
+struct Wt {
+    int64_t rows, cols;
+    int tab;
+    uint8_t *codes;
+    int8_t *q;
+    float *s2, *mean;
+    float *absmax;
+    bool valid_format;
+};
+Wt wt_of(const qlora_nf4_weight *w) {
+    return Wt{w->rows, w->cols, kTableNF4, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, nullptr, true};
+}
+Wt wt_of(const qlora_q4_weight *w) {
+    Wt t{w->rows, w->cols, w->table, w->codes, nullptr, nullptr, nullptr, nullptr, true};
+    if (w->double_quant) {
+        t.q = w->absmax_q;
+        t.s2 = w->absmax_scale;
+        t.mean = w->absmax_mean;
+    } else {
+        t.absmax = w->absmax;
+    }
+    t.valid_format = (w->table == kTableNF4 || w->table == kTableINT4) && (w->double_quant == 0 || w->double_quant == 1);
+    return t;
+}
+
+qlora_status check_weight(const Wt &w, bool need_rows) {
+    if (!w.valid_format) return fail(QLORA_ERR_UNSUPPORTED, "unknown table or double_quant value");
+    if (!valid_dims(w.rows, w.cols))
         return fail(QLORA_ERR_SHAPE, "weight shape [%lld, %lld]: need rows >= 0, cols > 0, cols %% 64 == 0",
-                    (long long)w->rows, (long long)w->cols);
-    if (need_rows && w->rows == 0) return fail(QLORA_ERR_SHAPE, "weight has 0 rows");
-    if (!w->codes || !w->absmax_q || !w->absmax_scale || !w->absmax_mean)
+                    (long long)w.rows, (long long)w.cols);
+    if (need_rows && w.rows == 0) return fail(QLORA_ERR_SHAPE, "weight has 0 rows");
+    if (!w.codes || (w.absmax ? false : (!w.q || !w.s2 || !w.mean)) || (!w.q && !w.absmax))
         return fail(QLORA_ERR_NULL, "weight descriptor has a NULL array");
-    if (!al16(w->codes) || !al16(w->absmax_q) || !al16(w->absmax_scale) || !al16(w->absmax_mean))
+    if (!al16(w.codes) || (w.absmax && !al16(w.absmax)) || (w.q && (!al16(w.q) || !al16(w.s2) || !al16(w.mean))))
         return fail(QLORA_ERR_ALIGN, "weight arrays must be 16-byte aligned");
     return QLORA_OK;
+}
+qlora_status check_weight(const qlora_nf4_weight *w, bool need_rows) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return check_weight(wt_of(w), need_rows);
 }
 
 // Workspace carving helper: 256-byte aligned slices.
@@ -160,14 +192,22 @@ size_t quantize_ws(int64_t rows, int64_t cols, float **absmax, double **gsum, do
 // workspace or the built-in array): encode with the exact absmax and the
 // group sums of the pairwise tree, the tree's upper levels 256 values at a
 // time down to the mean, then the int8 codes and group scales.
-qlora_status quantize_launch(const void *W, qlora_nf4_weight *out, float *absmax, double *gsum, double *b0,
+qlora_status quantize_launch(const void *W, const Wt &out, float *absmax, double *gsum, double *b0,
                              double *b1, cudaStream_t s) {
-    const int64_t nb = out->rows * out->cols / kBlock, ng = cdiv(nb, kGroup);
+    const int64_t nb = out.rows * out.cols / kBlock, ng = cdiv(nb, kGroup);
     qlora_status st;
+    if (out.absmax) {
+        // no double quantization: the exact block absmax is the stored constant
+        ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
+        k_nf4_encode<<<(unsigned)ng, 256, 0, s>>>(static_cast<const uint4 *>(W), nb,
+                                                 reinterpret_cast<uint32_t *>(out.codes), out.absmax, nullptr,
+                                                 out.tab);
+        return launch_check("k_nf4_encode");
+    }
     {
         ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
         k_nf4_encode<<<(unsigned)ng, 256, 0, s>>>(static_cast<const uint4 *>(W), nb,
-                                                 reinterpret_cast<uint32_t *>(out->codes), absmax, gsum);
+                                                 reinterpret_cast<uint32_t *>(out.codes), absmax, gsum, out.tab);
     }
     if ((st = launch_check("k_nf4_encode"))) return st;
     const double *cur = gsum;
@@ -187,13 +227,12 @@ qlora_status quantize_launch(const void *W, qlora_nf4_weight *out, float *absmax
     }
     {
         ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
-        k_pairwise_reduce<<<1, 256, 0, s>>>(cur, n, nullptr, out->absmax_mean, nb);
+        k_pairwise_reduce<<<1, 256, 0, s>>>(cur, n, nullptr, out.mean, nb);
     }
     if ((st = launch_check("k_pairwise_reduce(mean)"))) return st;
     {
         ProfScope ps(QLORA_KERNEL_QUANTIZE, s);
-        k_dq_encode<<<(unsigned)cdiv(ng, 8), 256, 0, s>>>(absmax, nb, out->absmax_mean, out->absmax_q,
-                                                          out->absmax_scale);
+        k_dq_encode<<<(unsigned)cdiv(ng, 8), 256, 0, s>>>(absmax, nb, out.mean, out.q, out.s2);
     }
     if ((st = launch_check("k_dq_encode"))) return st;
     return ok();
@@ -704,14 +743,18 @@ size_t qlora_nf4_quantize_workspace(int64_t rows, int64_t cols) {
     return quantize_ws(rows, cols, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
-qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, size_t ws_bytes,
-                                qlora_stream_t stream) {
+static qlora_status quantize_impl(const void *W, const Wt &out, void *ws, size_t ws_bytes, qlora_stream_t stream) {
     qlora_status st = check_weight(out, false);
     if (st) return st;
     if (!W) return fail(QLORA_ERR_NULL, "W is NULL");
     if (!al16(W)) return fail(QLORA_ERR_ALIGN, "W must be 16-byte aligned");
-    const int64_t rows = out->rows, cols = out->cols;
+    const int64_t rows = out.rows, cols = out.cols;
     if (rows == 0) return ok();
+    if (out.absmax) {
+        if ((st = quantize_launch(W, out, nullptr, nullptr, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream))))
+            return st;
+        return ok();
+    }
     if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
     if (!al16(ws)) return fail(QLORA_ERR_ALIGN, "workspace must be 16-byte aligned");
     float *absmax;
@@ -720,6 +763,17 @@ qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, 
     if (ws_bytes < need)
         return fail(QLORA_ERR_WORKSPACE, "quantize workspace %zu < %zu bytes", ws_bytes, need);
     return quantize_launch(W, out, absmax, gsum, b0, b1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlora_status qlora_nf4_quantize(const void *W, qlora_nf4_weight *out, void *ws, size_t ws_bytes,
+                                qlora_stream_t stream) {
+    if (!out) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return quantize_impl(W, wt_of(out), ws, ws_bytes, stream);
+}
+
+qlora_status qlora_q4_quantize(const void *W, qlora_q4_weight *out, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    if (!out) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return quantize_impl(W, wt_of(out), ws, ws_bytes, stream);
 }
 
 // ---- quantize without a caller workspace ------------------------------------
@@ -789,7 +843,7 @@ qlora_status qlora_nf4_quantize_noalloc(const void *W, qlora_nf4_weight *out, ql
     float *absmax;
     double *gsum, *b0, *b1;
     quantize_ws(rows, cols, &absmax, &gsum, &b0, &b1, scratch);
-    return quantize_launch(W, out, absmax, gsum, b0, b1, reinterpret_cast<cudaStream_t>(stream));
+    return quantize_launch(W, wt_of(out), absmax, gsum, b0, b1, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t qlora_lora_merge_workspace(int64_t rows, int64_t cols) {
@@ -828,7 +882,7 @@ qlora_status qlora_lora_merge_requantize(const qlora_nf4_weight *w, const void *
     float *absmax;
     double *gsum, *b0, *b1;
     quantize_ws(N, K, &absmax, &gsum, &b0, &b1, static_cast<char *>(ws) + up((size_t)(N * K) * 2, 256));
-    return quantize_launch(merged, out, absmax, gsum, b0, b1, s);
+    return quantize_launch(merged, wt_of(out), absmax, gsum, b0, b1, s);
 }
 
 // A pointer the device can dereference: device or managed memory, or host
@@ -879,14 +933,14 @@ qlora_status qlora_adamw_step(float *param, uint16_t *param_bf16, const float *g
     return ok();
 }
 
-qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream) {
+static qlora_status dequantize_impl(const Wt &w, void *out, qlora_stream_t stream) {
     qlora_status st = check_weight(w, false);
     if (st) return st;
     if (!out) return fail(QLORA_ERR_NULL, "output is NULL");
     if (!al16(out)) return fail(QLORA_ERR_ALIGN, "output must be 16-byte aligned");
-    if (w->rows == 0) return ok();
+    if (w.rows == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t nb = w->rows * w->cols / kBlock;
+    const int64_t nb = w.rows * w.cols / kBlock;
     const cudaError_t aerr = smem_attr(k_nf4_dequant, kDeqSmem);
     if (aerr != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
     // the output viewed as [blocks, 64] bf16 rows of 128 bytes
@@ -898,11 +952,21 @@ qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_st
     const unsigned grid = (unsigned)std::min<int64_t>(cdiv(nchunks, kDeqWarps), 148 * 3);
     {
         ProfScope ps(QLORA_KERNEL_DEQUANT, s);
-        k_nf4_dequant<<<grid, kDeqWarps * 32, kDeqSmem, s>>>(tmO, reinterpret_cast<const uint4 *>(w->codes),
-                                                             w->absmax_q, w->absmax_scale, w->absmax_mean, nb);
+        k_nf4_dequant<<<grid, kDeqWarps * 32, kDeqSmem, s>>>(tmO, reinterpret_cast<const uint4 *>(w.codes), w.q,
+                                                             w.s2, w.mean, nb, w.absmax, w.tab);
     }
     if ((st = launch_check("k_nf4_dequant"))) return st;
     return ok();
+}
+
+qlora_status qlora_nf4_dequantize(const qlora_nf4_weight *w, void *out, qlora_stream_t stream) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return dequantize_impl(wt_of(w), out, stream);
+}
+
+qlora_status qlora_q4_dequantize(const qlora_q4_weight *w, void *out, qlora_stream_t stream) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return dequantize_impl(wt_of(w), out, stream);
 }
 
 size_t qlora_linear_fwd_workspace(int64_t M, const qlora_nf4_weight *w, int r) {
@@ -915,8 +979,17 @@ size_t qlora_linear_bwd_workspace(int64_t M, const qlora_nf4_weight *w, int r) {
     return bwd_ws(M, w->rows, w->cols, r, nullptr, nullptr);
 }
 
-static qlora_status check_linear_common(int64_t M, const qlora_nf4_weight *w, const void *A, const void *B, int r,
-                                        void *ws) {
+size_t qlora_q4_linear_fwd_workspace(int64_t M, const qlora_q4_weight *w, int r) {
+    if (!w || !valid_dims(w->rows, w->cols) || M < 0 || r < 1 || r > 128) return 0;
+    return fwd_ws(M, w->rows, w->cols, r, nullptr, nullptr);
+}
+
+size_t qlora_q4_linear_bwd_workspace(int64_t M, const qlora_q4_weight *w, int r) {
+    if (!w || !valid_dims(w->rows, w->cols) || M < 0 || r < 1 || r > 128) return 0;
+    return bwd_ws(M, w->rows, w->cols, r, nullptr, nullptr);
+}
+
+static qlora_status check_linear_common(int64_t M, const Wt &w, const void *A, const void *B, int r, void *ws) {
     qlora_status st = check_weight(w, true);
     if (st) return st;
     if (M < 0 || M >= kMaxDim) return fail(QLORA_ERR_SHAPE, "M = %lld out of range", (long long)M);
@@ -927,16 +1000,16 @@ static qlora_status check_linear_common(int64_t M, const qlora_nf4_weight *w, co
     return QLORA_OK;
 }
 
-qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *w, const void *A, const void *B,
-                              int r, float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
-                              qlora_stream_t stream) {
+static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const void *A, const void *B, int r,
+                                    float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
+                                    qlora_stream_t stream) {
     qlora_status st = check_linear_common(M, w, A, B, r, ws);
     if (st) return st;
     if (M > 0 && (!X || !Y)) return fail(QLORA_ERR_NULL, "X or Y is NULL");
     if ((X && !al16(X)) || (Y && !al16(Y)) || (U_save && !al16(U_save)))
         return fail(QLORA_ERR_ALIGN, "X, Y and U_save must be 16-byte aligned");
     if (M == 0) return ok();
-    const int64_t N = w->rows, K = w->cols;
+    const int64_t N = w.rows, K = w.cols;
     FwdWs f;
     const size_t need = fwd_ws(M, N, K, r, ws, &f);
     if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
@@ -949,11 +1022,11 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     if (few_path(M, N, K)) {
         // few tokens, K a multiple of 1024: persistent HBM-bound kernel
         if ((st = tc_device_ok())) return st;
-        const cudaError_t aerr = smem_attr(k_fwd_few<1>, FewCfg::SMEM_BYTES);
-        const cudaError_t aerr2 = smem_attr(k_fwd_few<2>, FewCfg::SMEM_BYTES);
-        if (aerr != cudaSuccess || aerr2 != cudaSuccess)
-            return fail(QLORA_ERR_CUDA, "setting shared memory size: %s",
-                        cudaGetErrorString(aerr != cudaSuccess ? aerr : aerr2));
+        auto kern = M <= 8 ? (w.absmax ? k_fwd_few<1, true> : k_fwd_few<1, false>)
+                           : (w.absmax ? k_fwd_few<2, true> : k_fwd_few<2, false>);
+        const cudaError_t aerr = smem_attr(kern, FewCfg::SMEM_BYTES);
+        if (aerr != cudaSuccess)
+            return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
         const FewPlan fp = few_plan(N, K, r);
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
@@ -966,18 +1039,23 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         // code boxes of 128 bytes x 32 rows (FewCfg::BOX_BYTES, what the kernel
         // expects per box), 128-byte swizzle
         static_assert(FewCfg::BOX_BYTES == 128 * FewCfg::ROWS, "code box");
-        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, FewCfg::ROWS,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "codes")) ||
-            (st = make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->absmax_q, K / kBlock, N, K / kBlock, 16,
-                           FewCfg::ROWS, CU_TENSOR_MAP_SWIZZLE_NONE, "absmax codes")))
+        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 128, FewCfg::ROWS,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "codes")))
+            return st;
+        // fp32 absmax: the kernel issues no absmax-code boxes and the second
+        // map is never used
+        if (w.absmax)
+            tmQ = tmC;
+        else if ((st = make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.q, K / kBlock, N, K / kBlock, 16,
+                                FewCfg::ROWS, CU_TENSOR_MAP_SWIZZLE_NONE, "absmax codes")))
             return st;
         FewParams prm{};
         prm.X = X16;
         prm.M = M;
         prm.N = N;
         prm.K = K;
-        prm.s2 = w->absmax_scale;
-        prm.mean = w->absmax_mean;
+        prm.s2 = w.s2;
+        prm.mean = w.mean;
         prm.sU = f.sU;
         prm.ldu = rp;
         prm.B = static_cast<const uint16_t *>(B);
@@ -1001,8 +1079,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         cudaError_t e;
         {
             ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
-            e = M <= 8 ? cudaLaunchKernelEx(&cfg, k_fwd_few<1>, tmC, tmQ, prm)
-                       : cudaLaunchKernelEx(&cfg, k_fwd_few<2>, tmC, tmQ, prm);
+            e = cudaLaunchKernelEx(&cfg, kern, tmC, tmQ, prm, (const float *)w.absmax, w.tab);
         }
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -1022,7 +1099,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
         }
         if ((st = launch_check("k_lora_down"))) return st;
         CUtensorMap tmC;
-        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 128, SmallCfg::ROWS,
+        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 128, SmallCfg::ROWS,
                            CU_TENSOR_MAP_SWIZZLE_128B, "codes")))
             return st;
         const unsigned grid = (unsigned)cdiv(N, SmallCfg::ROWS);
@@ -1042,10 +1119,10 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmC, (const uint16_t *)X16, M, K,
-                                                     (const int8_t *)w->absmax_q, (const float *)w->absmax_scale,
-                                                     (const float *)w->absmax_mean, N, (const uint16_t *)f.sU, rp,
-                                                     static_cast<const uint16_t *>(B), r, static_cast<uint16_t *>(Y),
-                                                     wait_ns());
+                                                     (const int8_t *)w.q, (const float *)w.s2, (const float *)w.mean,
+                                                     N, (const uint16_t *)f.sU, rp, static_cast<const uint16_t *>(B),
+                                                     r, static_cast<uint16_t *>(Y), wait_ns(),
+                                                     (const float *)w.absmax, w.tab);
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 return fail(QLORA_ERR_CUDA, "k_fwd_small: launch failed: %s", cudaGetErrorString(e));
@@ -1073,7 +1150,7 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
                        CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
         (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, r, K * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
-        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 32, 128,
+        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 32, 128,
                        CU_TENSOR_MAP_SWIZZLE_32B, "codes")) ||
         (st = make_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rs, M, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "sU")) ||
@@ -1093,9 +1170,11 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     prm.nk_main = K / kGemmBK;
     prm.lora_steps = rp / 64;
     prm.r = r;
-    prm.q = w->absmax_q;
-    prm.s2 = w->absmax_scale;
-    prm.mean = w->absmax_mean;
+    prm.q = w.q;
+    prm.s2 = w.s2;
+    prm.mean = w.mean;
+    prm.absmax = w.absmax;
+    prm.tab = w.tab;
     prm.out = static_cast<uint16_t *>(Y);
     prm.ldo = N;
     prm.out_v4 = (reinterpret_cast<uintptr_t>(Y) & 15) == 0 && (N & 7) == 0;
@@ -1107,9 +1186,9 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
     return ok();
 }
 
-qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
-                              const qlora_nf4_weight *w, const void *A, const void *B, int r, float scale, void *dX,
-                              float *dA, float *dB, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+static qlora_status linear_bwd_impl(const void *dY, const void *X, const void *U_saved, int64_t M, const Wt &w,
+                                    const void *A, const void *B, int r, float scale, void *dX, float *dA, float *dB,
+                                    void *ws, size_t ws_bytes, qlora_stream_t stream) {
     qlora_status st = check_linear_common(M, w, A, B, r, ws);
     if (st) return st;
     if (!dA || !dB) return fail(QLORA_ERR_NULL, "dA or dB is NULL");
@@ -1117,7 +1196,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     if ((dY && !al16(dY)) || (X && !al16(X)) || (dX && !al16(dX)) || !al16(dA) || !al16(dB) ||
         (U_saved && !al16(U_saved)))
         return fail(QLORA_ERR_ALIGN, "dY, X, U_saved, dX, dA and dB must be 16-byte aligned");
-    const int64_t N = w->rows, K = w->cols;
+    const int64_t N = w.rows, K = w.cols;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (M == 0) {
         if (cudaMemsetAsync(dA, 0, sizeof(float) * r * K, s) != cudaSuccess ||
@@ -1160,8 +1239,8 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
         dim3 grid((unsigned)cdiv(K, kSt), (unsigned)cdiv(M, kSt));
         {
             ProfScope ps(QLORA_KERNEL_DX_SIMT, s);
-            k_dx_simt<<<grid, 256, 0, s>>>(dY16, M, N, w->codes, w->absmax_q, w->absmax_scale, w->absmax_mean, K,
-                                           b.sV, rp, A16, r, static_cast<uint16_t *>(dX));
+            k_dx_simt<<<grid, 256, 0, s>>>(dY16, M, N, w.codes, w.q, w.s2, w.mean, K, b.sV, rp, A16, r,
+                                           static_cast<uint16_t *>(dX), w.absmax, w.tab);
         }
         if ((st = launch_check("k_dx_simt"))) return st;
         GradSplit ga = grad_split(M, K);
@@ -1226,7 +1305,7 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
                        CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
         (st = make_map(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "X (MN)")) ||
-        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, K / 2, N, K / 2, 64, 64,
+        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_64B, "codes")) ||
         (st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.sV, rs, M, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "sV")) ||
@@ -1264,9 +1343,11 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     prm.nk_main = cdiv(N, kGemmBK);
     prm.lora_steps = rp / 64;
     prm.r = r;
-    prm.q = w->absmax_q;
-    prm.s2 = w->absmax_scale;
-    prm.mean = w->absmax_mean;
+    prm.q = w.q;
+    prm.s2 = w.s2;
+    prm.mean = w.mean;
+    prm.absmax = w.absmax;
+    prm.tab = w.tab;
     prm.out = static_cast<uint16_t *>(dX);
     prm.ldo = K;
     prm.out_v4 = (reinterpret_cast<uintptr_t>(dX) & 15) == 0 && (K & 7) == 0;
@@ -1281,6 +1362,41 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
     const SkJob jb{&tmDmn, &tmUp, sk_plan(N, M, r), kRedDB, scale, nullptr, 0, nullptr, 0, dB};
     if ((st = run_skinny<1, 1>(ja, &jb, r, s, 5))) return st;
     return ok();
+}
+
+qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *w, const void *A, const void *B,
+                              int r, float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
+                              qlora_stream_t stream) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return linear_fwd_impl(X, M, wt_of(w), A, B, r, scale, Y, U_save, ws, ws_bytes, stream);
+}
+
+qlora_status qlora_q4_linear_fwd(const void *X, int64_t M, const qlora_q4_weight *w, const void *A, const void *B,
+                                 int r, float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
+                                 qlora_stream_t stream) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return linear_fwd_impl(X, M, wt_of(w), A, B, r, scale, Y, U_save, ws, ws_bytes, stream);
+}
+
+qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
+                              const qlora_nf4_weight *w, const void *A, const void *B, int r, float scale, void *dX,
+                              float *dA, float *dB, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return linear_bwd_impl(dY, X, U_saved, M, wt_of(w), A, B, r, scale, dX, dA, dB, ws, ws_bytes, stream);
+}
+
+qlora_status qlora_q4_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
+                                 const qlora_q4_weight *w, const void *A, const void *B, int r, float scale, void *dX,
+                                 float *dA, float *dB, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
+    return linear_bwd_impl(dY, X, U_saved, M, wt_of(w), A, B, r, scale, dX, dA, dB, ws, ws_bytes, stream);
+}
+
+void qlora_q4_table(int table, float levels[16]) {
+    if (!levels) return;
+    static const float tabs[2][16] = {QLORA_NF4_LEVELS, QLORA_INT4_LEVELS};
+    const bool known = table == QLORA_TABLE_NF4 || table == QLORA_TABLE_INT4;
+    for (int i = 0; i < 16; ++i) levels[i] = known ? tabs[table][i] : 0.0f;
 }
 
 void qlora_profile_start(void) {

@@ -61,7 +61,8 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
                                                                  const float *__restrict__ mean_p, int64_t N,
                                                                  const uint16_t *__restrict__ sU, int ldu,
                                                                  const uint16_t *__restrict__ B, int r,
-                                                                 uint16_t *__restrict__ Y, uint64_t wait_ns) {
+                                                                 uint16_t *__restrict__ Y, uint64_t wait_ns,
+                                                                 const float *__restrict__ absmax_f32, int tabid) {
     using C = SmallCfg;
     // X^T fragments are prefetched P stages ahead in registers
     constexpr int P = NT == 1 ? 2 : 1;
@@ -100,13 +101,14 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
     // reconstructed absmax a' of every (row, block) of this CTA's 16 rows,
     // while the codes stream in (loads of four entries in flight per thread)
     {
-        const float mean = *mean_p;
+        const float mean = absmax_f32 ? 0.0f : *mean_p;
         const int nb = (int)kblocks, total = 16 * nb;
 #pragma unroll 4
         for (int i = threadIdx.x; i < total; i += C::THREADS) {
             const int rr = i / nb, kb = i - rr * nb;
             const int64_t b = (n0 + rr) * kblocks + kb;
-            amax[rr][kb] = n0 + rr < N ? dq_absmax(__ldg(q + b), __ldg(s2 + (b >> 8)), mean) : 0.0f;
+            amax[rr][kb] = n0 + rr < N ? (absmax_f32 ? __ldg(absmax_f32 + b) : dq_absmax(__ldg(q + b), __ldg(s2 + (b >> 8)), mean))
+                                       : 0.0f;
         }
     }
     __syncthreads();
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(SmallCfg::THREADS) k_fwd_small(const __grid_co
     } else {
         // -------------------------------------------- compute warps 0..3 ----
         const int g = lane >> 2, t = lane & 3;
-        const Nf4Table tab = make_table(1.0f);  // bf16(L[i])
+        const Nf4Table tab = make_table(1.0f, tabid);  // bf16(L[i])
         // this thread's 8 code bytes of block `warp` of a stage's box, rows g
         // and g + 8 (128-byte rows, 128-byte swizzle: chunk c at c ^ (row % 8));
         // block warp + 4 sits in the second box, 2048 bytes on

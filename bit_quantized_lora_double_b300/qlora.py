@@ -14,6 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 from dataclasses import dataclass
+from typing import Optional
 
 import torch
 
@@ -32,7 +33,11 @@ EXPORTS = [
     "qlora_last_error", "qlora_check_device_status", "qlora_set_wait_limit", "qlora_version",
     "qlora_profile_start", "qlora_profile_stop", "qlora_debug_gemm_segments",
     "qlora_lora_merge_workspace", "qlora_lora_merge_requantize", "qlora_adamw_step",
+    "qlora_q4_table", "qlora_q4_quantize", "qlora_q4_dequantize", "qlora_q4_linear_fwd_workspace",
+    "qlora_q4_linear_bwd_workspace", "qlora_q4_linear_fwd", "qlora_q4_linear_bwd",
 ]
+
+TABLE_NF4, TABLE_INT4 = 0, 1
 
 KERNEL_KINDS = ["quantize", "dequant", "lora_pre", "fwd_gemm", "fwd_simt", "dx_gemm", "dx_simt", "grads", "optim"]
 
@@ -47,6 +52,12 @@ class Nf4WeightDesc(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("codes", ctypes.c_void_p),
                 ("absmax_q", ctypes.c_void_p), ("absmax_scale", ctypes.c_void_p),
                 ("absmax_mean", ctypes.c_void_p)]
+
+
+class Q4WeightDesc(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("table", ctypes.c_int32),
+                ("double_quant", ctypes.c_int32), ("codes", ctypes.c_void_p), ("absmax_q", ctypes.c_void_p),
+                ("absmax_scale", ctypes.c_void_p), ("absmax_mean", ctypes.c_void_p), ("absmax", ctypes.c_void_p)]
 
 
 def lib():
@@ -96,6 +107,21 @@ def lib():
         L.qlora_lora_merge_requantize.argtypes = [W, vp, vp, i32, f32, W, vp, sz, vp]
         L.qlora_adamw_step.restype = i32
         L.qlora_adamw_step.argtypes = [vp, vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, i64, vp]
+        Q = ctypes.POINTER(Q4WeightDesc)
+        L.qlora_q4_table.restype = None
+        L.qlora_q4_table.argtypes = [i32, vp]
+        L.qlora_q4_quantize.restype = i32
+        L.qlora_q4_quantize.argtypes = [vp, Q, vp, sz, vp]
+        L.qlora_q4_dequantize.restype = i32
+        L.qlora_q4_dequantize.argtypes = [Q, vp, vp]
+        L.qlora_q4_linear_fwd_workspace.restype = sz
+        L.qlora_q4_linear_fwd_workspace.argtypes = [i64, Q, i32]
+        L.qlora_q4_linear_bwd_workspace.restype = sz
+        L.qlora_q4_linear_bwd_workspace.argtypes = [i64, Q, i32]
+        L.qlora_q4_linear_fwd.restype = i32
+        L.qlora_q4_linear_fwd.argtypes = [vp, i64, Q, vp, vp, i32, f32, vp, vp, vp, sz, vp]
+        L.qlora_q4_linear_bwd.restype = i32
+        L.qlora_q4_linear_bwd.argtypes = [vp, vp, vp, i64, Q, vp, vp, i32, f32, vp, vp, vp, vp, sz, vp]
         L.qlora_debug_gemm_segments.restype = i64
         L.qlora_debug_gemm_segments.argtypes = [i64, i64, i64, i32, i32, vp, i64]
         _lib = L
@@ -134,6 +160,28 @@ class Nf4Weight:
                              self.absmax_scale.data_ptr(), self.absmax_mean.data_ptr())
 
 
+@dataclass
+class Q4Weight:
+    """A quantized weight of either level table, with the block absmax
+    double-quantized (absmax_q, absmax_scale, absmax_mean) or as fp32
+    (absmax); the unused arrays are None."""
+    rows: int
+    cols: int
+    table: int
+    double_quant: bool
+    codes: torch.Tensor
+    absmax_q: Optional[torch.Tensor] = None
+    absmax_scale: Optional[torch.Tensor] = None
+    absmax_mean: Optional[torch.Tensor] = None
+    absmax: Optional[torch.Tensor] = None
+
+    @property
+    def desc(self) -> Q4WeightDesc:
+        p = lambda t: None if t is None else t.data_ptr()
+        return Q4WeightDesc(self.rows, self.cols, self.table, int(self.double_quant), self.codes.data_ptr(),
+                            p(self.absmax_q), p(self.absmax_scale), p(self.absmax_mean), p(self.absmax))
+
+
 # ---- sizes -----------------------------------------------------------------
 
 def qlora_nf4_codes_bytes(rows, cols):
@@ -163,6 +211,23 @@ def qlora_nf4_table():
     return out
 
 
+def qlora_q4_table(table: int):
+    import numpy as np
+    out = np.zeros(16, np.float32)
+    lib().qlora_q4_table(int(table), out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def qlora_q4_linear_fwd_workspace(M, w: Q4Weight, r):
+    d = w.desc
+    return lib().qlora_q4_linear_fwd_workspace(M, ctypes.byref(d), r)
+
+
+def qlora_q4_linear_bwd_workspace(M, w: Q4Weight, r):
+    d = w.desc
+    return lib().qlora_q4_linear_bwd_workspace(M, ctypes.byref(d), r)
+
+
 def qlora_linear_fwd_workspace(M, w: Nf4Weight, r):
     d = w.desc
     return lib().qlora_linear_fwd_workspace(M, ctypes.byref(d), r)
@@ -183,6 +248,22 @@ def alloc_nf4_weight(rows: int, cols: int, device="cuda") -> Nf4Weight:
                      torch.empty(nb, dtype=torch.int8, device=device),
                      torch.empty(qlora_nf4_scale_count(rows, cols), dtype=torch.float32, device=device),
                      torch.empty(4, dtype=torch.float32, device=device))
+
+
+def alloc_q4_weight(rows: int, cols: int, table: int, double_quant: bool, device="cuda") -> Q4Weight:
+    """Allocates the device arrays of a quantized weight of the given format."""
+    nb = qlora_nf4_absmax_count(rows, cols)
+    if qlora_nf4_codes_bytes(rows, cols) == 0 and rows != 0:
+        raise QloraError(2, f"invalid weight shape [{rows}, {cols}]")
+    codes = torch.empty(rows * cols // 2, dtype=torch.uint8, device=device)
+    if double_quant:
+        return Q4Weight(rows, cols, table, True, codes,
+                        absmax_q=torch.empty(nb, dtype=torch.int8, device=device),
+                        absmax_scale=torch.empty(qlora_nf4_scale_count(rows, cols), dtype=torch.float32,
+                                                 device=device),
+                        absmax_mean=torch.empty(4, dtype=torch.float32, device=device))
+    return Q4Weight(rows, cols, table, False, codes, absmax=torch.empty(max(nb, 4), dtype=torch.float32,
+                                                                         device=device))
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
@@ -220,6 +301,32 @@ def qlora_linear_bwd(dY, X, U_saved, M, w: Nf4Weight, A, B, r, scale, dX, dA, dB
     _check(lib().qlora_linear_bwd(_ptr(dY), _ptr(X), _ptr(U_saved), M, ctypes.byref(d), _ptr(A), _ptr(B), r,
                                   float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws),
                                   0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qlora_q4_quantize(W: torch.Tensor, out: Q4Weight, ws, stream=None):
+    """Quantize into `out`'s format; `ws` may be None when out.double_quant is False."""
+    d = out.desc
+    _check(lib().qlora_q4_quantize(_ptr(W), ctypes.byref(d), _ptr(ws),
+                                   0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qlora_q4_dequantize(w: Q4Weight, out: torch.Tensor, stream=None):
+    d = w.desc
+    _check(lib().qlora_q4_dequantize(ctypes.byref(d), _ptr(out), _stream(stream)))
+
+
+def qlora_q4_linear_fwd(X, M, w: Q4Weight, A, B, r, scale, Y, U_save, ws, stream=None):
+    d = w.desc
+    _check(lib().qlora_q4_linear_fwd(_ptr(X), M, ctypes.byref(d), _ptr(A), _ptr(B), r, float(scale), _ptr(Y),
+                                     _ptr(U_save), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                     _stream(stream)))
+
+
+def qlora_q4_linear_bwd(dY, X, U_saved, M, w: Q4Weight, A, B, r, scale, dX, dA, dB, ws, stream=None):
+    d = w.desc
+    _check(lib().qlora_q4_linear_bwd(_ptr(dY), _ptr(X), _ptr(U_saved), M, ctypes.byref(d), _ptr(A), _ptr(B), r,
+                                     float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws),
+                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def qlora_lora_merge_workspace(rows, cols):

@@ -96,6 +96,34 @@ typedef struct {
     float *absmax_mean;     /* 1 fp32 */
 } qlora_nf4_weight;
 
+/* Storage variants of the 4-bit weight (the same kernels decode all four):
+ *  - table: QLORA_TABLE_NF4, the NormalFloat levels above, or
+ *    QLORA_TABLE_INT4, the INT4 baseline the NF4 levels are compared against
+ *    (ashishsrivastav.com, section "NF4 Quantization: Beyond Standard INT4":
+ *    16 evenly spaced levels). Reading: symmetric absmax INT4, level i is
+ *    (i - 7) / 7 rounded to fp32 (code 7 the exact zero, codes 0 and 14 are
+ *    -1 and +1, code 15 is never chosen), nearest level with ties to the lower
+ *    code as for NF4;
+ *  - double_quant: 1 keeps the absmax double-quantized (absmax_q,
+ *    absmax_scale, absmax_mean, as qlora_nf4_weight); 0 keeps it as one fp32
+ *    per block in `absmax` (4.5 bits per weight: xingyuzhitong.com, section
+ *    "QLoRA: quantize the frozen base to 4 bits"), a' = absmax as stored.
+ * Arrays not used by the variant may be NULL. All pointers are device
+ * pointers owned by the caller, 16-byte aligned. */
+#define QLORA_TABLE_NF4 0
+#define QLORA_TABLE_INT4 1
+typedef struct {
+    int64_t rows;           /* N */
+    int64_t cols;           /* K, cols % 64 == 0 */
+    int32_t table;          /* QLORA_TABLE_NF4 or QLORA_TABLE_INT4 */
+    int32_t double_quant;   /* 1: absmax_q/absmax_scale/absmax_mean; 0: absmax */
+    uint8_t *codes;         /* rows*cols/2 bytes */
+    int8_t *absmax_q;       /* double_quant: nb int8 codes */
+    float *absmax_scale;    /* double_quant: ceil(nb/256) fp32 */
+    float *absmax_mean;     /* double_quant: 1 fp32 */
+    float *absmax;          /* !double_quant: nb fp32 */
+} qlora_q4_weight;
+
 /* ---- sizes (host-only, no GPU needed) --------------------------------- */
 
 /* Bytes of packed codes: rows*cols/2. Returns 0 for invalid sizes. */
@@ -113,6 +141,10 @@ size_t qlora_nf4_quantize_workspace(int64_t rows, int64_t cols);
 /* Host copy of the 16 fp32 NF4 levels the kernels use (ascending; code 7 is
  * the exact zero). */
 void qlora_nf4_table(float levels[16]);
+
+/* Host copy of the 16 fp32 levels of a table (QLORA_TABLE_NF4 or
+ * QLORA_TABLE_INT4); all zero for an unknown table. */
+void qlora_q4_table(int table, float levels[16]);
 
 /* ---- codec ------------------------------------------------------------- */
 
@@ -184,6 +216,24 @@ size_t qlora_lora_merge_workspace(int64_t rows, int64_t cols);
 qlora_status qlora_lora_merge_requantize(const qlora_nf4_weight *w, const void *A, const void *B, int r,
                                          float scale, qlora_nf4_weight *out, void *ws, size_t ws_bytes,
                                          qlora_stream_t stream);
+
+/* The storage variants (qlora_q4_weight): quantize, dequantize, forward and
+ * backward exactly as the qlora_nf4_* / qlora_linear_* calls, which are these
+ * calls with table = QLORA_TABLE_NF4 and double_quant = 1. Without double
+ * quantization the quantizer writes the exact block absmax to `absmax` and
+ * needs no workspace (ws may be NULL, ws_bytes 0); with it, the workspace is
+ * qlora_nf4_quantize_workspace bytes. The linear workspaces are the same as
+ * for qlora_linear_fwd / qlora_linear_bwd. */
+qlora_status qlora_q4_quantize(const void *W, qlora_q4_weight *out, void *ws, size_t ws_bytes, qlora_stream_t stream);
+qlora_status qlora_q4_dequantize(const qlora_q4_weight *w, void *out, qlora_stream_t stream);
+size_t qlora_q4_linear_fwd_workspace(int64_t M, const qlora_q4_weight *w, int r);
+size_t qlora_q4_linear_bwd_workspace(int64_t M, const qlora_q4_weight *w, int r);
+qlora_status qlora_q4_linear_fwd(const void *X, int64_t M, const qlora_q4_weight *w, const void *A, const void *B,
+                                 int r, float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
+                                 qlora_stream_t stream);
+qlora_status qlora_q4_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
+                                 const qlora_q4_weight *w, const void *A, const void *B, int r, float scale, void *dX,
+                                 float *dA, float *dB, void *ws, size_t ws_bytes, qlora_stream_t stream);
 
 /* ---- linear layer with LoRA ------------------------------------------- */
 

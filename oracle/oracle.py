@@ -76,6 +76,10 @@ def lib():
                                             vp, i64, vp, i64, vp, i64, vp, vp, vp]
             L.oracle_lora_merge.argtypes = [vp, i64, i64, vp, vp, i32, f32, vp]
             L.oracle_adamw_step.argtypes = [vp, vp, vp, vp, i64, f64, f64, f64, f64, f64, i64]
+            L.oracle_int4_table.argtypes = [vp]
+            L.oracle_q4_encode.argtypes = [vp, i64, vp, vp, vp]
+            L.oracle_q4_dequantize_dq.argtypes = [vp, vp, vp, f32, i64, i64, vp, vp]
+            L.oracle_q4_dequantize_f32.argtypes = [vp, vp, i64, i64, vp, vp]
             _lib = L
     return _lib
 
@@ -279,3 +283,52 @@ def adamw_step(p, g, m, v, lr, beta1, beta2, eps, weight_decay, step):
         assert a.dtype == np.float64 and a.flags.c_contiguous
     g = np.ascontiguousarray(g, np.float64)
     lib().oracle_adamw_step(_p(p), _p(g), _p(m), _p(v), p.size, lr, beta1, beta2, eps, weight_decay, step)
+
+
+# ------------------------------------------------------------- variants ----
+# Storage variants of the 4-bit weight: the NF4 or the INT4 table, and the
+# absmax double-quantized (q, scale, mean) or kept as fp32 per block.
+
+def int4_table() -> np.ndarray:
+    L = np.zeros(16, np.float32)
+    lib().oracle_int4_table(_p(L))
+    return L
+
+
+def q4_table(table: str) -> np.ndarray:
+    return nf4_table() if table == "nf4" else int4_table()
+
+
+def q4_quantize(W: np.ndarray, table: str = "nf4", double_quant: bool = True):
+    """bf16 [rows, cols] -> dict(codes, table, double_quant, absmax (fp32) or absmax_q/scale/mean)."""
+    W = _u16(W)
+    rows, cols = W.shape
+    n = rows * cols
+    nb = n // 64
+    codes = np.zeros(n // 2, np.uint8)
+    a = np.zeros(nb, np.float32)
+    L = q4_table(table)
+    lib().oracle_q4_encode(_p(W), n, _p(L), _p(codes), _p(a))
+    out = dict(codes=codes, rows=rows, cols=cols, table=table, double_quant=double_quant, absmax_exact=a)
+    if double_quant:
+        q, s, mean = dq_encode(a)
+        out.update(absmax_q=q, absmax_scale=s, absmax_mean=np.float32(mean))
+    else:
+        out.update(absmax=a.copy())
+    return out
+
+
+def q4_dequantize(qw: dict) -> np.ndarray:
+    rows, cols = qw["rows"], qw["cols"]
+    out = np.zeros((rows, cols), np.uint16)
+    codes = np.ascontiguousarray(qw["codes"], np.uint8)
+    L = q4_table(qw["table"])
+    if qw["double_quant"]:
+        q = np.ascontiguousarray(qw["absmax_q"], np.int8)
+        s = np.ascontiguousarray(qw["absmax_scale"], np.float32)
+        lib().oracle_q4_dequantize_dq(_p(codes), _p(q), _p(s), ctypes.c_float(float(qw["absmax_mean"])),
+                                      rows, cols, _p(L), _p(out))
+    else:
+        a = np.ascontiguousarray(qw["absmax"], np.float32)
+        lib().oracle_q4_dequantize_f32(_p(codes), _p(a), rows, cols, _p(L), _p(out))
+    return out

@@ -142,12 +142,20 @@ int oracle_nf4_nearest(float x, const float L[16]) {
 /* Blockwise absmax + NF4 encode + packing [QL-70B "NF4 Quantization"].     */
 /* ------------------------------------------------------------------------ */
 
-/* Encodes n = rows*cols bf16 weights (n % 64 == 0). Writes the packed codes
- * (n/2 bytes) and the exact per-block absmax (n/64 floats). The codes use the
- * exact absmax: the weights are quantized first, then the constants. */
-void oracle_nf4_encode(const uint16_t *W, int64_t n, uint8_t *codes, float *absmax) {
-    float L[16];
-    oracle_nf4_table(L);
+/* INT4 baseline table [QL-70B "NF4 Quantization: Beyond Standard INT4": the
+ * standard 4-bit integer format has 16 evenly spaced levels]. Reading:
+ * symmetric absmax INT4, L[i] = (i - 7) / 7, so code 7 is the exact zero,
+ * codes 0 and 14 are -1 and +1, and code 15 (8/7) is never the nearest level
+ * of an x in [-1, 1]. Rounded once from double to fp32. */
+void oracle_int4_table(float L[16]) {
+    for (int i = 0; i < 16; ++i) L[i] = (float)((double)(i - 7) / 7.0);
+}
+
+/* Encodes n = rows*cols bf16 weights (n % 64 == 0) with the 16-level table L
+ * (NF4 or INT4). Writes the packed codes (n/2 bytes) and the exact per-block
+ * absmax (n/64 floats). The codes use the exact absmax: the weights are
+ * quantized first, then the constants. */
+void oracle_q4_encode(const uint16_t *W, int64_t n, const float L[16], uint8_t *codes, float *absmax) {
     int64_t nb = n / NF4_BLOCK;
 #pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < nb; ++b) {
@@ -170,6 +178,13 @@ void oracle_nf4_encode(const uint16_t *W, int64_t n, uint8_t *codes, float *absm
         for (int i = 0; i < NF4_BLOCK / 2; ++i)
             codes[b * (NF4_BLOCK / 2) + i] = (uint8_t)((c[2 * i] << 4) | c[2 * i + 1]);
     }
+}
+
+/* NF4 encode: oracle_q4_encode with the NF4 table. */
+void oracle_nf4_encode(const uint16_t *W, int64_t n, uint8_t *codes, float *absmax) {
+    float L[16];
+    oracle_nf4_table(L);
+    oracle_q4_encode(W, n, L, codes, absmax);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -252,11 +267,10 @@ float oracle_dq_decode(int8_t qb, float s2, float mean) {
     return t + mean;
 }
 
-/* W'[i] = bf16_rne( fp32( L[code_i] * a'_b ) ) for all n elements. */
-void oracle_nf4_dequantize(const uint8_t *codes, const int8_t *q, const float *scale, float mean,
-                           int64_t rows, int64_t cols, uint16_t *out) {
-    float L[16];
-    oracle_nf4_table(L);
+/* W'[i] = bf16_rne( fp32( L[code_i] * a'_b ) ) for all n elements, with
+ * the table L and the double-quantized absmax a'_b. */
+void oracle_q4_dequantize_dq(const uint8_t *codes, const int8_t *q, const float *scale, float mean,
+                             int64_t rows, int64_t cols, const float L[16], uint16_t *out) {
     int64_t n = rows * cols, nb = n / NF4_BLOCK;
 #pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < nb; ++b) {
@@ -268,6 +282,32 @@ void oracle_nf4_dequantize(const uint8_t *codes, const int8_t *q, const float *s
             out[b * NF4_BLOCK + i] = f32_to_bf16_rne(v);
         }
     }
+}
+
+/* The same with the absmax kept as fp32 per block (no double quantization;
+ * the 4.5 bits per weight of xingyuzhitong.com, section "QLoRA: quantize the
+ * frozen base to 4 bits"): a_b is used as stored. */
+void oracle_q4_dequantize_f32(const uint8_t *codes, const float *absmax, int64_t rows, int64_t cols,
+                              const float L[16], uint16_t *out) {
+    int64_t n = rows * cols, nb = n / NF4_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nb; ++b) {
+        float a = absmax[b];
+        for (int i = 0; i < NF4_BLOCK; ++i) {
+            uint8_t byte = codes[b * (NF4_BLOCK / 2) + i / 2];
+            int c = (i % 2 == 0) ? (byte >> 4) : (byte & 15);
+            float v = L[c] * a;
+            out[b * NF4_BLOCK + i] = f32_to_bf16_rne(v);
+        }
+    }
+}
+
+/* NF4 dequantize: oracle_q4_dequantize_dq with the NF4 table. */
+void oracle_nf4_dequantize(const uint8_t *codes, const int8_t *q, const float *scale, float mean,
+                           int64_t rows, int64_t cols, uint16_t *out) {
+    float L[16];
+    oracle_nf4_table(L);
+    oracle_q4_dequantize_dq(codes, q, scale, mean, rows, cols, L, out);
 }
 
 /* ------------------------------------------------------------------------ */

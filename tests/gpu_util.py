@@ -42,9 +42,37 @@ def weight_from_oracle(qw: dict):
     return w
 
 
+TABLES = {"nf4": qlora.TABLE_NF4, "int4": qlora.TABLE_INT4}
+
+
+def q4_quantize(W: np.ndarray, table: str, double_quant: bool):
+    rows, cols = W.shape
+    w = qlora.alloc_q4_weight(rows, cols, TABLES[table], double_quant)
+    ws = qlora.workspace(qlora.qlora_nf4_quantize_workspace(rows, cols)) if double_quant else None
+    qlora.qlora_q4_quantize(dev_bf16(W), w, ws)
+    return w
+
+
+def q4_weight_from_oracle(qw: dict):
+    """Device copy of an oracle-quantized weight of any format."""
+    w = qlora.alloc_q4_weight(qw["rows"], qw["cols"], TABLES[qw["table"]], qw["double_quant"])
+    w.codes.copy_(torch.from_numpy(qw["codes"]))
+    if qw["double_quant"]:
+        w.absmax_q.copy_(torch.from_numpy(qw["absmax_q"]))
+        w.absmax_scale.copy_(torch.from_numpy(qw["absmax_scale"]))
+        w.absmax_mean[0] = float(qw["absmax_mean"])
+    else:
+        w.absmax[:len(qw["absmax"])].copy_(torch.from_numpy(qw["absmax"]))
+    return w
+
+
+def _is_q4(w) -> bool:
+    return isinstance(w, qlora.Q4Weight)
+
+
 def dequantize(w) -> np.ndarray:
     out = torch.empty((w.rows, w.cols), dtype=torch.bfloat16, device="cuda")
-    qlora.qlora_nf4_dequantize(w, out)
+    (qlora.qlora_q4_dequantize if _is_q4(w) else qlora.qlora_nf4_dequantize)(w, out)
     torch.cuda.synchronize()
     return host_u16(out)
 
@@ -54,8 +82,12 @@ def fwd(X, w, A, B, r, scale, save_u=True):
     Xd, Ad, Bd = dev_bf16(X), dev_bf16(A), dev_bf16(B)
     Y = torch.empty((M, w.rows), dtype=torch.bfloat16, device="cuda")
     U = torch.empty((M, r), dtype=torch.bfloat16, device="cuda") if save_u else None
-    ws = qlora.workspace(qlora.qlora_linear_fwd_workspace(M, w, r))
-    qlora.qlora_linear_fwd(Xd, M, w, Ad, Bd, r, scale, Y, U, ws)
+    if _is_q4(w):
+        ws = qlora.workspace(qlora.qlora_q4_linear_fwd_workspace(M, w, r))
+        qlora.qlora_q4_linear_fwd(Xd, M, w, Ad, Bd, r, scale, Y, U, ws)
+    else:
+        ws = qlora.workspace(qlora.qlora_linear_fwd_workspace(M, w, r))
+        qlora.qlora_linear_fwd(Xd, M, w, Ad, Bd, r, scale, Y, U, ws)
     torch.cuda.synchronize()
     qlora.qlora_check_device_status()
     return Y, U
@@ -66,8 +98,14 @@ def bwd(dY, X, U, w, A, B, r, scale):
     dX = torch.empty((M, w.cols), dtype=torch.bfloat16, device="cuda")
     dA = torch.empty((r, w.cols), dtype=torch.float32, device="cuda")
     dB = torch.empty((w.rows, r), dtype=torch.float32, device="cuda")
-    ws = qlora.workspace(qlora.qlora_linear_bwd_workspace(M, w, r))
-    qlora.qlora_linear_bwd(dev_bf16(dY), dev_bf16(X), U, M, w, dev_bf16(A), dev_bf16(B), r, scale, dX, dA, dB, ws)
+    if _is_q4(w):
+        ws = qlora.workspace(qlora.qlora_q4_linear_bwd_workspace(M, w, r))
+        qlora.qlora_q4_linear_bwd(dev_bf16(dY), dev_bf16(X), U, M, w, dev_bf16(A), dev_bf16(B), r, scale, dX, dA,
+                                  dB, ws)
+    else:
+        ws = qlora.workspace(qlora.qlora_linear_bwd_workspace(M, w, r))
+        qlora.qlora_linear_bwd(dev_bf16(dY), dev_bf16(X), U, M, w, dev_bf16(A), dev_bf16(B), r, scale, dX, dA, dB,
+                               ws)
     torch.cuda.synchronize()
     qlora.qlora_check_device_status()
     return dX, dA, dB

@@ -42,6 +42,12 @@ def test_table_matches_oracle(q, oracle):
     assert np.array_equal(q.qlora_nf4_table().view(np.uint32), oracle.nf4_table().view(np.uint32))
 
 
+def test_q4_tables_match_oracle(q, oracle):
+    assert np.array_equal(q.qlora_q4_table(q.TABLE_NF4).view(np.uint32), oracle.q4_table("nf4").view(np.uint32))
+    assert np.array_equal(q.qlora_q4_table(q.TABLE_INT4).view(np.uint32), oracle.q4_table("int4").view(np.uint32))
+    assert not q.qlora_q4_table(7).any()
+
+
 
 
 def test_storage_bits_match_pages(q):
@@ -102,6 +108,34 @@ def test_quantize_rejects_on_host(q):
     assert call_quant(q, FAKE, desc(codes=0), FAKE, need) == 1
     assert call_quant(q, FAKE, desc(s=FAKE + 4), FAKE, need) == 3
     assert call_quant(q, FAKE, desc(), 0, need) == 1
+
+
+def q4desc(table=0, dq=0, rows=64, cols=128, codes=FAKE, qq=0, s=0, m=0, a=FAKE):
+    return q_mod().Q4WeightDesc(rows, cols, table, dq, codes, qq, s, m, a)
+
+
+def test_q4_quantize_rejects_on_host(q):
+    L = q.lib()
+    c = ctypes.c_void_p
+
+    def call(d, ws=0, nbytes=0):
+        return L.qlora_q4_quantize(c(FAKE), ctypes.byref(d), c(ws), nbytes, None)
+    assert call(q4desc(table=2)) == 8
+    assert call(q4desc(dq=2)) == 8
+    assert call(q4desc(a=0)) == 1
+    assert call(q4desc(a=FAKE + 4)) == 3
+    # double-quantized: its three arrays and the workspace are required
+    assert call(q4desc(dq=1, a=0)) == 1
+    assert call(q4desc(dq=1, qq=FAKE, s=FAKE, m=FAKE, a=0)) == 1
+    need = q.qlora_nf4_quantize_workspace(64, 128)
+    assert call(q4desc(dq=1, qq=FAKE, s=FAKE, m=FAKE, a=0), FAKE, need - 1) == 4
+    d = q4desc(table=1, rows=0)
+    assert call(d) == 0  # no rows: nothing to launch
+    assert L.qlora_q4_dequantize(ctypes.byref(q4desc(table=3)), c(FAKE), None) == 8
+    assert L.qlora_q4_linear_fwd_workspace(16, ctypes.byref(q4desc()), 8) == \
+        L.qlora_linear_fwd_workspace(16, ctypes.byref(desc()), 8)
+    assert L.qlora_q4_linear_fwd(c(FAKE), 16, ctypes.byref(q4desc(table=9)), c(FAKE), c(FAKE), 8, 2.0, c(FAKE),
+                                 None, c(FAKE), 1 << 30, None) == 8
 
 
 def call_fwd(q, M=16, d=None, r=8, ws_bytes=None, X=FAKE, A=FAKE, B=FAKE, Y=FAKE):
