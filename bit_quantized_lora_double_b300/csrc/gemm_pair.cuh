@@ -169,16 +169,23 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64
 // of it. Inside that range a pair works through segments, one per tile
 // touched:
 //   kSegFull  the whole tile: the pair writes the output;
-//   kSegPart  the tile's tail (the range starts inside the tile): always the
-//             pair's first stream-K segment; the fp32 partial goes to the
-//             pair's slot and each epilogue warp raises its ready flag;
+//   kSegPart  a later part of the tile (the range starts inside the tile):
+//             always the pair's first stream-K segment;
 //   kSegHead  the tile's first steps (the range ends inside the tile): always
-//             the pair's last segment; the pair adds the partials of the
-//             following pairs (whose ranges start inside this tile), in pair
-//             order, and writes the output.
-// Every pair holds at most one slot's worth of partial and finishes at most
-// one shared tile, and the tails it waits for were its neighbours' first
-// stream-K work.
+//             the pair's last segment.
+// A shared tile's contributors are its head pair h and the pairs h + 1 ..
+// h + n - 1 whose ranges start inside it. Each epilogue warp of each
+// contributor, once its accumulators are complete, counts itself in on the
+// tile's arrival counter. The last to arrive finishes the tile: it waits for
+// the others' ready flags, adds their fp32 partials and its own accumulators
+// in pair order (so the sum is the same whoever arrives last) and writes the
+// output. Every other contributor writes its partial to its slot (the head
+// slot or the tail slot: a pair may hold one of each) and raises the slot's
+// ready flag. A pair only ever waits for contributors that have already
+// arrived, so no pair depends on another pair being resident or making
+// progress. With the host's schedule a shared tile has at most four
+// contributors, and the head, whose segment is its pair's last, usually
+// arrives last.
 enum { kSegFull = 0, kSegHead = 1, kSegPart = 2 };
 
 struct PairSeg {
@@ -226,6 +233,14 @@ __host__ __device__ __forceinline__ int64_t head_contrib_end(const PairPlan &pl,
     int64_t e = q + 1;
     while (e < pl.P && pl.begin(e) < tend) ++e;
     return e;
+}
+
+// The pair computing tile t's first steps: the last pair whose range begins
+// at or before step t * S (pair q's range begins after it).
+__host__ __device__ __forceinline__ int64_t head_pair(const PairPlan &pl, int64_t q, int64_t t) {
+    int64_t h = q;
+    while (h > 0 && pl.begin(h) > t * pl.S) --h;
+    return h;
 }
 
 // Walks one pair's segments: its data-parallel tiles, then its stream-K range.
@@ -294,6 +309,11 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 // Bounded wait for a ready flag raised by another pair.
 __device__ __forceinline__ bool flag_wait(const uint32_t *f, uint64_t limit_ns, unsigned code,
@@ -618,16 +638,20 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         //
         // A partial tile goes to the pair's slot in this warp's own order:
         // [CTA][warp][batch][8-column chunk][lane][8 fp32], so every store
-        // instruction writes 1 KB of consecutive bytes. Finishing a tile, the
-        // warp fetches the matching 8 KB pieces of the contributors' slots
-        // into the (now idle) stage buffers with bulk copies, NFIX in flight,
-        // and adds them in pair order.
+        // instruction writes 1 KB of consecutive bytes. Finishing a tile in
+        // the pair's last segment, the warp fetches the matching 8 KB pieces
+        // of the other contributors' slots into the (now idle) stage buffers
+        // with bulk copies, NFIX in flight; finishing one earlier, it loads
+        // them from global memory. It adds them in pair order.
         const int ew = warp - (2 + C::GROUP_WARPS * C::DEC_GROUPS);  // 0..3
         const int quarter = warp & 3;
         uint8_t *stg = smem + C::EPI_OFF + ew * 4096;
         const uint32_t tempty_addr0 = mapa_u32(smem_u32(tempty), 0);
         uint8_t *fixbuf = smem + ew * (C::NFIX * 8192);  // NFIX 8 KB buffers of this warp
-        int fx_issued = 0, fx_waited = 0;     // pieces fetched / consumed (one head segment at most)
+        // pieces fetched / consumed, counted over the whole launch: a pair may
+        // finish two shared tiles, and the piece ring's barriers keep their
+        // phases from one to the next
+        int fx_issued = 0, fx_waited = 0;
         int64_t tl = 0;
         SegWalk sw = seg_walk(pl, pair_id);
         PairSeg w;
@@ -636,28 +660,68 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 break;
             tc_fence_after();
             const int nb = w.two ? C::NBATCH : C::NBATCH / 2;
-            // contributors of a head segment: pairs pair_id + 1 .. qend - 1
-            const int64_t qend = w.role == kSegHead ? head_contrib_end(pl, pair_id, w.t) : pair_id + 1;
-            const int nq = (int)(qend - pair_id - 1);
-            const int nitems = nq * nb;
+            // a shared tile: contributors h .. h + n - 1, this pair is number m
+            int64_t h = pair_id;
+            int n = 1;
+            if (w.role != kSegFull) {
+                if (w.role == kSegPart) h = head_pair(pl, pair_id, w.t);
+                n = (int)(head_contrib_end(pl, h, w.t) - h);
+            }
+            const int m = (int)(pair_id - h);
+            bool finish = true;
+            if (n > 1) {
+                uint32_t old = 0;
+                if (lane == 0)
+                    old = atom_add_acq_rel_gpu(p.flags + kSkReadyWords + (h * 2 + rank) * C::EPI_WARPS + ew, 1u);
+                finish = __shfl_sync(0xffffffffu, old, 0) == (uint32_t)(n - 1);
+            }
+            // the others' partials this warp adds when it finishes the tile:
+            // piece i = (batch b, other contributor qi), the one of pair
+            // h + j with j = qi (before this pair) or qi + 1 (after it); the
+            // head's partial is in its head slot, the others' in their tail slots
+            const int nq = finish ? n - 1 : 0;
+            if (nq > C::NFIX) {
+                // (the schedule never shares a tile this widely)
+                if (lane == 0) {
+                    record_error((p.kernel_id << 16) | 9);
+                    *abort_flag = 1;
+                    st_cluster_u32(peer_abort, 1u);
+                }
+                break;
+            }
+            // The pieces go through the stage ring (bulk copies, NFIX in
+            // flight) only when this is the pair's last segment: the ring is
+            // idle then (every load issued has been consumed by the MMAs).
+            // A pair finishing a tile with more segments to come (a tail that
+            // arrived last) reads the partials from global memory instead.
+            SegWalk nx = sw;
+            PairSeg wn;
+            const bool use_ring = !seg_next(p, pl, nx, wn);
+            const int nitems = use_ring ? nq * nb : 0;
+            const int fx0 = fx_issued;  // this segment's piece i is piece fx0 + i of the launch
+            auto other = [&](int qi) { return qi < m ? qi : qi + 1; };
+            auto slot_of = [&](int64_t q, int head) { return p.slots + (q * 2 + head) * kSlotFloats; };
+            auto ready_of = [&](int64_t q, int head) { return p.flags + ((q * 2 + head) * 2 + rank) * C::EPI_WARPS + ew; };
             auto fetch_piece = [&](int i) {
                 if (i >= nitems) return;
-                fx_issued = i + 1;
+                const int gi = fx0 + i;
+                fx_issued = gi + 1;
                 if (lane != 0) return;
                 const int b = i / nq;
-                const int64_t q = pair_id + 1 + i % nq;
-                const float *src =
-                    p.slots + q * kSlotFloats + (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
-                uint64_t *fb = &fixbar[ew * C::NFIX + i % C::NFIX];
+                const int j = other(i % nq);
+                const float *src = slot_of(h + j, j == 0) + (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
+                uint64_t *fb = &fixbar[ew * C::NFIX + gi % C::NFIX];
                 mbar_arrive_expect_tx(fb, 8192);
-                bulk_g2s(fixbuf + (i % C::NFIX) * 8192, src, 8192, fb);
+                bulk_g2s(fixbuf + (gi % C::NFIX) * 8192, src, 8192, fb);
             };
             if (nq > 0) {
                 bool ok = true;
                 if (lane == 0) {
-                    for (int64_t q = pair_id + 1; q < qend && ok; ++q)
-                        ok = flag_wait(p.flags + (q * 2 + rank) * C::EPI_WARPS + ew, p.wait_ns, (p.kernel_id << 16) | 7,
-                                       abort_flag, peer_abort);
+                    for (int qi = 0; qi < nq && ok; ++qi) {
+                        const int j = other(qi);
+                        ok = flag_wait(ready_of(h + j, j == 0), p.wait_ns, (p.kernel_id << 16) | 7, abort_flag,
+                                       peer_abort);
+                    }
                     if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -685,8 +749,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive_cluster(tempty_addr0);
                     }
-                    if (w.role == kSegPart) {
-                        float *dst = p.slots + pair_id * kSlotFloats +
+                    if (!finish) {
+                        float *dst = slot_of(pair_id, m == 0) +
                                      (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
 #pragma unroll
                         for (int jc = 0; jc < 8; ++jc) {
@@ -697,28 +761,52 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         }
                         continue;
                     }
-                    for (int qi = 0; qi < nq; ++qi) {
-                        const int i = b * nq + qi;
-                        if (!pair_wait(&fixbar[ew * C::NFIX + i % C::NFIX], (uint32_t)(i / C::NFIX) & 1, p.wait_ns,
-                                       (p.kernel_id << 16) | 8, abort_flag, peer_abort)) {
-                            alive = false;
-                            break;
+                    if (nq > 0) {
+                        // this batch's pieces (nq <= NFIX: all in the ring at once)
+                        for (int qi = 0; qi < nq && alive && use_ring; ++qi) {
+                            const int gi = fx0 + b * nq + qi;
+                            alive = pair_wait(&fixbar[ew * C::NFIX + gi % C::NFIX], (uint32_t)(gi / C::NFIX) & 1,
+                                              p.wait_ns, (p.kernel_id << 16) | 8, abort_flag, peer_abort);
+                            if (alive) fx_waited = gi + 1;
                         }
-                        fx_waited = i + 1;
-                        const float *src = reinterpret_cast<const float *>(fixbuf + (i % C::NFIX) * 8192);
+                        if (!alive) break;
+                        // the n terms in pair order, this pair's own (in v) as term m
 #pragma unroll
                         for (int jc = 0; jc < 8; ++jc) {
-                            const float4 a0 = *reinterpret_cast<const float4 *>(src + (jc * 32 + lane) * 8);
-                            const float4 a1 = *reinterpret_cast<const float4 *>(src + (jc * 32 + lane) * 8 + 4);
-                            const float add[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                            float a[8];
+#pragma unroll 1
+                            for (int j = 0; j < n; ++j) {
+                                float t[8];
+                                if (j == m) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                v[8 * jc + e] = __float_as_uint(__uint_as_float(v[8 * jc + e]) + add[e]);
+                                    for (int e = 0; e < 8; ++e) t[e] = __uint_as_float(v[8 * jc + e]);
+                                } else {
+                                    float4 t0, t1;
+                                    if (use_ring) {
+                                        const int gi = fx0 + b * nq + (j < m ? j : j - 1);
+                                        const float *src = reinterpret_cast<const float *>(
+                                                               fixbuf + (gi % C::NFIX) * 8192) + (jc * 32 + lane) * 8;
+                                        t0 = *reinterpret_cast<const float4 *>(src);
+                                        t1 = *reinterpret_cast<const float4 *>(src + 4);
+                                    } else {
+                                        const float *src = slot_of(h + j, j == 0) +
+                                                           (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048 +
+                                                           (jc * 32 + lane) * 8;
+                                        t0 = __ldcg(reinterpret_cast<const float4 *>(src));
+                                        t1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                                    }
+                                    t[0] = t0.x, t[1] = t0.y, t[2] = t0.z, t[3] = t0.w;
+                                    t[4] = t1.x, t[5] = t1.y, t[6] = t1.z, t[7] = t1.w;
+                                }
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) a[e] = j == 0 ? t[e] : a[e] + t[e];
+                            }
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[8 * jc + e] = __float_as_uint(a[e]);
                         }
-                        __syncwarp();  // every lane has read the buffer before it is refilled
-                        fetch_piece(i + C::NFIX);
+                        __syncwarp();  // every lane has read the buffers before they are refilled
+                        for (int qi = 0; qi < nq; ++qi) fetch_piece(b * nq + qi + C::NFIX);
                     }
-                    if (!alive) break;
                     const int64_t ncol = p.Nd - (w.c0 + col);  // valid columns from here
                     if (p.out_v4) {
                         // the previous batch's store has read the staging tile
@@ -753,12 +841,12 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 }
             }
             if (!alive) break;
-            if (w.role == kSegPart) {
+            if (!finish) {
                 // this warp's share of the partial tile is written: raise its flag
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
-                    st_release_gpu(p.flags + (pair_id * 2 + rank) * C::EPI_WARPS + ew, 1u);
+                    st_release_gpu(ready_of(pair_id, m == 0), 1u);
                 }
             }
         }

@@ -20,10 +20,15 @@ enum { kFwd = 0, kDx = 1 };
 // Contraction steps are 64 deep (one NF4 block of a weight row).
 constexpr int kGemmBK = 64;
 
-// Stream-K hand-off area: per pair (at most 74), room for 16 ready flags (one
-// per CTA and epilogue warp) and a 512 x 256 fp32 partial tile.
+// Stream-K hand-off area, per pair (at most 74): two 512 x 256 fp32
+// partial-tile slots (one for the tail of a tile the pair shares with the pairs
+// before it, one for the head of a tile it shares with the pairs after it),
+// a ready flag per slot, CTA and epilogue warp (16 words), and an arrival
+// counter per CTA and epilogue warp for the shared tile the pair heads
+// (8 words). All words start at zero.
 constexpr int kSkPairs = 74;
-constexpr int kSkFlagWords = kSkPairs * 16;
+constexpr int kSkReadyWords = kSkPairs * 16;
+constexpr int kSkFlagWords = kSkPairs * 24;
 constexpr int64_t kSlotFloats = 512 * 256;
 
 struct TcParams {
@@ -41,9 +46,9 @@ struct TcParams {
     int tab;               // level table (kTableNF4 / kTableINT4)
     uint16_t *out;
     int64_t ldo;
-    // Stream-K hand-off between pairs (zeroed flags before the launch):
-    // flags [kSkFlagWords] and one partial-tile slot of kSlotFloats fp32
-    // per pair.
+    // Stream-K hand-off between pairs (zeroed before the launch):
+    // flags [kSkFlagWords] (ready flags, then arrival counters) and two
+    // partial-tile slots of kSlotFloats fp32 per pair.
     uint32_t *flags;
     float *slots;
     int64_t dp_tiles;      // tiles t < dp_tiles run data-parallel, the rest stream-K

@@ -267,9 +267,9 @@ SkPlan sk_plan(int64_t rows, int64_t L, int r) {
     return p;
 }
 
-// Stream-K hand-off area of the fused GEMM: the ready flags (zeroed by the
-// skinny kernel that precedes the GEMM in the same call) and one fp32
-// partial-tile slot per CTA pair.
+// Stream-K hand-off area of the fused GEMM: the ready flags and arrival
+// counters (zeroed by the skinny kernel that precedes the GEMM in the same
+// call) and two fp32 partial-tile slots per CTA pair.
 struct SkArea {
     uint32_t *flags;
     float *slots;
@@ -278,7 +278,7 @@ SkArea take_sk_area(Carve &c) {
     SkArea a;
     a.flags = c.take<uint32_t>((size_t)kSkFlagWords);
     // 32-byte stores into the slots: align within the (16-byte aligned) workspace
-    char *raw = c.take<char>((size_t)kSkPairs * (size_t)kSlotFloats * sizeof(float) + 32);
+    char *raw = c.take<char>((size_t)kSkPairs * 2 * (size_t)kSlotFloats * sizeof(float) + 32);
     a.slots = raw ? reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(raw) + 31) & ~uintptr_t(31)) : nullptr;
     return a;
 }
@@ -701,7 +701,9 @@ int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lo
         SegWalk sw = seg_walk(pl, q);
         PairSeg w;
         while (seg_next(prm, pl, sw, w)) {
-            if (n + 8 > cap) return -1;
+            if (n + 9 > cap) return -1;
+            // the same head / contributor computation as the kernel's epilogue
+            const int64_t h = w.role == kSegPart ? head_pair(pl, q, w.t) : q;
             out[n++] = q;
             out[n++] = w.t;
             out[n++] = w.m0;
@@ -709,10 +711,11 @@ int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lo
             out[n++] = w.kbeg;
             out[n++] = w.nk;
             out[n++] = w.role;
-            out[n++] = w.role == kSegHead ? head_contrib_end(pl, q, w.t) : -1;
+            out[n++] = h;
+            out[n++] = w.role == kSegFull ? 1 : head_contrib_end(pl, h, w.t) - h;
         }
     }
-    return (n - 4) / 8;
+    return (n - 4) / 9;
 }
 
 const char *qlora_last_error(void) { return t_last_error.c_str(); }

@@ -366,16 +366,16 @@ def qlora_version() -> str:
 def qlora_debug_gemm_segments(M: int, Nd: int, nk_main: int, lora_steps: int, pairs_resident: int):
     """The fused GEMM's work schedule (host computation, no GPU): returns
     (tile_rows, dp_tiles, pairs, tiles, records), records an int64 array of
-    rows (pair, tile, row0, col0, kbeg, nk, role, contrib_end); see the C
-    header for the fields. Raises QloraError(QLORA_ERR_SHAPE) on bad input."""
+    rows (pair, tile, row0, col0, kbeg, nk, role, head, contributors); see the
+    C header for the fields. Raises QloraError(QLORA_ERR_SHAPE) on bad input."""
     import numpy as np
-    cap = 4 + 8 * 4096
+    cap = 4 + 9 * 4096
     while True:
         out = np.zeros(cap, np.int64)
         n = lib().qlora_debug_gemm_segments(int(M), int(Nd), int(nk_main), int(lora_steps), int(pairs_resident),
                                             out.ctypes.data, cap)
         if n >= 0:
-            return int(out[0]), int(out[1]), int(out[2]), int(out[3]), out[4:4 + 8 * n].reshape(n, 8).copy()
+            return int(out[0]), int(out[1]), int(out[2]), int(out[3]), out[4:4 + 9 * n].reshape(n, 9).copy()
         if n != -1:
             raise QloraError(2, "qlora_debug_gemm_segments: invalid arguments")
         cap *= 4

@@ -59,7 +59,10 @@
  *    a wait that runs out sets a device error word, which
  *    qlora_check_device_status() reports as QLORA_ERR_TIMEOUT.
  *  - The calls keep no state between calls and may run concurrently on
- *    different streams when their buffers do not overlap.
+ *    different streams when their buffers do not overlap. No kernel waits
+ *    for a thread block that may not be resident: work shared between thread
+ *    blocks outside a cluster is finished by whichever contributor arrives
+ *    last, so concurrent calls progress however the GPU divides its SMs.
  *  - Alignment: every device pointer must be 16-byte aligned.
  */
 #ifndef QLORA_B300_H
@@ -348,11 +351,13 @@ const char *qlora_version(void);
  * ceil(r / 64)) on a device holding `pairs_resident` (1..74) CTA pairs at
  * once. Writes to out[0..3] the tile height in rows (512 or 256), the number
  * of tiles run data-parallel, the pairs launched and the number of tiles T;
- * then one record of 8 values per segment, pair by pair in the order each pair
+ * then one record of 9 values per segment, pair by pair in the order each pair
  * runs them: pair, tile, first output row, first output column, first k-step,
- * k-steps, role (0 whole tile, 1 head: the pair finishes the tile, 2 tail: the
- * pair's fp32 partial goes to its slot) and, for a head, one past the last
- * pair whose tail it adds (-1 otherwise). Returns the number of records, -1
+ * k-steps, role (0 whole tile, 1 head: the tile's first k-steps, 2 tail: a
+ * later part of the tile), the tile's head pair h and its number of
+ * contributors n (pairs h .. h + n - 1; h = pair and n = 1 for a whole tile).
+ * Of a shared tile's contributors, whichever arrives last adds the others'
+ * fp32 partials and writes the output. Returns the number of records, -1
  * when `cap` (values available in out) is too small, -2 for invalid
  * arguments.
  * Tiles are 256 output columns wide; a tile's k-steps are the main steps then

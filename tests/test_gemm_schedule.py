@@ -1,14 +1,17 @@
 """The fused GEMM's work schedule, checked on the host (no GPU).
 
 The tensor-core GEMM runs on a persistent grid of CTA pairs: whole output
-tiles data-parallel, then a stream-K line in which a pair starting inside a
-tile computes its tail (an fp32 partial) and the pair holding the tile's first
-k-steps finishes it with the following pairs' tails. The kernel's four roles
-(TMA producer, MMA issuer, decoders, epilogue) walk the same segments; the
-library exports a host enumeration built from those very functions. A wrong
-schedule would drop or double a k-step (wrong output) or make a finishing
-pair wait for a tail nobody writes (a bounded wait that runs out), so the
-invariants are checked here over many shapes and pair counts.
+tiles data-parallel, then a stream-K line in which the pairs sharing a tile
+(its head, holding the first k-steps, and the pairs whose ranges start inside
+it) each compute an fp32 partial, and whichever arrives last adds the others'
+in pair order and writes the output. The kernel's four roles (TMA producer,
+MMA issuer, decoders, epilogue) walk the same segments; the library exports a
+host enumeration built from those very functions, with each segment's head
+pair and contributor count as the epilogue computes them. A wrong schedule
+would drop or double a k-step (wrong output), name a contributor that writes
+no partial (a bounded wait that runs out), or share a tile among more pairs
+than the epilogue's finishing ring holds, so the invariants are checked here
+over many shapes and pair counts.
 """
 import numpy as np
 import pytest
@@ -32,15 +35,19 @@ def check(M, Nd, nk_main, lora_steps, P_res):
     origin = {}
     first_sk, last = {}, {}
     by_pair = {}
-    for q, t, m0, c0, kb, nk, role, ce in rec.tolist():
+    contrib = {}
+    for q, t, m0, c0, kb, nk, role, h, n in rec.tolist():
         assert 0 <= q < P and 0 <= t < T and nk >= 1 and 0 <= kb and kb + nk <= S
         assert m0 % tile_rows == 0 and 0 <= m0 < M and c0 % BN == 0 and 0 <= c0 < Nd
         # one (row, column) origin per tile, and no two tiles share one
         assert origin.setdefault(t, (m0, c0)) == (m0, c0)
         cover[t, kb:kb + nk] += 1
-        by_pair.setdefault(q, []).append((t, kb, nk, role, ce))
+        by_pair.setdefault(q, []).append((t, kb, nk, role, h, n))
         full = kb == 0 and nk == S
         assert role == (0 if full else (1 if kb == 0 else 2))
+        assert (h, n) == (q, 1) if full else (h <= q < h + n and n >= 2)
+        assert (role == 1) == (not full and h == q)
+        contrib.setdefault(t, []).append((q, kb, nk, h, n))
     assert len(set(origin.values())) == T
     assert (cover == 1).all(), "every k-step of every tile exactly once"
     for q, segs in by_pair.items():
@@ -56,25 +63,20 @@ def check(M, Nd, nk_main, lora_steps, P_res):
                 assert i == len(sk) - 1, "a head is the pair's last segment"
         first_sk[q] = sk[0] if sk else None
         last[q] = segs[-1]
-    # each head's contributors hold exactly the rest of its tile, as tails
+    # a shared tile's contributors are pairs h .. h + n - 1, in k order, each
+    # agreeing on (h, n); at most four share a tile (the epilogue's finishing
+    # ring holds the pieces of up to six others)
     n_heads = 0
-    for q, (t, kb, nk, role, ce) in last.items():
-        if role != 1:
+    for t, segs in contrib.items():
+        if len(segs) == 1 and segs[0][2] == S:
             continue
         n_heads += 1
-        assert q + 1 < ce <= P
-        pieces = [(kb, nk)]
-        for c in range(q + 1, ce):
-            tc, kbc, nkc, rolec, _ = first_sk[c]
-            assert tc == t and rolec == 2
-            pieces.append((kbc, nkc))
-        pieces.sort()
-        assert pieces[0][0] == 0 and sum(p[1] for p in pieces) == S
-        assert all(a[0] + a[1] == b[0] for a, b in zip(pieces, pieces[1:]))
-    # every tail is consumed by some head
-    for c, s in first_sk.items():
-        if s is not None and s[3] == 2:
-            assert any(last[q][3] == 1 and last[q][0] == s[0] and q < c < last[q][4] for q in last)
+        segs.sort()
+        h, n = segs[0][3], segs[0][4]
+        assert all((s[3], s[4]) == (h, n) for s in segs)
+        assert [s[0] for s in segs] == list(range(h, h + n)), "contributors are consecutive pairs"
+        assert segs[0][1] == 0 and all(a[1] + a[2] == b[1] for a, b in zip(segs, segs[1:]))
+        assert 2 <= n <= 4
     return tile_rows, dpt, P, T, n_heads
 
 
