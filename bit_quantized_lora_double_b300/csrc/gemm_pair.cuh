@@ -189,7 +189,9 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64
 enum { kSegFull = 0, kSegHead = 1, kSegPart = 2 };
 
 struct PairSeg {
-    int64_t t, m0, c0;
+    int64_t t, m0;
+    int64_t c0;     // first output column, within the column group's projection
+    int cg;         // column group (forward: the projection)
     int64_t kbeg;   // first main k-step
     int64_t nmain;  // main k-steps
     int64_t lbeg;   // first LoRA k-step
@@ -285,7 +287,11 @@ __host__ __device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const Pa
     const int64_t rows_in = min64(kRowBand, pl.mt - band * kRowBand);
     const int64_t rb = w.t - band * kRowBand * pl.nt;
     w.m0 = (band * kRowBand + rb % rows_in) * p.tile_rows;
-    w.c0 = (rb / rows_in) * PairCfg::BN;
+    const int64_t ct = rb / rows_in;  // column tile of the launch
+    int cg = 0;
+    while (cg + 1 < p.ncg && ct >= p.cg_first[cg + 1]) ++cg;
+    w.cg = cg;
+    w.c0 = (ct - p.cg_first[cg]) * PairCfg::BN;
     w.kbeg = k0;
     w.nmain = max64(0, min64(k1, p.nk_main) - k0);
     w.lbeg = max64(k0, p.nk_main) - p.nk_main;
@@ -338,9 +344,7 @@ __device__ __forceinline__ bool flag_wait(const uint32_t *f, uint64_t limit_ns, 
 // pairs' schedule.
 template <int MODE>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
-    k_gemm_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
-                const __grid_constant__ CUtensorMap tm_lact, const __grid_constant__ CUtensorMap tm_lw,
-                const __grid_constant__ CUtensorMap tm_out, const TcParams p) {
+    k_gemm_pair(const __grid_constant__ GemmMaps tm, const TcParams p) {
     using C = PairCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -385,11 +389,14 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         tmem_relinquish2();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tm_act);
-        prefetch_tmap(&tm_codes);
-        prefetch_tmap(&tm_lact);
-        prefetch_tmap(&tm_lw);
-        if (p.out_v4) prefetch_tmap(&tm_out);
+        const int nw = p.ncg > p.nkg ? p.ncg : p.nkg;
+        for (int g = 0; g < p.nkg; ++g) prefetch_tmap(&tm.act[g]);
+        for (int g = 0; g < nw; ++g) prefetch_tmap(&tm.codes[g]);
+        prefetch_tmap(&tm.lact);
+        for (int g = 0; g < p.ncg; ++g) {
+            prefetch_tmap(&tm.lw[g]);
+            if (p.pj[g].out_v4) prefetch_tmap(&tm.out[g]);
+        }
         // the first steps' activation and code tiles into L2 while the
         // preceding kernel finishes (L2 stays coherent with its writes)
         SegWalk sw = seg_walk(pl, pair_id);
@@ -398,13 +405,15 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             const int64_t rowA0 = w.m0 + (int64_t)rank * C::SUB;
             const int64_t ch = w.c0 + (int64_t)rank * C::HN;
             for (int64_t it = 0; it < w.nmain && it < C::STAGES; ++it) {
-                const int32_t k = (int32_t)((w.kbeg + it) * C::BK);
-                tma_prefetch_2d(&tm_act, k, (int32_t)rowA0);
-                if (w.two) tma_prefetch_2d(&tm_act, k, (int32_t)(rowA0 + 256));
+                const int64_t kk = w.kbeg + it;
+                const int kg = MODE == kFwd ? 0 : kgroup_of(p, kk);
+                const int32_t k = (int32_t)((kk - p.kg_first[kg]) * C::BK);
+                tma_prefetch_2d(&tm.act[kg], k, (int32_t)rowA0);
+                if (w.two) tma_prefetch_2d(&tm.act[kg], k, (int32_t)(rowA0 + 256));
                 if (MODE == kFwd)
-                    tma_prefetch_2d(&tm_codes, k / 2, (int32_t)ch);
+                    tma_prefetch_2d(&tm.codes[w.cg], k / 2, (int32_t)ch);
                 else
-                    tma_prefetch_2d(&tm_codes, (int32_t)(ch / 2), k);
+                    tma_prefetch_2d(&tm.codes[kg], (int32_t)(ch / 2), k);
             }
         }
     }
@@ -437,24 +446,27 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                     }
                     if (it < w.nmain) {
                         mbar_arrive_expect_tx(&full[s], abytes + C::C_BYTES);
-                        const int32_t k = (int32_t)((w.kbeg + it) * C::BK);
-                        tma_load_2d(atile(s, 0), &tm_act, &full[s], k, (int32_t)rowA0);
-                        if (w.two) tma_load_2d(atile(s, 1), &tm_act, &full[s], k, (int32_t)rowA1);
+                        const int64_t kk = w.kbeg + it;
+                        const int kg = MODE == kFwd ? 0 : kgroup_of(p, kk);
+                        const int32_t k = (int32_t)((kk - p.kg_first[kg]) * C::BK);
+                        tma_load_2d(atile(s, 0), &tm.act[kg], &full[s], k, (int32_t)rowA0);
+                        if (w.two) tma_load_2d(atile(s, 1), &tm.act[kg], &full[s], k, (int32_t)rowA1);
                         if (MODE == kFwd)
-                            tma_load_2d(ctile(s), &tm_codes, &full[s], k / 2, (int32_t)ch);
+                            tma_load_2d(ctile(s), &tm.codes[w.cg], &full[s], k / 2, (int32_t)ch);
                         else
-                            tma_load_2d(ctile(s), &tm_codes, &full[s], (int32_t)(ch / 2), k);
+                            tma_load_2d(ctile(s), &tm.codes[kg], &full[s], (int32_t)(ch / 2), k);
                     } else {
                         const int32_t j = (int32_t)(w.lbeg + it - w.nmain) * C::BK;
+                        const int32_t jl = p.pj[w.cg].lcol + j;  // column of the LoRA activations
                         mbar_arrive_expect_tx(&full[s], abytes + C::W_BYTES);
-                        tma_load_2d(atile(s, 0), &tm_lact, &full[s], j, (int32_t)rowA0);
-                        if (w.two) tma_load_2d(atile(s, 1), &tm_lact, &full[s], j, (int32_t)rowA1);
+                        tma_load_2d(atile(s, 0), &tm.lact, &full[s], jl, (int32_t)rowA0);
+                        if (w.two) tma_load_2d(atile(s, 1), &tm.lact, &full[s], jl, (int32_t)rowA1);
                         if (MODE == kFwd) {
-                            tma_load_2d(wtile(s), &tm_lw, &full[s], j, (int32_t)ch);
+                            tma_load_2d(wtile(s), &tm.lw[w.cg], &full[s], j, (int32_t)ch);
                         } else {
 #pragma unroll
                             for (int b = 0; b < 2; ++b)
-                                tma_load_2d(wtile(s) + b * 8192, &tm_lw, &full[s], (int32_t)(ch + 64 * b), j);
+                                tma_load_2d(wtile(s) + b * 8192, &tm.lw[0], &full[s], (int32_t)(ch + 64 * b), j);
                         }
                     }
                 }
@@ -517,7 +529,6 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         const int dw = warp - 2;
         const int grp = dw / C::GROUP_WARPS;
         const int dt = (dw % C::GROUP_WARPS) * 32 + lane;  // 0..127 within the group
-        const float mean = p.absmax ? 0.0f : *p.mean;
         const int64_t kblocks = p.w_cols / kBlock;
         const uint32_t ready_addr0 = mapa_u32(smem_u32(ready), 0);
         uint32_t dst[8], csrc[2];
@@ -548,6 +559,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         struct Cursor {
             SegWalk sw;
             bool live;
+            int cg;
             int64_t it, g, nk, nmain, kbeg, c0;
         };
         auto enter = [&](Cursor &c) {
@@ -558,26 +570,35 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             c.nmain = w.nmain;
             c.kbeg = w.kbeg;
             c.c0 = w.c0;
+            c.cg = w.cg;
         };
         auto advance = [&](Cursor &c) {
             ++c.it;
             ++c.g;
             if (c.live && c.it >= c.nk) enter(c);
         };
-        auto fetch = [&](const Cursor &c, int &qv, float &sv) {
+        // The block's reconstructed absmax is a' = fp32(qv) * sv + mv: the
+        // double-quantized code, its group scale and the weight's mean, or
+        // (0, 0, a) for an fp32 absmax a (0 * 0 + a is exactly a).
+        auto fetch = [&](const Cursor &c, int &qv, float &sv, float &mv) {
             qv = 0;
             sv = 0.0f;
+            mv = 0.0f;
             if (!c.live || c.it >= c.nmain) return false;
             const int64_t ch = c.c0 + (int64_t)rank * C::HN;
-            const int64_t wrow = MODE == kFwd ? ch + dt : (c.kbeg + c.it) * C::BK + nl;
-            const int64_t kb = MODE == kFwd ? c.kbeg + c.it : ch / kBlock + b2;
-            if (wrow >= p.w_rows || kb >= kblocks) return false;
+            const int64_t kk = c.kbeg + c.it;
+            const int kg = MODE == kFwd ? 0 : kgroup_of(p, kk);
+            const TcProj &pw = p.pj[MODE == kFwd ? c.cg : kg];
+            const int64_t wrow = MODE == kFwd ? ch + dt : (kk - p.kg_first[kg]) * C::BK + nl;
+            const int64_t kb = MODE == kFwd ? kk : ch / kBlock + b2;
+            if (wrow >= pw.rows || kb >= kblocks) return false;
             const int64_t bidx = wrow * kblocks + kb;
-            if (p.absmax) {
-                sv = __ldg(p.absmax + bidx);
+            if (pw.absmax) {
+                mv = __ldg(pw.absmax + bidx);
             } else {
-                qv = __ldg(p.q + bidx);
-                sv = __ldg(p.s2 + (bidx >> 8));
+                qv = __ldg(pw.q + bidx);
+                sv = __ldg(pw.s2 + (bidx >> 8));
+                mv = __ldg(pw.mean);
             }
             return true;
         };
@@ -589,10 +610,10 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         Cursor nxt = cur;
         for (int i = 0; i < C::DEC_GROUPS; ++i) advance(nxt);
         int qv, qn;
-        float sv, sn;
-        bool valid = fetch(cur, qv, sv);
+        float sv, sn, mv, mn;
+        bool valid = fetch(cur, qv, sv, mv);
         while (cur.live) {
-            const bool valid_n = fetch(nxt, qn, sn);
+            const bool valid_n = fetch(nxt, qn, sn, mn);
             const int s = (int)(cur.g % C::STAGES);
             const uint32_t par = (uint32_t)(cur.g / C::STAGES) & 1;
             if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) break;
@@ -601,7 +622,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 const uint8_t *ct = ctile(s);
                 uint32_t o[8][4];
                 if (valid) {
-                    const Nf4Table tab = make_table(p.absmax ? sv : dq_absmax((int8_t)qv, sv, mean), p.tab);
+                    const Nf4Table tab = make_table(dq_absmax((int8_t)qv, sv, mv), p.tab);
                     uint4 cw[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) cw[h] = *reinterpret_cast<const uint4 *>(ct + csrc[h]);
@@ -622,6 +643,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             cur = nxt;
             qv = qn;
             sv = sn;
+            mv = mn;
             valid = valid_n;
             for (int i = 0; i < C::DEC_GROUPS; ++i) advance(nxt);
         }
@@ -807,8 +829,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         __syncwarp();  // every lane has read the buffers before they are refilled
                         for (int qi = 0; qi < nq; ++qi) fetch_piece(b * nq + qi + C::NFIX);
                     }
-                    const int64_t ncol = p.Nd - (w.c0 + col);  // valid columns from here
-                    if (p.out_v4) {
+                    const TcProj &po = p.pj[w.cg];
+                    const int64_t ncol = po.ncols - (w.c0 + col);  // valid columns from here
+                    if (po.out_v4) {
                         // the previous batch's store has read the staging tile
                         if (lane == 0) bulk_wait_read<0>();
                         __syncwarp();
@@ -828,13 +851,13 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         // one TMA store of the 32 x 64 box; rows and columns
                         // past the output's edge are clipped by the unit
                         if (lane == 0 && rbase < p.M) {
-                            tma_store_2d(&tm_out, stg, (int32_t)(w.c0 + col), (int32_t)rbase);
+                            tma_store_2d(&tm.out[w.cg], stg, (int32_t)(w.c0 + col), (int32_t)rbase);
                             bulk_commit();
                         }
                         continue;
                     }
                     if (row >= p.M) continue;
-                    uint16_t *dstp = p.out + row * p.ldo + w.c0 + col;
+                    uint16_t *dstp = po.out + row * po.ldo + w.c0 + col;
 #pragma unroll
                     for (int e = 0; e < 64; ++e)
                         if (e < ncol) dstp[e] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[e])));

@@ -31,21 +31,41 @@ constexpr int kSkReadyWords = kSkPairs * 16;
 constexpr int kSkFlagWords = kSkPairs * 24;
 constexpr int64_t kSlotFloats = 512 * 256;
 
-struct TcParams {
-    int64_t M;        // rows of the output
-    int64_t Nd;       // columns of the output (N for forward, K for dX)
-    int64_t w_rows;   // N
-    int64_t w_cols;   // K
-    int64_t nk_main;  // main k-steps (K/64 forward, ceil(N/64) dX)
-    int lora_steps;   // ceil(r / 64)
-    int r;
+// Projections of one launch (a group: weights sharing the activation X).
+// Forward: the output column tiles of the projections follow one another
+// (projection g owns column tiles [cg_first[g], cg_first[g + 1]) of the
+// launch), each tile computing Y_g = X W_g'^T + (sU_g) B_g^T. dX: the
+// contraction runs over the projections' rows one after another (projection g
+// owns main k-steps [kg_first[g], kg_first[g + 1])), so the launch computes
+// dX = sum_g dY_g W_g' + (sV) A over all of them.
+constexpr int kMaxGroup = 4;
+
+struct TcProj {
     const int8_t *q;
     const float *s2;
     const float *mean;
     const float *absmax;   // per-block fp32 absmax in place of q, s2, mean (null: double-quantized)
-    int tab;               // level table (kTableNF4 / kTableINT4)
-    uint16_t *out;
+    int64_t rows;          // N_g: rows of W_g
+    uint16_t *out;         // forward: Y_g; dX: dX (projection 0 only)
     int64_t ldo;
+    int64_t ncols;         // valid output columns (forward N_g, dX K)
+    int lcol;              // forward: first column of s*U_g in the LoRA activation tensor
+    int out_v4;            // out is 16-byte aligned and ldo % 8 == 0: stores through the output tensor map
+};
+
+struct TcParams {
+    int64_t M;        // rows of the output
+    int64_t Nd;       // columns of the launch's output (forward: 256 x column tiles of all projections; dX: K)
+    int64_t w_cols;   // K
+    int64_t nk_main;  // main k-steps (forward K/64; dX the sum of ceil(N_g/64))
+    int lora_steps;   // ceil(r / 64)
+    int r;            // width of the LoRA contraction (forward r; dX r x projections)
+    int tab;          // level table (kTableNF4 / kTableINT4)
+    int ncg;          // column groups: forward the projections, dX 1
+    int nkg;          // k groups: dX the projections, forward 1
+    int64_t cg_first[kMaxGroup + 1];
+    int64_t kg_first[kMaxGroup + 1];
+    TcProj pj[kMaxGroup];
     // Stream-K hand-off between pairs (zeroed before the launch):
     // flags [kSkFlagWords] (ready flags, then arrival counters) and two
     // partial-tile slots of kSlotFloats fp32 per pair.
@@ -55,8 +75,26 @@ struct TcParams {
     int tile_rows;         // rows per tile: 512 (two 256-row sub-tiles) or 256 (one)
     uint64_t wait_ns;
     unsigned kernel_id;
-    int out_v4;            // out is 16-byte aligned and ldo % 8 == 0: stores through the output tensor map
 };
+
+// Tensor maps of one launch. Forward: act[0] = X, codes[g], lact = s*U of all
+// projections side by side, lw[g] = B_g, out[g] = Y_g. dX: act[g] = dY_g,
+// codes[g], lact = s*V of all projections side by side, lw[0] = A of all
+// projections stacked, out[0] = dX.
+struct GemmMaps {
+    CUtensorMap act[kMaxGroup];
+    CUtensorMap codes[kMaxGroup];
+    CUtensorMap lact;
+    CUtensorMap lw[kMaxGroup];
+    CUtensorMap out[kMaxGroup];
+};
+
+// The k group of main k-step kk.
+__host__ __device__ __forceinline__ int kgroup_of(const TcParams &p, int64_t kk) {
+    int g = 0;
+    while (g + 1 < p.nkg && kk >= p.kg_first[g + 1]) ++g;
+    return g;
+}
 
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;

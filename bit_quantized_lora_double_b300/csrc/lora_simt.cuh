@@ -255,4 +255,29 @@ __global__ void __launch_bounds__(256) k_dx_simt(const uint16_t *__restrict__ dY
     }
 }
 
+// out = bf16(part_0 + part_1 + ... + part_{n-1}) element by element, the sum
+// in fp32 in part order; parts are n consecutive bf16 arrays of `count`
+// elements (count % 8 == 0, 16-byte aligned). Sums the per-projection dX of a
+// projection group on its CUDA-core path.
+__global__ void k_sum_parts(const uint16_t *__restrict__ parts, int n, int64_t count, uint16_t *__restrict__ out) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (i >= count) return;
+    float acc[8];
+    for (int g = 0; g < n; ++g) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(parts + (int64_t)g * count + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float x = __uint_as_float((w[e >> 1] >> (16 * (e & 1))) << 16);
+            acc[e] = g == 0 ? x : acc[e] + x;
+        }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4 *>(out + i) = o;
+}
+
 }  // namespace qlora

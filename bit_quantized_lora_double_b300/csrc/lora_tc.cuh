@@ -33,7 +33,8 @@ namespace qlora {
 //   kRedV:  sV [rows, ldb] bf16 = bf16(s * sum)
 //   kRedDA: dA [r, rows] fp32 = sum (element [j, row])
 //   kRedDB: dB [rows, r] fp32 = s * sum
-// For kRedU and kRedV, columns [r, ldb) of sU / sV are written as zeros.
+// For kRedU and kRedV, columns [r, zend) of sU / sV are written as zeros
+// (zend <= ldb).
 enum { kRedU = 0, kRedV = 1, kRedDA = 2, kRedDB = 3 };
 
 #ifndef QLORA_SK_STAGES
@@ -65,6 +66,7 @@ struct SkParams {
     int lda;
     uint16_t *o16b;
     int ldb;
+    int zend;
     float *o32;
     uint64_t wait_ns;
     unsigned kernel_id;
@@ -121,7 +123,7 @@ __device__ __forceinline__ void sk_store(const SkParams &p, int64_t row, int jba
                 }
             }
             if (last_z)
-                for (int jj = p.r; jj < p.ldb; ++jj) p.o16b[row * p.ldb + jj] = 0;
+                for (int jj = p.r; jj < p.zend; ++jj) p.o16b[row * p.ldb + jj] = 0;
             break;
         }
         case kRedDA:
@@ -139,7 +141,7 @@ __device__ __forceinline__ void sk_store(const SkParams &p, int64_t row, int jba
 
 // Writes row `row`, columns j0 .. j0 + nv - 1 (nv <= 4) of the tile's
 // complete sum, v holding those values in order; `pad` also writes the zero
-// columns [r, ldb) of sU / sV for that row.
+// columns [r, zend) of sU / sV for that row.
 __device__ __forceinline__ void sk_store4(const SkParams &p, int64_t row, int j0, int nv, float4 v, bool pad) {
     const float a[4] = {v.x, v.y, v.z, v.w};
     switch (p.mode) {
@@ -154,7 +156,7 @@ __device__ __forceinline__ void sk_store4(const SkParams &p, int64_t row, int j0
                 }
             }
             if (pad)
-                for (int jj = p.r; jj < p.ldb; ++jj) p.o16b[row * p.ldb + jj] = 0;
+                for (int jj = p.r; jj < p.zend; ++jj) p.o16b[row * p.ldb + jj] = 0;
             break;
         }
         case kRedDA:

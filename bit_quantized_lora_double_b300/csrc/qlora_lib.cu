@@ -503,16 +503,17 @@ int64_t gemm_schedule(TcParams &prm, int64_t P) {
 // more than the device holds at once) on the schedule above, launched as a
 // programmatic dependent of the preceding kernel.
 template <int MODE>
-qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUtensorMap &tl, const CUtensorMap &tw,
-                         TcParams prm, cudaStream_t s) {
+qlora_status launch_gemm(GemmMaps &tm, TcParams prm, cudaStream_t s) {
     // output tiles leave through a tensor map (32 x 64 boxes, 128-byte
     // swizzle) when its row pitch and base allow one
-    CUtensorMap to;
-    memset(&to, 0, sizeof to);
-    if (prm.out_v4) {
-        const qlora_status st = make_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, prm.out, prm.Nd, prm.M,
-                                         prm.ldo * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B, "output");
-        if (st) return st;
+    for (int g = 0; g < prm.ncg; ++g) {
+        TcProj &o = prm.pj[g];
+        o.out_v4 = (reinterpret_cast<uintptr_t>(o.out) & 15) == 0 && (o.ldo & 7) == 0;
+        if (o.out_v4) {
+            const qlora_status st = make_map(&tm.out[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o.out, o.ncols, prm.M,
+                                             o.ldo * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B, "output");
+            if (st) return st;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -532,7 +533,7 @@ qlora_status launch_gemm(const CUtensorMap &ta, const CUtensorMap &tc, const CUt
     cudaError_t e;
     {
         ProfScope ps(MODE == kFwd ? QLORA_KERNEL_FWD_GEMM : QLORA_KERNEL_DX_GEMM, s);
-        e = cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE>, ta, tc, tl, tw, to, prm);
+        e = cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE>, tm, prm);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -555,6 +556,7 @@ struct SkJob {
     uint16_t *o16b;
     int ldb;
     float *o32;
+    int zend = -1;  // zero columns [r, zend) of o16b (-1: up to ldb)
 };
 
 SkParams sk_params(const SkJob &j, int r, unsigned id) {
@@ -570,6 +572,7 @@ SkParams sk_params(const SkJob &j, int r, unsigned id) {
     prm.lda = j.lda;
     prm.o16b = j.o16b;
     prm.ldb = j.ldb;
+    prm.zend = j.zend < 0 ? j.ldb : j.zend;
     prm.o32 = j.o32;
     prm.wait_ns = wait_ns();
     prm.kernel_id = id;
@@ -673,6 +676,28 @@ qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsig
     return launch_check("k_lora_skinny");
 }
 
+// Runs same-kind skinny problems, two per launch where their contraction
+// lengths agree; the first launch zeroes `zero` (the stream-K flags).
+template <int A_MN, int B_MN>
+qlora_status run_skinny_list(SkJob *jobs, int nj, int r, cudaStream_t s, unsigned id, uint32_t *zero,
+                                    int nzero) {
+    bool done[kMaxGroup] = {};
+    for (int i = 0; i < nj; ++i) {
+        if (done[i]) continue;
+        done[i] = true;
+        int mate = -1;
+        for (int j = i + 1; j < nj && mate < 0; ++j)
+            if (!done[j] && jobs[j].pl.L == jobs[i].pl.L && jobs[j].pl.zt == jobs[i].pl.zt) mate = j;
+        if (mate >= 0) done[mate] = true;
+        const qlora_status st =
+            run_skinny<A_MN, B_MN>(jobs[i], mate >= 0 ? &jobs[mate] : nullptr, r, s, id, zero, nzero);
+        if (st) return st;
+        zero = nullptr;
+        nzero = 0;
+    }
+    return QLORA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -690,6 +715,9 @@ int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lo
     prm.Nd = Nd;
     prm.nk_main = nk_main;
     prm.lora_steps = lora_steps;
+    prm.ncg = prm.nkg = 1;
+    prm.cg_first[1] = cdiv(Nd, PairCfg::BN);
+    prm.kg_first[1] = nk_main;
     const int64_t pairs = gemm_schedule(prm, pairs_resident);
     const PairPlan pl = make_plan(prm, pairs);
     out[0] = prm.tile_rows;
@@ -1003,9 +1031,10 @@ static qlora_status check_linear_common(int64_t M, const Wt &w, const void *A, c
     return QLORA_OK;
 }
 
+// ldu: row pitch (elements) of U_save; r for the single-layer entry points.
 static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const void *A, const void *B, int r,
                                     float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
-                                    qlora_stream_t stream) {
+                                    qlora_stream_t stream, int ldu) {
     qlora_status st = check_linear_common(M, w, A, B, r, ws);
     if (st) return st;
     if (M > 0 && (!X || !Y)) return fail(QLORA_ERR_NULL, "X or Y is NULL");
@@ -1034,7 +1063,7 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
             k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r,
-                                                                 scale, U16, r, f.sU, rp, f.few_counters,
+                                                                 scale, U16, ldu, f.sU, rp, f.few_counters,
                                                                  (int)fp.groups);
         }
         if ((st = launch_check("k_lora_down"))) return st;
@@ -1098,7 +1127,7 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         {
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
             k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r, scale,
-                                                              U16, r, f.sU, rp);
+                                                              U16, ldu, f.sU, rp);
         }
         if ((st = launch_check("k_lora_down"))) return st;
         CUtensorMap tmC;
@@ -1148,50 +1177,51 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         if ((st = launch_check("k_pad_cols(B)"))) return st;
         Bl = f.Bp;
     }
-    CUtensorMap tmX, tmC, tmU, tmB, tmA;
+    GemmMaps gm;
+    memset(&gm, 0, sizeof gm);
+    CUtensorMap &tmX = gm.act[0];
+    CUtensorMap tmA;
     if ((st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
         (st = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, r, K * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
-        (st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 32, 128,
+        (st = make_map(&gm.codes[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 32, 128,
                        CU_TENSOR_MAP_SWIZZLE_32B, "codes")) ||
-        (st = make_map(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rs, M, rs * 2, 64, 128,
+        (st = make_map(&gm.lact, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.sU, rs, M, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "sU")) ||
-        (st = make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bl, rs, N, rs * 2, 64, 128,
+        (st = make_map(&gm.lw[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bl, rs, N, rs * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B, "B")))
         return st;
     // U = X A^T on the tensor cores; U (bf16) to U_save, s*U (bf16) to the workspace
     const SkPlan pu = sk_plan(M, K, r);
-    if ((st = run_skinny<0, 0>(SkJob{&tmX, &tmA, pu, kRedU, scale, U16, r, f.sU, rs, nullptr}, nullptr, r, s, 3,
+    if ((st = run_skinny<0, 0>(SkJob{&tmX, &tmA, pu, kRedU, scale, U16, ldu, f.sU, rs, nullptr}, nullptr, r, s, 3,
                                f.sk.flags, kSkFlagWords)))
         return st;
     TcParams prm{};
     prm.M = M;
     prm.Nd = N;
-    prm.w_rows = N;
     prm.w_cols = K;
     prm.nk_main = K / kGemmBK;
     prm.lora_steps = rp / 64;
     prm.r = r;
-    prm.q = w.q;
-    prm.s2 = w.s2;
-    prm.mean = w.mean;
-    prm.absmax = w.absmax;
     prm.tab = w.tab;
-    prm.out = static_cast<uint16_t *>(Y);
-    prm.ldo = N;
-    prm.out_v4 = (reinterpret_cast<uintptr_t>(Y) & 15) == 0 && (N & 7) == 0;
+    prm.ncg = prm.nkg = 1;
+    prm.cg_first[1] = cdiv(N, PairCfg::BN);
+    prm.kg_first[1] = prm.nk_main;
+    prm.pj[0] = TcProj{w.q, w.s2, w.mean, w.absmax, N, static_cast<uint16_t *>(Y), N, N, 0, 0};
     prm.flags = f.sk.flags;
     prm.slots = f.sk.slots;
     prm.wait_ns = wait_ns();
     prm.kernel_id = 1;
-    if ((st = launch_gemm<kFwd>(tmX, tmC, tmU, tmB, prm, s))) return st;
+    if ((st = launch_gemm<kFwd>(gm, prm, s))) return st;
     return ok();
 }
 
+// ldu: row pitch (elements) of U_saved; r for the single-layer entry points
+// (any multiple of 8 when r % 8 == 0).
 static qlora_status linear_bwd_impl(const void *dY, const void *X, const void *U_saved, int64_t M, const Wt &w,
                                     const void *A, const void *B, int r, float scale, void *dX, float *dA, float *dB,
-                                    void *ws, size_t ws_bytes, qlora_stream_t stream) {
+                                    void *ws, size_t ws_bytes, qlora_stream_t stream, int ldu_saved) {
     qlora_status st = check_linear_common(M, w, A, B, r, ws);
     if (st) return st;
     if (!dA || !dB) return fail(QLORA_ERR_NULL, "dA or dB is NULL");
@@ -1229,7 +1259,7 @@ static qlora_status linear_bwd_impl(const void *dY, const void *X, const void *U
         }
         if ((st = launch_check("k_lora_down(V)"))) return st;
         const uint16_t *U = static_cast<const uint16_t *>(U_saved);
-        int ldu = r;
+        int ldu = ldu_saved;
         if (!U) {
             {
                 ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
@@ -1319,7 +1349,7 @@ static qlora_status linear_bwd_impl(const void *dY, const void *X, const void *U
         (st = make_map(&tmBp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bl, ldb_l, N, ldb_l * 2, 64, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B, "B")) ||
         (st = make_map(&tmUp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ul, U_saved ? ldb_l : rs, M,
-                       (U_saved ? ldb_l : rs) * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "U")))
+                       (U_saved ? (r % 8 ? rs : ldu_saved) : rs) * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "U")))
         return st;
     // V = dY B -> sV = bf16(s * V)
     const SkPlan pv = sk_plan(M, N, r);
@@ -1341,24 +1371,26 @@ static qlora_status linear_bwd_impl(const void *dY, const void *X, const void *U
     TcParams prm{};
     prm.M = M;
     prm.Nd = K;
-    prm.w_rows = N;
     prm.w_cols = K;
     prm.nk_main = cdiv(N, kGemmBK);
     prm.lora_steps = rp / 64;
     prm.r = r;
-    prm.q = w.q;
-    prm.s2 = w.s2;
-    prm.mean = w.mean;
-    prm.absmax = w.absmax;
     prm.tab = w.tab;
-    prm.out = static_cast<uint16_t *>(dX);
-    prm.ldo = K;
-    prm.out_v4 = (reinterpret_cast<uintptr_t>(dX) & 15) == 0 && (K & 7) == 0;
+    prm.ncg = prm.nkg = 1;
+    prm.cg_first[1] = cdiv(K, PairCfg::BN);
+    prm.kg_first[1] = prm.nk_main;
+    prm.pj[0] = TcProj{w.q, w.s2, w.mean, w.absmax, N, static_cast<uint16_t *>(dX), K, K, 0, 0};
     prm.flags = b.sk.flags;
     prm.slots = b.sk.slots;
     prm.wait_ns = wait_ns();
     prm.kernel_id = 2;
-    if ((st = launch_gemm<kDx>(tmD, tmC, tmV, tmA, prm, s))) return st;
+    GemmMaps gm;
+    memset(&gm, 0, sizeof gm);
+    gm.act[0] = tmD;
+    gm.codes[0] = tmC;
+    gm.lact = tmV;
+    gm.lw[0] = tmA;
+    if ((st = launch_gemm<kDx>(gm, prm, s))) return st;
     // dA = (sV)^T X (rows k of dA^T) and dB = s dY^T U (rows n), both
     // contracting over the M tokens, in one launch
     const SkJob ja{&tmXmn, &tmVmn, sk_plan(K, M, r), kRedDA, 1.0f, nullptr, 0, nullptr, 0, dA};
@@ -1371,28 +1403,363 @@ qlora_status qlora_linear_fwd(const void *X, int64_t M, const qlora_nf4_weight *
                               int r, float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
                               qlora_stream_t stream) {
     if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
-    return linear_fwd_impl(X, M, wt_of(w), A, B, r, scale, Y, U_save, ws, ws_bytes, stream);
+    return linear_fwd_impl(X, M, wt_of(w), A, B, r, scale, Y, U_save, ws, ws_bytes, stream, r);
 }
 
 qlora_status qlora_q4_linear_fwd(const void *X, int64_t M, const qlora_q4_weight *w, const void *A, const void *B,
                                  int r, float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
                                  qlora_stream_t stream) {
     if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
-    return linear_fwd_impl(X, M, wt_of(w), A, B, r, scale, Y, U_save, ws, ws_bytes, stream);
+    return linear_fwd_impl(X, M, wt_of(w), A, B, r, scale, Y, U_save, ws, ws_bytes, stream, r);
 }
 
 qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
                               const qlora_nf4_weight *w, const void *A, const void *B, int r, float scale, void *dX,
                               float *dA, float *dB, void *ws, size_t ws_bytes, qlora_stream_t stream) {
     if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
-    return linear_bwd_impl(dY, X, U_saved, M, wt_of(w), A, B, r, scale, dX, dA, dB, ws, ws_bytes, stream);
+    return linear_bwd_impl(dY, X, U_saved, M, wt_of(w), A, B, r, scale, dX, dA, dB, ws, ws_bytes, stream, r);
 }
 
 qlora_status qlora_q4_linear_bwd(const void *dY, const void *X, const void *U_saved, int64_t M,
                                  const qlora_q4_weight *w, const void *A, const void *B, int r, float scale, void *dX,
                                  float *dA, float *dB, void *ws, size_t ws_bytes, qlora_stream_t stream) {
     if (!w) return fail(QLORA_ERR_NULL, "weight descriptor is NULL");
-    return linear_bwd_impl(dY, X, U_saved, M, wt_of(w), A, B, r, scale, dX, dA, dB, ws, ws_bytes, stream);
+    return linear_bwd_impl(dY, X, U_saved, M, wt_of(w), A, B, r, scale, dX, dA, dB, ws, ws_bytes, stream, r);
+}
+
+// ---- projection groups ------------------------------------------------------
+
+static_assert(QLORA_MAX_GROUP == kMaxGroup, "group size of the ABI and of the kernels");
+
+// Validated view of a group's projections.
+struct GroupView {
+    int n;
+    int64_t K;
+    Wt w[kMaxGroup];
+};
+
+// outputs: also check the pointers the call reads or writes besides the
+// weights and adapters (not for the workspace queries).
+static qlora_status check_group(int64_t M, const qlora_proj *proj, int n, int r, bool bwd, GroupView &gv,
+                                bool outputs = true) {
+    if (!proj) return fail(QLORA_ERR_NULL, "projection list is NULL");
+    if (n < 1 || n > kMaxGroup) return fail(QLORA_ERR_SHAPE, "group of %d projections: need 1..%d", n, kMaxGroup);
+    if (r < 8 || r > 128 || r % 8) return fail(QLORA_ERR_RANK, "group rank r = %d: need 8 <= r <= 128, r %% 8 == 0", r);
+    if (M < 0 || M >= kMaxDim) return fail(QLORA_ERR_SHAPE, "M = %lld out of range", (long long)M);
+    gv.n = n;
+    for (int g = 0; g < n; ++g) {
+        const qlora_proj &pj = proj[g];
+        if (!pj.w) return fail(QLORA_ERR_NULL, "projection %d: weight descriptor is NULL", g);
+        gv.w[g] = wt_of(pj.w);
+        qlora_status st = check_weight(gv.w[g], true);
+        if (st) return st;
+        if (g == 0) gv.K = gv.w[0].cols;
+        if (gv.w[g].cols != gv.K)
+            return fail(QLORA_ERR_SHAPE, "projection %d has K = %lld, projection 0 K = %lld", g,
+                        (long long)gv.w[g].cols, (long long)gv.K);
+        if (!pj.A || !pj.B) return fail(QLORA_ERR_NULL, "projection %d: A or B is NULL", g);
+        if (!al16(pj.A) || !al16(pj.B)) return fail(QLORA_ERR_ALIGN, "projection %d: A and B must be 16-byte aligned", g);
+        if (M == 0 || !outputs) continue;
+        if (!bwd) {
+            if (!pj.Y) return fail(QLORA_ERR_NULL, "projection %d: Y is NULL", g);
+            if (!al16(pj.Y)) return fail(QLORA_ERR_ALIGN, "projection %d: Y must be 16-byte aligned", g);
+        } else {
+            if (!pj.dY) return fail(QLORA_ERR_NULL, "projection %d: dY is NULL", g);
+            if (!al16(pj.dY)) return fail(QLORA_ERR_ALIGN, "projection %d: dY must be 16-byte aligned", g);
+        }
+    }
+    if (bwd && outputs)
+        for (int g = 0; g < n; ++g) {
+            if (!proj[g].dA || !proj[g].dB) return fail(QLORA_ERR_NULL, "projection %d: dA or dB is NULL", g);
+            if (!al16(proj[g].dA) || !al16(proj[g].dB))
+                return fail(QLORA_ERR_ALIGN, "projection %d: dA and dB must be 16-byte aligned", g);
+        }
+    return QLORA_OK;
+}
+
+// The tensor-core paths of a group: forward beyond the few-token sizes,
+// backward from kTcMinM tokens with every N_g a multiple of 8. Otherwise the
+// projections run one by one through the single-layer paths.
+static bool group_tc_fwd(int64_t M) { return M > kSmallMaxM; }
+static bool group_tc_bwd(int64_t M, const GroupView &gv) {
+    if (M < kTcMinM) return false;
+    for (int g = 0; g < gv.n; ++g)
+        if (gv.w[g].rows % 8) return false;
+    return true;
+}
+
+struct GroupWs {
+    uint16_t *Acat, *sU, *sV, *U, *parts;
+    float *dAcat;
+    SkArea sk;
+    char *rest;  // per-projection workspace of the one-by-one paths
+    size_t rest_bytes;
+};
+static size_t group_ws(int64_t M, const GroupView &gv, int r, bool bwd, void *ws, size_t ws_bytes, GroupWs *out) {
+    const int n = gv.n;
+    const int64_t K = gv.K, R = (int64_t)n * r;
+    Carve c(ws);
+    GroupWs w{};
+    size_t per = 0;
+    if (!bwd && group_tc_fwd(M)) {
+        w.Acat = c.take<uint16_t>((size_t)(R * K));
+        w.sU = c.take<uint16_t>((size_t)(M * R));
+        w.sk = take_sk_area(c);
+    } else if (bwd && group_tc_bwd(M, gv)) {
+        w.Acat = c.take<uint16_t>((size_t)(R * K));
+        w.sV = c.take<uint16_t>((size_t)(M * R));
+        w.U = c.take<uint16_t>((size_t)(M * R));
+        w.dAcat = c.take<float>((size_t)(R * K));
+        w.sk = take_sk_area(c);
+    } else {
+        if (bwd) w.parts = c.take<uint16_t>((size_t)(n * M * K));
+        for (int g = 0; g < n; ++g)
+            per = std::max(per, bwd ? bwd_ws(M, gv.w[g].rows, K, r, nullptr, nullptr)
+                                    : fwd_ws(M, gv.w[g].rows, K, r, nullptr, nullptr));
+        w.rest = c.take<char>(per);
+    }
+    const size_t need = c.off;
+    w.rest_bytes = per;
+    if (out) *out = w;
+    (void)ws_bytes;
+    return need;
+}
+
+// The stacked A_g [n * r, K]: the caller's when they already lie back to
+// back, else a copy in the workspace.
+static qlora_status stack_A(const qlora_proj *proj, int n, int r, int64_t K, uint16_t *Acat, cudaStream_t s,
+                            const void **out) {
+    const size_t bytes = (size_t)r * (size_t)K * 2;
+    bool contiguous = true;
+    for (int g = 1; g < n; ++g)
+        contiguous = contiguous && static_cast<const char *>(proj[g].A) == static_cast<const char *>(proj[0].A) + g * bytes;
+    if (contiguous) {
+        *out = proj[0].A;
+        return QLORA_OK;
+    }
+    for (int g = 0; g < n; ++g)
+        if (cudaMemcpyAsync(reinterpret_cast<char *>(Acat) + g * bytes, proj[g].A, bytes, cudaMemcpyDeviceToDevice,
+                            s) != cudaSuccess)
+            return fail(QLORA_ERR_CUDA, "copying A of projection %d failed", g);
+    *out = Acat;
+    return QLORA_OK;
+}
+
+static qlora_status group_fwd_impl(const void *X, int64_t M, const qlora_proj *proj, int n, int r, float scale,
+                                   void *U_save, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    GroupView gv;
+    qlora_status st = check_group(M, proj, n, r, false, gv);
+    if (st) return st;
+    if (M > 0 && !X) return fail(QLORA_ERR_NULL, "X is NULL");
+    if ((X && !al16(X)) || (U_save && !al16(U_save)) || (ws && !al16(ws)))
+        return fail(QLORA_ERR_ALIGN, "X, U_save and the workspace must be 16-byte aligned");
+    if (M == 0) return ok();
+    GroupWs gw;
+    const size_t need = group_ws(M, gv, r, false, ws, ws_bytes, &gw);
+    if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
+    if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "group forward workspace %zu < %zu bytes", ws_bytes, need);
+    const int64_t K = gv.K, R = (int64_t)n * r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!group_tc_fwd(M)) {
+        // few tokens: the projections one by one (HBM-bound kernels)
+        for (int g = 0; g < n; ++g)
+            if ((st = linear_fwd_impl(X, M, gv.w[g], proj[g].A, proj[g].B, r, scale, proj[g].Y,
+                                      U_save ? static_cast<uint16_t *>(U_save) + g * r : nullptr, gw.rest,
+                                      gw.rest_bytes, stream, (int)R)))
+                return st;
+        return ok();
+    }
+    if ((st = tc_device_ok()) || (st = tc_setup<kFwd>())) return st;
+    const void *Acat;
+    if ((st = stack_A(proj, n, r, K, gw.Acat, s, &Acat))) return st;
+    GemmMaps gm;
+    memset(&gm, 0, sizeof gm);
+    CUtensorMap tmAc;
+    if ((st = make_map(&gm.act[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
+        (st = make_map(&tmAc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Acat, K, R, K * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "stacked A")) ||
+        (st = make_map(&gm.lact, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, gw.sU, R, M, R * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "sU")))
+        return st;
+    TcParams prm{};
+    prm.M = M;
+    prm.w_cols = K;
+    prm.nk_main = K / kGemmBK;
+    prm.lora_steps = (int)cdiv(r, 64);
+    prm.r = r;
+    prm.tab = kTableNF4;
+    prm.ncg = n;
+    prm.nkg = 1;
+    prm.kg_first[1] = prm.nk_main;
+    for (int g = 0; g < n; ++g) {
+        const int64_t N = gv.w[g].rows;
+        if ((st = make_map(&gm.codes[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, gv.w[g].codes, K / 2, N, K / 2, 32, 128,
+                           CU_TENSOR_MAP_SWIZZLE_32B, "codes")) ||
+            (st = make_map(&gm.lw[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, proj[g].B, r, N, r * 2, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "B")))
+            return st;
+        prm.cg_first[g + 1] = prm.cg_first[g] + cdiv(N, PairCfg::BN);
+        prm.pj[g] = TcProj{gv.w[g].q, gv.w[g].s2, gv.w[g].mean, gv.w[g].absmax, N, static_cast<uint16_t *>(proj[g].Y),
+                           N, N, g * r, 0};
+    }
+    prm.Nd = prm.cg_first[n] * PairCfg::BN;
+    // U_g = X A_g^T for all projections in one pass: U to U_save, s*U to the workspace
+    if ((st = run_skinny<0, 0>(SkJob{&gm.act[0], &tmAc, sk_plan(M, K, (int)R), kRedU, scale,
+                                     static_cast<uint16_t *>(U_save), (int)R, gw.sU, (int)R, nullptr},
+                               nullptr, (int)R, s, 3, gw.sk.flags, kSkFlagWords)))
+        return st;
+    prm.flags = gw.sk.flags;
+    prm.slots = gw.sk.slots;
+    prm.wait_ns = wait_ns();
+    prm.kernel_id = 1;
+    if ((st = launch_gemm<kFwd>(gm, prm, s))) return st;
+    return ok();
+}
+
+static qlora_status group_bwd_impl(const void *X, const void *U_saved, int64_t M, const qlora_proj *proj, int n, int r,
+                                   float scale, void *dX, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    GroupView gv;
+    qlora_status st = check_group(M, proj, n, r, true, gv);
+    if (st) return st;
+    if (M > 0 && (!X || !dX)) return fail(QLORA_ERR_NULL, "X or dX is NULL");
+    if ((X && !al16(X)) || (dX && !al16(dX)) || (U_saved && !al16(U_saved)) || (ws && !al16(ws)))
+        return fail(QLORA_ERR_ALIGN, "X, U_saved, dX and the workspace must be 16-byte aligned");
+    const int64_t K = gv.K, R = (int64_t)n * r;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (M == 0) {
+        for (int g = 0; g < n; ++g)
+            if (cudaMemsetAsync(proj[g].dA, 0, sizeof(float) * r * K, s) != cudaSuccess ||
+                cudaMemsetAsync(proj[g].dB, 0, sizeof(float) * r * gv.w[g].rows, s) != cudaSuccess)
+                return fail(QLORA_ERR_CUDA, "memset of dA/dB failed");
+        return ok();
+    }
+    GroupWs gw;
+    const size_t need = group_ws(M, gv, r, true, ws, ws_bytes, &gw);
+    if (!ws) return fail(QLORA_ERR_NULL, "workspace is NULL");
+    if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "group backward workspace %zu < %zu bytes", ws_bytes, need);
+    const uint16_t *U16 = static_cast<const uint16_t *>(U_saved);
+    if (!group_tc_bwd(M, gv)) {
+        // few tokens: the projections one by one, then dX = the sum of their parts
+        for (int g = 0; g < n; ++g)
+            if ((st = linear_bwd_impl(proj[g].dY, X, U16 ? U16 + g * r : nullptr, M, gv.w[g], proj[g].A, proj[g].B, r,
+                                      scale, gw.parts + g * M * K, proj[g].dA, proj[g].dB, gw.rest, gw.rest_bytes,
+                                      stream, (int)R)))
+                return st;
+        {
+            ProfScope ps(QLORA_KERNEL_DX_SIMT, s);
+            k_sum_parts<<<(unsigned)cdiv(M * K / 8, 256), 256, 0, s>>>(gw.parts, n, M * K,
+                                                                      static_cast<uint16_t *>(dX));
+        }
+        if ((st = launch_check("k_sum_parts"))) return st;
+        return ok();
+    }
+    if ((st = tc_device_ok()) || (st = tc_setup<kDx>())) return st;
+    const void *Acat;
+    if ((st = stack_A(proj, n, r, K, gw.Acat, s, &Acat))) return st;
+    const uint16_t *Ucur = U16 ? U16 : gw.U;
+    GemmMaps gm;
+    memset(&gm, 0, sizeof gm);
+    CUtensorMap tmDmn[kMaxGroup], tmBp[kMaxGroup], tmUg[kMaxGroup], tmXk, tmXmn, tmVmn;
+    if ((st = make_map(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "X")) ||
+        (st = make_map(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, K * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "X (MN)")) ||
+        (st = make_map(&gm.lact, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, gw.sV, R, M, R * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "sV")) ||
+        (st = make_map(&tmVmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, gw.sV, R, M, R * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "sV (MN)")) ||
+        (st = make_map(&gm.lw[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Acat, K, R, K * 2, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, "stacked A")))
+        return st;
+    TcParams prm{};
+    prm.M = M;
+    prm.Nd = K;
+    prm.w_cols = K;
+    prm.tab = kTableNF4;
+    prm.ncg = 1;
+    prm.nkg = n;
+    prm.cg_first[1] = cdiv(K, PairCfg::BN);
+    SkJob vj[kMaxGroup], bj[kMaxGroup];
+    for (int g = 0; g < n; ++g) {
+        const int64_t N = gv.w[g].rows;
+        if ((st = make_map(&gm.act[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, proj[g].dY, N, M, N * 2, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "dY")) ||
+            (st = make_map(&tmDmn[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, proj[g].dY, N, M, N * 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "dY (MN)")) ||
+            (st = make_map(&gm.codes[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, gv.w[g].codes, K / 2, N, K / 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_64B, "codes")) ||
+            (st = make_map(&tmBp[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, proj[g].B, r, N, r * 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "B")) ||
+            (st = make_map(&tmUg[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ucur + g * r, r, M, R * 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "U")))
+            return st;
+        prm.kg_first[g + 1] = prm.kg_first[g] + cdiv(N, kGemmBK);
+        prm.pj[g] = TcProj{gv.w[g].q, gv.w[g].s2, gv.w[g].mean, gv.w[g].absmax, N, static_cast<uint16_t *>(dX), K,
+                           K, 0, 0};
+        // V_g = dY_g B_g -> columns [g r, (g + 1) r) of sV = bf16(s * V)
+        vj[g] = SkJob{&gm.act[g], &tmBp[g], sk_plan(M, N, r), kRedV, scale, nullptr, 0, gw.sV + g * r, (int)R, nullptr};
+        vj[g].zend = r;
+        // dB_g = s dY_g^T U_g
+        bj[g] = SkJob{&tmDmn[g], &tmUg[g], sk_plan(N, M, r), kRedDB, scale, nullptr, 0, nullptr, 0, proj[g].dB};
+    }
+    prm.nk_main = prm.kg_first[n];
+    prm.lora_steps = (int)cdiv(R, 64);
+    prm.r = (int)R;
+    if ((st = run_skinny_list<0, 1>(vj, n, r, s, 4, gw.sk.flags, kSkFlagWords))) return st;
+    if (!U16) {
+        // U recomputed for all projections in one pass as X A^T (A stacked)
+        if ((st = run_skinny<0, 0>(SkJob{&tmXk, &gm.lw[0], sk_plan(M, K, (int)R), kRedV, 1.0f, nullptr, 0, gw.U,
+                                         (int)R, nullptr},
+                                   nullptr, (int)R, s, 3)))
+            return st;
+    }
+    // dX = sum_g dY_g W_g' + (sV) A over all projections' rows in one launch
+    prm.flags = gw.sk.flags;
+    prm.slots = gw.sk.slots;
+    prm.wait_ns = wait_ns();
+    prm.kernel_id = 2;
+    if ((st = launch_gemm<kDx>(gm, prm, s))) return st;
+    // dA of all projections at once: dA^T = X^T (sV), rank n r; into the
+    // caller's dA when those lie back to back
+    const size_t abytes = (size_t)r * (size_t)K * sizeof(float);
+    bool dA_contiguous = true;
+    for (int g = 1; g < n; ++g)
+        dA_contiguous = dA_contiguous &&
+                        reinterpret_cast<char *>(proj[g].dA) == reinterpret_cast<char *>(proj[0].dA) + g * abytes;
+    float *dAdst = dA_contiguous ? proj[0].dA : gw.dAcat;
+    if ((st = run_skinny<1, 1>(SkJob{&tmXmn, &tmVmn, sk_plan(K, M, (int)R), kRedDA, 1.0f, nullptr, 0, nullptr, 0, dAdst},
+                               nullptr, (int)R, s, 5)))
+        return st;
+    if ((st = run_skinny_list<1, 1>(bj, n, r, s, 5, nullptr, 0))) return st;
+    if (!dA_contiguous)
+        for (int g = 0; g < n; ++g)
+            if (cudaMemcpyAsync(proj[g].dA, reinterpret_cast<char *>(gw.dAcat) + g * abytes, abytes,
+                                cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+                return fail(QLORA_ERR_CUDA, "copying dA of projection %d failed", g);
+    return ok();
+}
+
+size_t qlora_group_fwd_workspace(int64_t M, const qlora_proj *proj, int n, int r) {
+    GroupView gv;
+    if (check_group(M, proj, n, r, false, gv, false) != QLORA_OK) return 0;
+    return group_ws(M, gv, r, false, nullptr, 0, nullptr);
+}
+
+size_t qlora_group_bwd_workspace(int64_t M, const qlora_proj *proj, int n, int r) {
+    GroupView gv;
+    if (check_group(M, proj, n, r, true, gv, false) != QLORA_OK) return 0;
+    return group_ws(M, gv, r, true, nullptr, 0, nullptr);
+}
+
+qlora_status qlora_group_fwd(const void *X, int64_t M, const qlora_proj *proj, int n, int r, float scale,
+                             void *U_save, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    return group_fwd_impl(X, M, proj, n, r, scale, U_save, ws, ws_bytes, stream);
+}
+
+qlora_status qlora_group_bwd(const void *X, const void *U_saved, int64_t M, const qlora_proj *proj, int n, int r,
+                             float scale, void *dX, void *ws, size_t ws_bytes, qlora_stream_t stream) {
+    return group_bwd_impl(X, U_saved, M, proj, n, r, scale, dX, ws, ws_bytes, stream);
 }
 
 void qlora_q4_table(int table, float levels[16]) {

@@ -35,7 +35,10 @@ EXPORTS = [
     "qlora_lora_merge_workspace", "qlora_lora_merge_requantize", "qlora_adamw_step",
     "qlora_q4_table", "qlora_q4_quantize", "qlora_q4_dequantize", "qlora_q4_linear_fwd_workspace",
     "qlora_q4_linear_bwd_workspace", "qlora_q4_linear_fwd", "qlora_q4_linear_bwd",
+    "qlora_group_fwd_workspace", "qlora_group_bwd_workspace", "qlora_group_fwd", "qlora_group_bwd",
 ]
+
+MAX_GROUP = 4
 
 TABLE_NF4, TABLE_INT4 = 0, 1
 
@@ -58,6 +61,11 @@ class Q4WeightDesc(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("table", ctypes.c_int32),
                 ("double_quant", ctypes.c_int32), ("codes", ctypes.c_void_p), ("absmax_q", ctypes.c_void_p),
                 ("absmax_scale", ctypes.c_void_p), ("absmax_mean", ctypes.c_void_p), ("absmax", ctypes.c_void_p)]
+
+
+class ProjDesc(ctypes.Structure):
+    _fields_ = [("w", ctypes.POINTER(Nf4WeightDesc)), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("Y", ctypes.c_void_p), ("dY", ctypes.c_void_p), ("dA", ctypes.c_void_p), ("dB", ctypes.c_void_p)]
 
 
 def lib():
@@ -122,6 +130,14 @@ def lib():
         L.qlora_q4_linear_fwd.argtypes = [vp, i64, Q, vp, vp, i32, f32, vp, vp, vp, sz, vp]
         L.qlora_q4_linear_bwd.restype = i32
         L.qlora_q4_linear_bwd.argtypes = [vp, vp, vp, i64, Q, vp, vp, i32, f32, vp, vp, vp, vp, sz, vp]
+        P = ctypes.POINTER(ProjDesc)
+        for n in ("qlora_group_fwd_workspace", "qlora_group_bwd_workspace"):
+            getattr(L, n).restype = sz
+            getattr(L, n).argtypes = [i64, P, i32, i32]
+        L.qlora_group_fwd.restype = i32
+        L.qlora_group_fwd.argtypes = [vp, i64, P, i32, i32, f32, vp, vp, sz, vp]
+        L.qlora_group_bwd.restype = i32
+        L.qlora_group_bwd.argtypes = [vp, vp, i64, P, i32, i32, f32, vp, vp, sz, vp]
         L.qlora_debug_gemm_segments.restype = i64
         L.qlora_debug_gemm_segments.argtypes = [i64, i64, i64, i32, i32, vp, i64]
         _lib = L
@@ -327,6 +343,48 @@ def qlora_q4_linear_bwd(dY, X, U_saved, M, w: Q4Weight, A, B, r, scale, dX, dA, 
     _check(lib().qlora_q4_linear_bwd(_ptr(dY), _ptr(X), _ptr(U_saved), M, ctypes.byref(d), _ptr(A), _ptr(B), r,
                                      float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws),
                                      0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ---- projection groups --------------------------------------------------------
+
+def _projs(ws_, As, Bs, Ys=None, dYs=None, dAs=None, dBs=None):
+    """A ctypes array of projection descriptors (it keeps the weight
+    descriptors it points to alive)."""
+    n = len(ws_)
+    descs = [w.desc for w in ws_]
+    arr = (ProjDesc * n)()
+    for g in range(n):
+        arr[g].w = ctypes.pointer(descs[g])
+        arr[g].A = As[g].data_ptr()
+        arr[g].B = Bs[g].data_ptr()
+        arr[g].Y = Ys[g].data_ptr() if Ys is not None else None
+        arr[g].dY = dYs[g].data_ptr() if dYs is not None else None
+        arr[g].dA = dAs[g].data_ptr() if dAs is not None else None
+        arr[g].dB = dBs[g].data_ptr() if dBs is not None else None
+    arr._keep = descs
+    return arr
+
+
+def qlora_group_fwd_workspace(M, ws_, As, Bs, r):
+    return lib().qlora_group_fwd_workspace(M, _projs(ws_, As, Bs), len(ws_), r)
+
+
+def qlora_group_bwd_workspace(M, ws_, As, Bs, r):
+    return lib().qlora_group_bwd_workspace(M, _projs(ws_, As, Bs), len(ws_), r)
+
+
+def qlora_group_fwd(X, M, ws_, As, Bs, r, scale, Ys, U_save, ws, stream=None):
+    """Forward of the projections (weights ws_, adapters As, Bs) sharing X; U_save [M, n r] or None."""
+    p = _projs(ws_, As, Bs, Ys=Ys)
+    _check(lib().qlora_group_fwd(_ptr(X), M, p, len(ws_), r, float(scale), _ptr(U_save), _ptr(ws),
+                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qlora_group_bwd(X, U_saved, M, ws_, As, Bs, r, scale, dYs, dX, dAs, dBs, ws, stream=None):
+    """Backward of the projections: dA_g, dB_g and dX = the sum over g of the input gradients."""
+    p = _projs(ws_, As, Bs, dYs=dYs, dAs=dAs, dBs=dBs)
+    _check(lib().qlora_group_bwd(_ptr(X), _ptr(U_saved), M, p, len(ws_), r, float(scale), _ptr(dX), _ptr(ws),
+                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def qlora_lora_merge_workspace(rows, cols):

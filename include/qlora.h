@@ -274,6 +274,54 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
                               float scale, void *dX, float *dA, float *dB, void *ws,
                               size_t ws_bytes, qlora_stream_t stream);
 
+/* ---- projection groups: several layers that share their input ---------- */
+
+/* A group is 1..QLORA_MAX_GROUP LoRA linear layers that read the same X
+ * [M, K] with their own weights: the attention's q, k and v projections, or
+ * the MLP's gate and up projections (xingyuzhitong.com "Fine-Tuning Memory
+ * Requirements", section "LoRA: freeze the base, train small adapters", and
+ * serverroom.net, section "Setting up Unsloth on the server": adapters on
+ * q/k/v/o/gate/up/down). One grouped call computes, for every projection g,
+ *   Y_g = X W_g'^T + scale * (X A_g^T) B_g^T
+ * and the backward the adapter gradients of every projection and
+ *   dX = sum_g ( dY_g W_g' + scale * (dY_g B_g) A_g )     bf16 [M, K]
+ * (the gradient of the shared input). The arithmetic per projection is the
+ * single-layer calls' (the same results up to fp32 summation order); the
+ * group runs as one fused GEMM launch over all projections' output columns
+ * (forward) or over all their rows (dX), one LoRA down-projection over the
+ * stacked A_g, and reads X once per pass instead of once per projection.
+ * Requirements: every weight has the same cols K; one rank r for all,
+ * r % 8 == 0 and 8 <= r <= 128; one scale. All pointers are device
+ * pointers, 16-byte aligned, owned by the caller. A QLORA_ERR_* status is
+ * returned before anything is launched when a requirement fails. */
+#define QLORA_MAX_GROUP 4
+typedef struct {
+    const qlora_nf4_weight *w; /* W_g [N_g, K] */
+    const void *A;             /* bf16 [r, K] */
+    const void *B;             /* bf16 [N_g, r] */
+    void *Y;                   /* forward: bf16 [M, N_g] output (overwritten) */
+    const void *dY;            /* backward: bf16 [M, N_g] */
+    float *dA;                 /* backward: fp32 [r, K] output (overwritten) */
+    float *dB;                 /* backward: fp32 [N_g, r] output (overwritten) */
+} qlora_proj;
+
+/* Workspace bytes of qlora_group_fwd / qlora_group_bwd for these sizes
+ * (0 for invalid arguments). */
+size_t qlora_group_fwd_workspace(int64_t M, const qlora_proj *proj, int n, int r);
+size_t qlora_group_bwd_workspace(int64_t M, const qlora_proj *proj, int n, int r);
+
+/* Forward of n projections (fields w, A, B, Y of each are used).
+ * U_save: bf16 [M, n * r] or NULL; receives U_g = X A_g^T (bf16) in columns
+ * [g * r, (g + 1) * r), the layout qlora_group_bwd reads. */
+qlora_status qlora_group_fwd(const void *X, int64_t M, const qlora_proj *proj, int n, int r, float scale,
+                             void *U_save, void *ws, size_t ws_bytes, qlora_stream_t stream);
+
+/* Backward of n projections (fields w, A, B, dY, dA, dB of each are used):
+ * dA_g, dB_g as qlora_linear_bwd computes them for projection g, and dX
+ * above. U_saved: the forward's U_save [M, n * r], or NULL to recompute. */
+qlora_status qlora_group_bwd(const void *X, const void *U_saved, int64_t M, const qlora_proj *proj, int n, int r,
+                             float scale, void *dX, void *ws, size_t ws_bytes, qlora_stream_t stream);
+
 /* ---- optimizer step for the adapters ----------------------------------- */
 
 /* One AdamW step on n fp32 parameters (the flattened adapter A or B master

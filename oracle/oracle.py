@@ -257,6 +257,30 @@ def linear_bwd(dY, X, Wdq, A, B, scale, rows=None, ncols=None, kcols=None):
     return dX, dA, dB
 
 
+# --------------------------------------------------------------- groups ----
+# Several LoRA linears reading the same X (q/k/v, gate/up: xingyuzhitong.com
+# "Fine-Tuning Memory Requirements", section "LoRA: freeze the base, train
+# small adapters"). Each output is its own projection's; the gradient of the
+# shared input is the sum of the projections' (the chain rule through a value
+# used n times).
+
+def group_fwd(X, Wdqs, As, Bs, scale, rows=None):
+    """[(Y_g, U_g)] for every projection g, as linear_fwd computes them."""
+    return [linear_fwd(X, W, A, B, scale, rows=rows) for W, A, B in zip(Wdqs, As, Bs)]
+
+
+def group_bwd(dYs, X, Wdqs, As, Bs, scale, rows=None):
+    """(dX = sum over g of linear_bwd's dX_g, in fp64 in projection order, and
+    [(dA_g, dB_g)])."""
+    dX = None
+    grads = []
+    for dY, W, A, B in zip(dYs, Wdqs, As, Bs):
+        dXg, dA, dB = linear_bwd(dY, X, W, A, B, scale, rows=rows)
+        dX = dXg if dX is None else dX + dXg
+        grads.append((dA, dB))
+    return dX, grads
+
+
 # ---------------------------------------------------------------- merge ----
 
 def lora_merge(Wdq, A, B, scale):

@@ -138,6 +138,46 @@ def test_q4_quantize_rejects_on_host(q):
                                  None, c(FAKE), 1 << 30, None) == 8
 
 
+def test_group_rejects_on_host(q):
+    L = q.lib()
+    c = ctypes.c_void_p
+    d1, d2, d3 = desc(rows=64, cols=128), desc(rows=128, cols=128), desc(rows=64, cols=256)
+
+    def projs(ds, **kw):
+        arr = (q.ProjDesc * len(ds))()
+        for i, d in enumerate(ds):
+            arr[i].w = ctypes.pointer(d)
+            for f in ("A", "B", "Y", "dY", "dA", "dB"):
+                setattr(arr[i], f, kw.get(f, FAKE))
+        return arr
+
+    def fwd(ds, n=None, r=16, M=64, ws_bytes=1 << 40, **kw):
+        return L.qlora_group_fwd(c(FAKE), M, projs(ds, **kw), len(ds) if n is None else n, r, 2.0, None, c(FAKE),
+                                 ws_bytes, None)
+
+    def bwd(ds, r=16, M=64, **kw):
+        return L.qlora_group_bwd(c(FAKE), None, M, projs(ds, **kw), len(ds), r, 2.0, c(FAKE), c(FAKE), 1 << 40, None)
+    assert fwd([d1, d2], n=0) == 2
+    assert fwd([d1, d2], n=5) == 2
+    assert fwd([d1, d2], r=12) == 5     # r % 8
+    assert fwd([d1, d2], r=136) == 5
+    assert fwd([d1, d3]) == 2           # different K
+    assert fwd([d1, d2], A=0) == 1
+    assert fwd([d1, d2], Y=0) == 1
+    assert fwd([d1, d2], Y=FAKE + 8) == 3
+    assert fwd([d1, d2], ws_bytes=16) == 4
+    assert fwd([d1, desc(cols=100)]) == 2
+    assert bwd([d1, d2], dY=0) == 1
+    assert bwd([d1, d2], dA=0) == 1
+    assert bwd([d1, d2], dB=FAKE + 4) == 3
+    assert fwd([d1, d2], M=0) == 0      # nothing to launch
+    # workspace queries: 0 for invalid groups, outputs not needed
+    assert L.qlora_group_fwd_workspace(64, projs([d1, d3]), 2, 16) == 0
+    assert L.qlora_group_fwd_workspace(64, projs([d1, d2], Y=0), 2, 16) > 0
+    assert L.qlora_group_bwd_workspace(64, projs([d1, d2], dY=0), 2, 16) > 0
+    assert L.qlora_group_bwd_workspace(64, projs([d1, d2]), 2, 12) == 0
+
+
 def call_fwd(q, M=16, d=None, r=8, ws_bytes=None, X=FAKE, A=FAKE, B=FAKE, Y=FAKE):
     d = d or desc()
     if ws_bytes is None:
