@@ -3,7 +3,11 @@
 One step = forward + backward of all seven NF4-LoRA projections of a
 Llama-70B-shaped decoder layer (q, k, v, o, gate, up, down with d_model 8192,
 KV width 1024, FFN 28672; LoRA r = 64, alpha = 16; M = 4096 tokens), inputs
-resident in HBM. The same JSON line carries: the roofline of the step's
+resident in HBM, run as the layer runs them: q/k/v on one input and gate/up
+on one input, each group as one grouped call (o and down alone), so the
+backward returns one input gradient per group. The same step as seven
+single-layer calls is timed beside it ("ungrouped"). The same JSON line
+carries: the roofline of the step's
 dominant kernel kind; an end-to-end figure through the C ABI with host buffers;
 the Llama-3.1-8B-shaped layer (M = 2048, r = 16) and the single 1024 x 1024
 layer (M = 256, r = 8); the standalone codec (14336 x 4096 quantize once +
@@ -41,6 +45,8 @@ SINGLE = 0            # single 1024 x 1024 layer, M = 256, r = 8
 CODEC_WORKLOAD = 2    # 14336 x 4096 codec
 SWEEP = 4             # gate 4096 -> 14336 token sweep
 CPU_SAMPLE_TOKENS = 24
+# projections of a decoder layer that read the same input
+LAYER_GROUPS = [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)]
 METRIC = "QLoRA linear fwd+bwd TFLOP/s and % bf16 peak; NF4 dequant GB/s and % HBM"
 
 
@@ -167,11 +173,26 @@ class Clocks:
                 "interval_ms": self.interval}
 
 
+def groups_of(P):
+    """Index lists of the projections by LAYER_GROUPS (others alone)."""
+    names = [d["name"] for d in P]
+    out, used = [], set()
+    for gr in LAYER_GROUPS:
+        idx = [names.index(n) for n in gr if n in names]
+        if idx:
+            out.append(idx)
+            used.update(idx)
+    out += [[i] for i in range(len(P)) if i not in used]
+    return out
+
+
 def load_layer(qlora, torch, dev, wl_id, pinned=False):
     """Seeded inputs of every projection of a workload (synth recipe, numpy),
     copied to the device; weights quantized on the GPU; outputs and one
     workspace per projection; pinned host copies of X and dY for the
-    end-to-end leg when asked."""
+    end-to-end leg when asked. Projections of one group read the first
+    member's X. Returns the workload, the projections and the groups (their
+    shared input, stacked U, input gradient and workspace)."""
     wl = synth.WORKLOADS[wl_id]
     M, r = wl["M"], wl["r"]
     P = []
@@ -197,11 +218,41 @@ def load_layer(qlora, torch, dev, wl_id, pinned=False):
         d["ws"] = qlora.workspace(max(qlora.qlora_linear_fwd_workspace(M, w, r),
                                       qlora.qlora_linear_bwd_workspace(M, w, r)), dev)
         P.append(d)
+    G = []
+    for idx in groups_of(P):
+        first = P[idx[0]]
+        for i in idx[1:]:
+            P[i]["X"] = first["X"]
+            if pinned:
+                P[i]["hX"] = first["hX"]
+        mem = [P[i] for i in idx]
+        ws_, As, Bs = [d["w"] for d in mem], [d["A"] for d in mem], [d["B"] for d in mem]
+        G.append(dict(idx=idx, name="/".join(d["name"] for d in mem), X=first["X"], s=first["s"], k=first["k"],
+                      w=ws_, A=As, B=Bs, Y=[d["Y"] for d in mem], dY=[d["dY"] for d in mem],
+                      dA=[d["dA"] for d in mem], dB=[d["dB"] for d in mem],
+                      U=torch.empty((M, len(idx) * r), dtype=torch.bfloat16, device=dev),
+                      dX=torch.empty((M, first["k"]), dtype=torch.bfloat16, device=dev),
+                      ws=qlora.workspace(max(qlora.qlora_group_fwd_workspace(M, ws_, As, Bs, r),
+                                             qlora.qlora_group_bwd_workspace(M, ws_, As, Bs, r)), dev)))
     torch.cuda.synchronize()
-    return wl, P
+    return wl, P, G
+
+
+def make_group_step(qlora, G, M, r, world):
+    """The layer step through the grouped calls."""
+    def step():
+        for g in G:
+            qlora.qlora_group_fwd(g["X"], M, g["w"], g["A"], g["B"], r, g["s"], g["Y"], g["U"], g["ws"])
+        for g in reversed(G):
+            qlora.qlora_group_bwd(g["X"], g["U"], M, g["w"], g["A"], g["B"], r, g["s"], g["dY"], g["dX"], g["dA"],
+                                  g["dB"], g["ws"])
+            if world > 1:
+                dp.allreduce_adapter_grads(g["dA"] + g["dB"])
+    return step
 
 
 def make_step(qlora, P, M, r, world):
+    """The layer step as one single-layer call per projection."""
     def step():
         for d in P:
             qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"])
@@ -277,52 +328,62 @@ def roofline_of(kind_ms, kind_n, graph_ms, M, projections, r, pk, clocks):
                       "that the kinds sum to the graph-timed ms_per_step"}
 
 
-def e2e_leg(qlora, torch, dev, P, M, r, world, steps, flops):
+def e2e_leg(qlora, torch, dev, P, G, M, r, world, steps, flops):
     """Same step through the C ABI with pinned host buffers: per step the H2D
-    copy of every X and dY and the D2H copy of Y, dX, dA and dB, on two copy
-    streams overlapping the compute stream."""
-    hY = {d["name"]: torch.empty(d["Y"].shape, dtype=torch.bfloat16, pin_memory=True) for d in P}
-    hdX = {d["name"]: torch.empty(d["dX"].shape, dtype=torch.bfloat16, pin_memory=True) for d in P}
-    hdA = {d["name"]: torch.empty(d["dA"].shape, dtype=torch.float32, pin_memory=True) for d in P}
-    hdB = {d["name"]: torch.empty(d["dB"].shape, dtype=torch.float32, pin_memory=True) for d in P}
-    h2d = sum(d["hX"].numel() * 2 + d["hdY"].numel() * 2 for d in P)
-    d2h = sum(d["Y"].numel() * 2 + d["dX"].numel() * 2 + d["dA"].numel() * 4 + d["dB"].numel() * 4 for d in P)
+    copy of every group's X and every projection's dY, and the D2H copy of
+    every Y, dA, dB and every group's dX, on two copy streams overlapping the
+    compute stream."""
+    hY = [torch.empty(d["Y"].shape, dtype=torch.bfloat16, pin_memory=True) for d in P]
+    hdA = [torch.empty(d["dA"].shape, dtype=torch.float32, pin_memory=True) for d in P]
+    hdB = [torch.empty(d["dB"].shape, dtype=torch.float32, pin_memory=True) for d in P]
+    hdX = [torch.empty(g["dX"].shape, dtype=torch.bfloat16, pin_memory=True) for g in G]
+    h2d = sum(P[g["idx"][0]]["hX"].numel() * 2 for g in G) + sum(d["hdY"].numel() * 2 for d in P)
+    d2h = sum(d["Y"].numel() * 2 + d["dA"].numel() * 4 + d["dB"].numel() * 4 for d in P) + \
+        sum(g["dX"].numel() * 2 for g in G)
     s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     comp = torch.cuda.current_stream()
 
-    def e2e_step():
-        for d in P:
-            with torch.cuda.stream(s_h2d):
-                d["X"].copy_(d["hX"], non_blocking=True)
-                d["ev_x"] = torch.cuda.Event()
-                d["ev_x"].record(s_h2d)
-                d["dY"].copy_(d["hdY"], non_blocking=True)
-                d["ev_dy"] = torch.cuda.Event()
-                d["ev_dy"].record(s_h2d)
-        for d in P:
-            comp.wait_event(d["ev_x"])
-            qlora.qlora_linear_fwd(d["X"], M, d["w"], d["A"], d["B"], r, d["s"], d["Y"], d["U"], d["ws"])
-            ev = torch.cuda.Event()
-            ev.record(comp)
-            s_d2h.wait_event(ev)
-            with torch.cuda.stream(s_d2h):
-                hY[d["name"]].copy_(d["Y"], non_blocking=True)
-        for d in reversed(P):
-            comp.wait_event(d["ev_dy"])
-            qlora.qlora_linear_bwd(d["dY"], d["X"], d["U"], M, d["w"], d["A"], d["B"], r, d["s"], d["dX"], d["dA"],
-                                   d["dB"], d["ws"])
-            if world > 1:
-                dp.allreduce_adapter_grads([d["dA"], d["dB"]])
-            ev = torch.cuda.Event()
-            ev.record(comp)
-            s_d2h.wait_event(ev)
-            with torch.cuda.stream(s_d2h):
-                hdX[d["name"]].copy_(d["dX"], non_blocking=True)
-                hdA[d["name"]].copy_(d["dA"], non_blocking=True)
-                hdB[d["name"]].copy_(d["dB"], non_blocking=True)
+    def after(stream_from, stream_to):
         ev = torch.cuda.Event()
-        ev.record(s_d2h)
-        comp.wait_event(ev)
+        ev.record(stream_from)
+        stream_to.wait_event(ev)
+
+    def e2e_step():
+        ev_x, ev_dy = [], []
+        for g in G:
+            with torch.cuda.stream(s_h2d):
+                g["X"].copy_(P[g["idx"][0]]["hX"], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_h2d)
+                ev_x.append(e)
+        for g in G:
+            with torch.cuda.stream(s_h2d):
+                for i in g["idx"]:
+                    P[i]["dY"].copy_(P[i]["hdY"], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_h2d)
+                ev_dy.append(e)
+        for gi, g in enumerate(G):
+            comp.wait_event(ev_x[gi])
+            qlora.qlora_group_fwd(g["X"], M, g["w"], g["A"], g["B"], r, g["s"], g["Y"], g["U"], g["ws"])
+            after(comp, s_d2h)
+            with torch.cuda.stream(s_d2h):
+                for i in g["idx"]:
+                    hY[i].copy_(P[i]["Y"], non_blocking=True)
+        for gi in reversed(range(len(G))):
+            g = G[gi]
+            comp.wait_event(ev_dy[gi])
+            qlora.qlora_group_bwd(g["X"], g["U"], M, g["w"], g["A"], g["B"], r, g["s"], g["dY"], g["dX"], g["dA"],
+                                  g["dB"], g["ws"])
+            if world > 1:
+                dp.allreduce_adapter_grads(g["dA"] + g["dB"])
+            after(comp, s_d2h)
+            with torch.cuda.stream(s_d2h):
+                hdX[gi].copy_(g["dX"], non_blocking=True)
+                for i in g["idx"]:
+                    hdA[i].copy_(P[i]["dA"], non_blocking=True)
+                    hdB[i].copy_(P[i]["dB"], non_blocking=True)
+        after(s_d2h, comp)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -335,25 +396,31 @@ def e2e_leg(qlora, torch, dev, P, M, r, world, steps, flops):
     ms = a.elapsed_time(b) / steps
     return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "note": "pinned host buffers; H2D of every X and dY and D2H of Y, dX, dA, dB on two copy streams "
-                    "overlapping the compute stream"}
+            "note": "pinned host buffers; H2D of every group's X and every dY, D2H of every Y, dA, dB and every "
+                    "group's dX, on two copy streams overlapping the compute stream; grouped calls"}
 
 
 def bench_layer(qlora, torch, dev, pk, wl_id, steps):
-    """A whole layer step (graph-timed) of another workload, with its own
-    per-kind times."""
-    wl, P = load_layer(qlora, torch, dev, wl_id)
+    """A whole layer step (graph-timed) of another workload, grouped as the
+    headline step, with its own per-kind times, and the same step as one
+    call per projection."""
+    wl, P, G = load_layer(qlora, torch, dev, wl_id)
     M, r = wl["M"], wl["r"]
-    step = make_step(qlora, P, M, r, 1)
+    step = make_group_step(qlora, G, M, r, 1)
     ms = graph_time(torch, step, steps, 3)
     kms, kn = profile_kinds(qlora, torch, step, 3)
+    ms_u = graph_time(torch, make_step(qlora, P, M, r, 1), steps, 3)
+    _, kn_u = profile_kinds(qlora, torch, make_step(qlora, P, M, r, 1), 1)
     flops = step_flops(M, wl["projections"], r)
     v = flops / (ms * 1e-3) / 1e12
     out = {"workload": wl["name"], "M": M, "r": r, "alpha": wl["alpha"], "ms_per_step": ms, "value": v,
            "unit": "TFLOP/s", "pct_bf16_peak": v / pk["bf16"], "pct_bf16_peak_sustained": v / pk["bf16_sus"],
-           "flops_per_step": flops, "kernels_ms_per_step_eager": kms, "kernels_launches_per_step": kn,
-           "roofline": roofline_of(kms, kn, ms, M, wl["projections"], r, pk, None)}
-    del P
+           "flops_per_step": flops, "groups": [g["name"] for g in G], "kernels_ms_per_step_eager": kms,
+           "kernels_launches_per_step": kn,
+           "roofline": roofline_of(kms, kn, ms, M, wl["projections"], r, pk, None),
+           "ungrouped": {"ms_per_step": ms_u, "value": flops / (ms_u * 1e-3) / 1e12,
+                         "launches_per_step": sum(kn_u.values())}}
+    del P, G
     torch.cuda.empty_cache()
     return out
 
@@ -649,10 +716,10 @@ def main():
     pk = peaks()
     props = torch.cuda.get_device_properties(dev)
 
-    wl, P = load_layer(qlora, torch, dev, WORKLOAD, pinned=True)
+    wl, P, G = load_layer(qlora, torch, dev, WORKLOAD, pinned=True)
     projs, M, r = wl["projections"], wl["M"], wl["r"]
     stream = torch.cuda.current_stream()
-    step = make_step(qlora, P, M, r, world)
+    step = make_group_step(qlora, G, M, r, world)
 
     def barrier():
         if world > 1:
@@ -697,9 +764,18 @@ def main():
     kind_ms, kind_n = profile_kinds(qlora, torch, step, max(1, args.prof_steps))
     launches = sum(kind_n.values()) * args.steps
     roof = roofline_of(kind_ms, kind_n, ms_step, M, projs, r, pk, clocks)
-    e2e = e2e_leg(qlora, torch, dev, P, M, r, world, args.e2e_steps, flops)
+    e2e = e2e_leg(qlora, torch, dev, P, G, M, r, world, args.e2e_steps, flops)
     timed_region = "CUDA graph of one step replayed" if graph is not None else "eager launches"
-    del P, graph
+    ungrouped = None
+    if world == 1 and not args.no_extra:
+        ustep = make_step(qlora, P, M, r, 1)
+        ms_u = graph_time(torch, ustep, max(10, args.steps // 4), 3)
+        _, kn_u = profile_kinds(qlora, torch, ustep, 1)
+        ungrouped = {"ms_per_step": ms_u, "value": flops / (ms_u * 1e-3) / 1e12,
+                     "launches_per_step": sum(kn_u.values()),
+                     "note": "the same step as seven single-layer calls (each projection reads X itself and "
+                             "returns its own dX)"}
+    del P, G, graph
     torch.cuda.empty_cache()
 
     extra = {}
@@ -719,7 +795,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "pct_bf16_peak": value / world / pk["bf16"], "pct_bf16_peak_sustained": value / world / pk["bf16_sus"],
-            "config": {"workload": wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=64 alpha=16",
+            "config": {"workload": wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=64 alpha=16; "
+                                   "groups q/k/v, o, gate/up, down",
                        "M": M, "r": r, "alpha": wl["alpha"], "projections": [[n_, k_] for _, n_, k_ in projs],
                        "flops_per_step": flops, "parallelism": f"dp{world}",
                        "l2": "inputs larger than L2 (several GB touched per step)",
@@ -730,6 +807,7 @@ def main():
             "gpu_launches": launches,
             "kernels_ms_per_step_eager": kind_ms,
             "kernels_launches_per_step": kind_n,
+            "ungrouped": ungrouped,
             "timed_region": timed_region,
             "clocks": clocks,
             **extra,
