@@ -476,15 +476,28 @@ int64_t gemm_pairs_resident() {
 // full); stream-K over every tile when there are fewer tiles than half the
 // pairs (on at most three pairs per tile: each more partial to add back
 // costs the finishing pair more than the shorter share saves); otherwise
-// data-parallel rounds with the last one-and-a-fraction rounds stream-K.
+// whole data-parallel rounds with the last one-and-a-fraction rounds
+// stream-K. When the activation operand is larger than three quarters of
+// the L2 (big_act), the stream-K phase covers only the R = T mod P tiles left if
+// every pair's share of them is at least a third of a tile (so at most four
+// pairs share a tile): its pairs work at unrelated k offsets and share no
+// activation reads through L2, and with a 235 MB activation (4096 x 28672) a
+// stream-K phase over P + R tiles read about ten times the activation bytes
+// from DRAM. With an activation that stays in L2 the longer phase is
+// slightly faster (fewer, longer shares).
 struct GemmSched {
     int64_t dp_tiles, pairs;
 };
-GemmSched gemm_sched(int64_t T, int64_t S, int64_t P) {
+GemmSched gemm_sched(int64_t T, int64_t S, int64_t P, bool big_act) {
     if (2 * T < P) return {0, std::min({P, T * S, 3 * T})};
     if (T <= P || T % P == 0 || 2 * (T % P) >= P) return {T, std::min(P, T)};
+    if (big_act && (T % P) * S / P >= (S + 2) / 3) return {(T / P) * P, P};
     return {(T / P - 1) * P, P};
 }
+
+// Activation operand size above which the stream-K phase is kept short:
+// three quarters of the B300's 126 MB L2.
+constexpr int64_t kBigActBytes = 96ll << 20;
 
 // Sets prm.tile_rows and prm.dp_tiles for P resident pairs; returns the pairs
 // to launch. Very few tiles of 512 rows (fewer than a quarter of the pairs):
@@ -494,7 +507,9 @@ GemmSched gemm_sched(int64_t T, int64_t S, int64_t P) {
 int64_t gemm_schedule(TcParams &prm, int64_t P) {
     const int64_t nt = cdiv(prm.Nd, PairCfg::BN);
     prm.tile_rows = 4 * nt * cdiv(prm.M, PairCfg::PAIR_M) < P ? PairCfg::PAIR_M / 2 : PairCfg::PAIR_M;
-    const GemmSched sc = gemm_sched(nt * cdiv(prm.M, (int64_t)prm.tile_rows), prm.nk_main + prm.lora_steps, P);
+    const bool big_act = prm.M * prm.nk_main * kGemmBK * 2 > kBigActBytes;
+    const GemmSched sc =
+        gemm_sched(nt * cdiv(prm.M, (int64_t)prm.tile_rows), prm.nk_main + prm.lora_steps, P, big_act);
     prm.dp_tiles = sc.dp_tiles;
     return sc.pairs;
 }

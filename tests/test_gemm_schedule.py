@@ -97,7 +97,14 @@ def test_llama8b_layer_schedules():
     assert check(2048, 4096, 64, 1, 74)[:4] == (512, 64, 64, 64)      # q/o fwd and dX
     assert check(2048, 4096, 224, 1, 74)[:4] == (512, 64, 64, 64)     # gate/up dX, down fwd
     assert check(2048, 1024, 64, 1, 74)[:4] == (256, 0, 74, 32)       # k/v fwd
-    assert check(32768, 14336, 64, 1, 74)[:4] == (512, 3478, 74, 3584)
+    # 48 whole rounds, then stream-K over the 32 tiles left (a share of 28
+    # steps per pair, over a third of a 65-step tile)
+    assert check(32768, 14336, 64, 1, 74)[:4] == (512, 3552, 74, 3584)
+    # the 70B layer (M = 4096): with a 224 MiB activation (down forward, gate
+    # and up dX) 3 rounds of the 256 tiles, then stream-K over 34; with a
+    # 64 MiB one (q/o), which stays in L2, 2 rounds and stream-K over 108
+    assert check(4096, 8192, 448, 1, 74)[:4] == (512, 222, 74, 256)
+    assert check(4096, 8192, 128, 1, 74)[:4] == (512, 148, 74, 256)
 
 
 def test_rejects_bad_arguments():
