@@ -15,6 +15,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libqlora_b300.so")
+# diagnostic build: the same library with the fused GEMM recording per-step
+# timestamps of one CTA pair (see profile_case.py --stamps)
+STAMPS_LIB = os.path.join(PKG, "libqlora_b300_stamps.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 FLAGS = [
@@ -32,28 +35,30 @@ def sources():
                   + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "qlora.h")])
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(s) > t for s in sources())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [NVCC, *FLAGS, *(["-Xptxas", "-v"] if ptxas_v else []), "-o", tmp, os.path.join(CSRC, "qlora_lib.cu")]
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, stamps: bool = False) -> str:
+    lib = STAMPS_LIB if stamps else LIB
+    if not force and not needs_build(lib):
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = [NVCC, *FLAGS, *(["-DQLORA_GEMM_STAMPS"] if stamps else []), *(["-Xptxas", "-v"] if ptxas_v else []),
+           "-o", tmp, os.path.join(CSRC, "qlora_lib.cu")]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc failed building libqlora_b300.so")
+        raise RuntimeError(f"nvcc failed building {os.path.basename(lib)}")
     if verbose or ptxas_v:
         sys.stderr.write(r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -96,18 +96,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 }
 constexpr uint32_t kWaitHintNs = 20000;
 
-// Bounded wait: spins at most `limit` times on try_wait (each try_wait itself
-// suspends for a hardware-defined interval). On running out it records
-// `code` in the device error word and returns false; the caller then stops
-// issuing work that depends on this barrier.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int64_t limit,
-                                                  unsigned int code) {
-    for (int64_t i = 0; i < limit; ++i)
-        if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
-    record_error(code);
-    return false;
-}
-
 // 2-D TMA tile load into shared memory, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t x,
                                             int32_t y) {

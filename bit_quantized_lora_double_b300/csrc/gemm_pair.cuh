@@ -41,6 +41,29 @@
 
 namespace qlora {
 
+// Diagnostic timeline (built only with -DQLORA_GEMM_STAMPS, into a separate
+// library): globaltimer stamps of the first CTA pair of the last launch, per
+// k-step g (rows 0-4, 7) or per tile (rows 5, 6):
+//   0 producer: stage free, loads about to be issued     (CTA 0)
+//   1 decode group: the stage's bytes have landed          (CTA 0, first warp)
+//   2 decode group: decoded tile stored                    (CTA 0, first warp)
+//   3 MMA issuer: decoded halves ready                     (CTA 0)
+//   4 MMA issuer: MMAs issued and committed                (CTA 0)
+//   5 epilogue: accumulators complete                      (CTA 0, warp 0)
+//   6 epilogue: accumulators read, released to the MMAs    (CTA 0, warp 0)
+//   7 decode group: decoded tile stored                    (CTA 1, first warp)
+#ifdef QLORA_GEMM_STAMPS
+constexpr int kStampSteps = 4096;
+__device__ unsigned long long d_gemm_stamps[8][kStampSteps];
+#define QLORA_STAMP(row, cta, idx)                                                                    \
+    do {                                                                                              \
+        if (blockIdx.x == (cta) && (idx) < kStampSteps) d_gemm_stamps[row][idx] = globaltimer();        \
+    } while (0)
+#else
+#define QLORA_STAMP(row, cta, idx) \
+    do {                           \
+    } while (0)
+#endif
 
 struct PairCfg {
     static constexpr int SUB = 128;               // rows per CTA per sub-tile
@@ -444,6 +467,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         alive = false;
                         break;
                     }
+                    QLORA_STAMP(0, 0, g);
                     if (it < w.nmain) {
                         mbar_arrive_expect_tx(&full[s], abytes + C::C_BYTES);
                         const int64_t kk = w.kbeg + it;
@@ -499,6 +523,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    QLORA_STAMP(3, 0, g);
                     int nmma = 4;
                     if (it >= w.nmain) {
                         const int rem = p.r - (int)(w.lbeg + it - w.nmain) * C::BK;
@@ -513,6 +538,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         if (w.two) tc_mma2_bf16(tmem + 256, smem_desc_sw128(a1 + kk * 32, 16, 1024), bd, idesc, acc);
                     }
                     tc_commit2_both(&empty[s]);
+                    QLORA_STAMP(4, 0, g);
                 }
                 tc_commit2_both(tfull);
             }
@@ -617,6 +643,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             const int s = (int)(cur.g % C::STAGES);
             const uint32_t par = (uint32_t)(cur.g / C::STAGES) & 1;
             if (!pair_wait(&full[s], par, p.wait_ns, (p.kernel_id << 16) | 2, abort_flag, peer_abort)) break;
+            if (lane == 0 && dw % C::GROUP_WARPS == 0) QLORA_STAMP(1, 0, cur.g);
             if (cur.it < cur.nmain) {
                 uint8_t *wt = wtile(s);
                 const uint8_t *ct = ctile(s);
@@ -639,6 +666,10 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 fence_proxy_async_smem();
             }
             __syncwarp();
+            if (lane == 0 && dw % C::GROUP_WARPS == 0) {
+                QLORA_STAMP(2, 0, cur.g);
+                QLORA_STAMP(7, 1, cur.g);
+            }
             if (lane == 0) mbar_arrive_cluster(ready_addr0 + (uint32_t)(s * 8));
             cur = nxt;
             qv = qn;
@@ -680,6 +711,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         for (; seg_next(p, pl, sw, w); ++tl) {
             if (!pair_wait(tfull, (uint32_t)tl & 1, p.wait_ns, (p.kernel_id << 16) | 5, abort_flag, peer_abort))
                 break;
+            if (ew == 0 && lane == 0) QLORA_STAMP(5, 0, tl);
             tc_fence_after();
             const int nb = w.two ? C::NBATCH : C::NBATCH / 2;
             // a shared tile: contributors h .. h + n - 1, this pair is number m
@@ -769,6 +801,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         // the MMAs of the next segment may overwrite them
                         tc_fence_before();
                         __syncwarp();
+                        if (ew == 0 && lane == 0) QLORA_STAMP(6, 0, tl);
                         if (lane == 0) mbar_arrive_cluster(tempty_addr0);
                     }
                     if (!finish) {

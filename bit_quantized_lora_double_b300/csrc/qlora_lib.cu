@@ -761,6 +761,15 @@ int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lo
     return (n - 4) / 9;
 }
 
+#ifdef QLORA_GEMM_STAMPS
+// Diagnostic build only (not part of the ABI header): copies the fused GEMM's
+// timeline of the last launch (8 rows of kStampSteps globaltimer values, row
+// meanings in gemm_pair.cuh) to `host`; 0 on success.
+int qlora_debug_gemm_stamps(unsigned long long *host) {
+    return cudaMemcpyFromSymbol(host, d_gemm_stamps, sizeof(d_gemm_stamps)) == cudaSuccess ? 0 : 1;
+}
+#endif
+
 const char *qlora_last_error(void) { return t_last_error.c_str(); }
 
 void qlora_set_wait_limit(int64_t microseconds) { g_wait_limit = microseconds > 0 ? microseconds : 0; }

@@ -5,6 +5,13 @@ small, self-contained case to put under a profiler:
   python -m bit_quantized_lora_double_b300.profile_case --projection gate --M 2048 --reps 3
   python -m bit_quantized_lora_double_b300.profile_case --projection gate --M 1 --fwd-only
   python -m bit_quantized_lora_double_b300.profile_case --codec --reps 3   # 14336 x 4096 quantize + dequantize
+  python -m bit_quantized_lora_double_b300.profile_case --workload 3 --projection q --M 4096 --stamps fwd
+
+--stamps fwd|dx builds the diagnostic library (the fused GEMM records
+globaltimer stamps of its first CTA pair; no work is skipped), runs the
+projection and prints the timeline of the last forward (or dX) GEMM launch:
+k-step period, TMA latency as the decoders see it, decode time, how early the
+decoded tiles are ready, the MMA issue time, and the drain at tile ends.
 """
 from __future__ import annotations
 
@@ -25,7 +32,11 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--codec", action="store_true")
+    ap.add_argument("--stamps", choices=["fwd", "dx"], default=None)
     args = ap.parse_args()
+    if args.stamps:
+        from bit_quantized_lora_double_b300 import _build
+        qlora._LIB_PATH = _build.build(stamps=True)
 
     def dev(h):
         return torch.from_numpy(np.ascontiguousarray(h).view(np.int16)).view(torch.bfloat16).cuda()
@@ -71,9 +82,49 @@ def main():
     torch.cuda.synchronize()
     ms, cnt, total = qlora.qlora_profile_stop()
     qlora.qlora_check_device_status()
+    if args.stamps:
+        if args.stamps == "fwd":
+            qlora.qlora_linear_fwd(Xd, M, w, Ad, Bd, r, s, Y, U, ws)
+            seg = qlora.qlora_debug_gemm_segments(M, n, k // 64, (r + 63) // 64, 74)
+        else:
+            qlora.qlora_linear_bwd(dYd, Xd, U, M, w, Ad, Bd, r, s, dX, dA, dB, ws)
+            seg = qlora.qlora_debug_gemm_segments(M, k, (n + 63) // 64, (r + 63) // 64, 74)
+        torch.cuda.synchronize()
+        print_timeline(seg)
     print(json.dumps({"projection": args.projection, "M": M, "N": n, "K": k, "r": r, "reps": args.reps,
                       "ms_per_rep": {kk: v / args.reps for kk, v in ms.items() if cnt[kk]},
                       "launches_per_rep": {kk: v // args.reps for kk, v in cnt.items() if v}}))
+
+
+def print_timeline(seg):
+    """Summary of the diagnostic GEMM timeline of the first CTA pair."""
+    import ctypes
+    L = qlora.lib()
+    L.qlora_debug_gemm_stamps.argtypes = [ctypes.c_void_p]
+    L.qlora_debug_gemm_stamps.restype = ctypes.c_int
+    h = np.zeros(8 * 4096, np.uint64)
+    assert L.qlora_debug_gemm_stamps(h.ctypes.data) == 0
+    h = h.reshape(8, 4096).astype(np.int64)
+    rec = seg[4]
+    mine = rec[rec[:, 0] == 0]  # pair 0's segments
+    steps, tiles = int(mine[:, 5].sum()), len(mine)
+    iss, fl, dec, rdy, cm, pdec = (h[i, :steps] for i in (0, 1, 2, 3, 4, 7))
+    q = lambda a, p: float(np.percentile(a, p))
+    per = np.diff(cm) / 1e3
+    late = np.maximum(dec, pdec)[1:] > cm[:-1]
+    out = {
+        "pair0_steps": steps, "pair0_segments": tiles,
+        "span_us": (cm[-1] - iss[0]) / 1e3,
+        "step_us": {"median": q(per, 50), "mean": float(per.mean()), "p90": q(per, 90)},
+        "tma_landed_after_issue_us": {"median": q((fl - iss) / 1e3, 50), "p90": q((fl - iss) / 1e3, 90)},
+        "decode_us": {"median": q((dec - fl) / 1e3, 50), "p90": q((dec - fl) / 1e3, 90)},
+        "decoded_ahead_of_issuer_us_median": q((rdy - dec) / 1e3, 50),
+        "steps_decoded_late_pct": 100.0 * float(late.mean()),
+        "mma_issue_us_median": q((cm - rdy) / 1e3, 50),
+        "issuer_wait_between_steps_us_median": q((rdy[1:] - cm[:-1]) / 1e3, 50),
+        "tile_drain_us": [float((h[6, t] - h[5, t]) / 1e3) for t in range(tiles) if h[6, t] > h[5, t]],
+    }
+    print(json.dumps({"gemm_timeline": out}))
 
 
 if __name__ == "__main__":
