@@ -339,6 +339,16 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+// 16-byte load through a generic address (shared or global memory), at gpu
+// scope so a global address never reads a stale L1 line.
+__device__ __forceinline__ float4 ld_f4_gpu(const float *p) {
+    float4 v;
+    asm volatile("ld.relaxed.gpu.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -825,39 +835,52 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                             if (alive) fx_waited = gi + 1;
                         }
                         if (!alive) break;
-                        // the n terms in pair order, this pair's own (in v) as term m
-#pragma unroll
-                        for (int jc = 0; jc < 8; ++jc) {
-                            float a[8];
+                        // Pair order, ((P_0 + P_1) + ...) + P_{n-1}, with this
+                        // pair's accumulators (v) as P_m: the terms before P_m
+                        // are first folded, in order, into one buffer Q (P_0's
+                        // piece in the ring, else this pair's own tail slot,
+                        // unused while it finishes this tile); then v = v + Q,
+                        // the same as Q + v, and v += P_{m+1}, ... in order.
+                        auto piece = [&](int j) -> float * {
+                            if (use_ring)
+                                return reinterpret_cast<float *>(
+                                    fixbuf + ((fx0 + b * nq + (j < m ? j : j - 1)) % C::NFIX) * 8192);
+                            return slot_of(h + j, j == 0) + (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
+                        };
+                        float *q = nullptr;
+                        if (m >= 2) {
+                            q = use_ring ? piece(0)
+                                         : slot_of(pair_id, 0) + (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048;
 #pragma unroll 1
-                            for (int j = 0; j < n; ++j) {
-                                float t[8];
-                                if (j == m) {
+                            for (int j = use_ring ? 1 : 0; j < m; ++j) {
+                                const float *src = piece(j);
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) t[e] = __uint_as_float(v[8 * jc + e]);
-                                } else {
-                                    float4 t0, t1;
-                                    if (use_ring) {
-                                        const int gi = fx0 + b * nq + (j < m ? j : j - 1);
-                                        const float *src = reinterpret_cast<const float *>(
-                                                               fixbuf + (gi % C::NFIX) * 8192) + (jc * 32 + lane) * 8;
-                                        t0 = *reinterpret_cast<const float4 *>(src);
-                                        t1 = *reinterpret_cast<const float4 *>(src + 4);
-                                    } else {
-                                        const float *src = slot_of(h + j, j == 0) +
-                                                           (((int64_t)rank * C::EPI_WARPS + ew) * C::NBATCH + b) * 2048 +
-                                                           (jc * 32 + lane) * 8;
-                                        t0 = __ldcg(reinterpret_cast<const float4 *>(src));
-                                        t1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                                for (int jc = 0; jc < 8; ++jc) {
+                                    const int o = (jc * 32 + lane) * 8;
+                                    float4 x0 = ld_f4_gpu(src + o), x1 = ld_f4_gpu(src + o + 4);
+                                    if (j > 0) {
+                                        const float4 y0 = ld_f4_gpu(q + o), y1 = ld_f4_gpu(q + o + 4);
+                                        x0 = make_float4(y0.x + x0.x, y0.y + x0.y, y0.z + x0.z, y0.w + x0.w);
+                                        x1 = make_float4(y1.x + x1.x, y1.y + x1.y, y1.z + x1.z, y1.w + x1.w);
                                     }
-                                    t[0] = t0.x, t[1] = t0.y, t[2] = t0.z, t[3] = t0.w;
-                                    t[4] = t1.x, t[5] = t1.y, t[6] = t1.z, t[7] = t1.w;
+                                    *reinterpret_cast<float4 *>(q + o) = x0;
+                                    *reinterpret_cast<float4 *>(q + o + 4) = x1;
                                 }
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) a[e] = j == 0 ? t[e] : a[e] + t[e];
                             }
+                        }
+#pragma unroll 1
+                        for (int j = 0; j < n; ++j) {
+                            if (j == m || (j > 0 && j < m)) continue;
+                            const float *src = j == 0 && m >= 2 ? q : piece(j);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) v[8 * jc + e] = __float_as_uint(a[e]);
+                            for (int jc = 0; jc < 8; ++jc) {
+                                const float4 a0 = ld_f4_gpu(src + (jc * 32 + lane) * 8);
+                                const float4 a1 = ld_f4_gpu(src + (jc * 32 + lane) * 8 + 4);
+                                const float add[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    v[8 * jc + e] = __float_as_uint(__uint_as_float(v[8 * jc + e]) + add[e]);
+                            }
                         }
                         __syncwarp();  // every lane has read the buffers before they are refilled
                         for (int qi = 0; qi < nq; ++qi) fetch_piece(b * nq + qi + C::NFIX);
