@@ -173,6 +173,12 @@ class Clocks:
                 "interval_ms": self.interval}
 
 
+def workload_name(wl):
+    """The headline workload's name, the same on both arms."""
+    return (wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=%d alpha=%g; groups q/k/v, o, gate/up, down"
+            % (wl["r"], wl["alpha"]))
+
+
 def groups_of(P):
     """Index lists of the projections by LAYER_GROUPS (others alone)."""
     names = [d["name"] for d in P]
@@ -515,19 +521,20 @@ def bench_sweep(qlora, torch, dev, pk):
 
         reps = max(3, min(200, int(2e11 / max(1, M * n * k * 2))))
         if copies > 1:
-            # eager launches (the rotation over weight copies is host-side)
-            for _ in range(5):
-                fwd()
+            # one CUDA graph holding one call per weight copy, replayed: the
+            # device time of the calls (eager launches from Python would be
+            # bound by the host at these sizes); per-kernel times from eager
+            # profiled calls
+            def fwd_all():
+                for _ in range(copies):
+                    fwd()
+            f_ms = graph_time(torch, fwd_all, max(3, reps // copies), 3) / copies
             torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             qlora.qlora_profile_start()
-            a.record()
             for _ in range(reps):
                 fwd()
-            b.record()
             torch.cuda.synchronize()
             pms, pn, _ = qlora.qlora_profile_stop()
-            f_ms = a.elapsed_time(b) / reps
         else:
             f_ms = graph_time(torch, fwd, reps, 3)
         f_fl = 2 * M * n * k + 2 * M * r * (n + k)
@@ -538,6 +545,7 @@ def bench_sweep(qlora, torch, dev, pk):
             gbs = byts / (f_ms * 1e-3) / 1e9
             row.update({"fwd_gbs": gbs, "fwd_pct_hbm": gbs / pk["hbm"], "fwd_bytes": byts,
                         "kernels_ms_per_call": {kk: v / reps for kk, v in pms.items() if pn[kk]},
+                        "kernels_timing": "CUDA events around each launch during eager calls",
                         "l2": "6 rotating weight copies (> L2)"})
         if M >= 128:
             dYd = dv(dY)
@@ -676,7 +684,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w["name"], "M": w["M"], "r": r,
+        "config": {"workload": workload_name(w), "M": w["M"], "r": r,
                    "sample": "1 token of one projection per step (round robin over q,k,v,o,gate,up,down)"},
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "1 token of one projection (round robin over q,k,v,o,gate,up,down) per step"},
@@ -800,8 +808,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "pct_bf16_peak": value / world / pk["bf16"], "pct_bf16_peak_sustained": value / world / pk["bf16_sus"],
-            "config": {"workload": wl["name"] + ": q,k,v,o,gate,up,down NF4+DQ, LoRA r=64 alpha=16; "
-                                   "groups q/k/v, o, gate/up, down",
+            "config": {"workload": workload_name(wl),
                        "M": M, "r": r, "alpha": wl["alpha"], "projections": [[n_, k_] for _, n_, k_ in projs],
                        "flops_per_step": flops, "parallelism": f"dp{world}",
                        "l2": "inputs larger than L2 (several GB touched per step)",

@@ -388,17 +388,17 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
         uint32_t ph = 0;
         zero_acc();
         set_rows(rg);
+        auto mine_at = [&](int i) { return !(i == 0 && warp < wfirst) && !(i == nst - 1 && warp >= wlast); };
+        // the block scales of a stage are requested one stage ahead (a
+        // dependent L2 read in every stage otherwise: ~1 us per stage); the
+        // X fragments, L1 hits after the first stages, with the stage itself
+        float sv_next[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (nst > 0 && mine_at(0)) load_s2(kc, sv_next);
         for (int i = 0; i < nst; ++i) {
-            const bool mine = !(i == 0 && warp < wfirst) && !(i == nst - 1 && warp >= wlast);
-            // this stage's X fragments and scales are requested before the
-            // wait for its codes (fetching them a stage ahead measured no
-            // faster and costs registers the 16-token case does not have)
+            const bool mine = mine_at(i);
             uint4 xv[NT][2];
-            float sv[4];
-            if (alive && mine) {
-                load_x(kc * 16 + warp, xv);
-                load_s2(kc, sv);
-            }
+            float sv[4] = {sv_next[0], sv_next[1], sv_next[2], sv_next[3]};
+            if (alive && mine) load_x(kc * 16 + warp, xv);
             if (alive && !tc_wait(&full[s], ph, p.wait_ns, (10u << 16) | 2, abort_flag)) alive = false;
             if (alive) {
                 if (mine) {
@@ -475,6 +475,7 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
                 zero_acc();
             }
             if (rg_n != rg) set_rows(rg_n);
+            if (alive && i + 1 < nst && mine_at(i + 1)) load_s2(kc_n, sv_next);
             rg = rg_n;
             kc = kc_n;
         }
