@@ -182,7 +182,7 @@ __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, uint64
 }
 
 // Work schedule: data-parallel waves, then a stream-K remainder. The T
-// output tiles of 512 x 256 are numbered band by band (kRowBand row tiles per
+// output tiles of 512 x 256 are numbered band by band (p.band row tiles per
 // band), with the row tiles of a column tile adjacent inside a band; each is
 // S = nk_main + lora_steps k-steps deep. Tiles t < dp_tiles
 // go data-parallel: pair q of the P pairs computes tiles q, q + P, ... whole,
@@ -223,10 +223,12 @@ struct PairSeg {
     bool two;       // the tile has a second 256-row sub-tile
 };
 
-// Row tiles per band of the tile order: the pairs working at the same time
-// touch at most this many row tiles (4096 activation rows at 512-row tiles),
-// so the activations they stream stay in L2 while every column tile passes.
-constexpr int kRowBand = 8;
+// Row tiles per band of the tile order (TcParams::band, chosen per launch by
+// the host): the pairs working at the same time touch at most this many row
+// tiles, so the band's activation rows stay in L2 across the band's
+// data-parallel rounds while every column tile passes; a smaller band reads
+// each weight column tile once per band instead. The host takes the largest
+// band of 8, 4, 2 or 1 row tiles whose activation slice fits kBandBytes.
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -304,12 +306,13 @@ __host__ __device__ __forceinline__ PairSeg pair_seg(const TcParams &p, const Pa
     PairSeg w;
     w.t = g / pl.S;
     const int64_t k0 = g - w.t * pl.S, k1 = min64(pl.S, k0 + (end - g));
-    // tile t -> (row tile, column tile): bands of kRowBand row tiles, the
+    // tile t -> (row tile, column tile): bands of p.band row tiles, the
     // row tiles of a column tile adjacent inside a band
-    const int64_t band = w.t / (kRowBand * pl.nt);
-    const int64_t rows_in = min64(kRowBand, pl.mt - band * kRowBand);
-    const int64_t rb = w.t - band * kRowBand * pl.nt;
-    w.m0 = (band * kRowBand + rb % rows_in) * p.tile_rows;
+    const int64_t rbnd = p.band > 0 ? p.band : 1;
+    const int64_t band = w.t / (rbnd * pl.nt);
+    const int64_t rows_in = min64(rbnd, pl.mt - band * rbnd);
+    const int64_t rb = w.t - band * rbnd * pl.nt;
+    w.m0 = (band * rbnd + rb % rows_in) * p.tile_rows;
     const int64_t ct = rb / rows_in;  // column tile of the launch
     int cg = 0;
     while (cg + 1 < p.ncg && ct >= p.cg_first[cg + 1]) ++cg;

@@ -73,6 +73,7 @@ struct TcParams {
     float *slots;
     int64_t dp_tiles;      // tiles t < dp_tiles run data-parallel, the rest stream-K
     int tile_rows;         // rows per tile: 512 (two 256-row sub-tiles) or 256 (one)
+    int band;              // row tiles per band of the tile order
     uint64_t wait_ns;
     unsigned kernel_id;
 };

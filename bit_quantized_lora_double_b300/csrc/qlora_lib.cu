@@ -495,6 +495,12 @@ GemmSched gemm_sched(int64_t T, int64_t S, int64_t P, bool big_act) {
     return {(T / P - 1) * P, P};
 }
 
+// Activation bytes of one band of row tiles at most (gemm_pair.cuh, tile
+// order): measured on the 70B-shaped layer, bands of 4 row tiles (32 MB) for
+// an 8192-deep contraction and of 1-2 for a 28672-deep one were fastest; bands
+// of 8 re-read a 64 MB activation from DRAM every data-parallel round.
+constexpr int64_t kBandBytes = 32ll << 20;
+
 // Activation operand size above which the stream-K phase is kept short:
 // three quarters of the B300's 126 MB L2.
 constexpr int64_t kBigActBytes = 96ll << 20;
@@ -508,6 +514,9 @@ int64_t gemm_schedule(TcParams &prm, int64_t P) {
     const int64_t nt = cdiv(prm.Nd, PairCfg::BN);
     prm.tile_rows = 4 * nt * cdiv(prm.M, PairCfg::PAIR_M) < P ? PairCfg::PAIR_M / 2 : PairCfg::PAIR_M;
     const bool big_act = prm.M * prm.nk_main * kGemmBK * 2 > kBigActBytes;
+    const int64_t row_tile_bytes = (int64_t)prm.tile_rows * prm.nk_main * kGemmBK * 2;
+    prm.band = 8;
+    while (prm.band > 1 && prm.band * row_tile_bytes > kBandBytes) prm.band /= 2;
     const GemmSched sc =
         gemm_sched(nt * cdiv(prm.M, (int64_t)prm.tile_rows), prm.nk_main + prm.lora_steps, P, big_act);
     prm.dp_tiles = sc.dp_tiles;
