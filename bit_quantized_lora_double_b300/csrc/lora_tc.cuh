@@ -172,20 +172,32 @@ __device__ __forceinline__ void sk_store4(const SkParams &p, int64_t row, int j0
     }
 }
 
-// One launch may carry two problems of the same kind and contraction length
-// (dA and dB): CTAs with blockIdx.x < tiles0 take problem 0 (maps a0, b0),
-// the others problem 1 (maps a1, b1).
+// One launch carries up to kSkMaxJobs problems of the same kind (the same
+// operand majorness) and rank-tile count: CTAs with first[j] <= blockIdx.x <
+// first[j + 1] take problem j (maps a[j], b[j]). The problems share the
+// cluster size (contraction chunks per tile); each splits its own contraction
+// into that many chunks (chunks past its end stream nothing and add zeros).
+constexpr int kSkMaxJobs = 5;
+struct SkMaps {
+    CUtensorMap a[kSkMaxJobs];
+    CUtensorMap b[kSkMaxJobs];
+};
+struct SkBatch {
+    SkParams p[kSkMaxJobs];
+    int first[kSkMaxJobs + 1];
+    int n;
+};
+
 template <int A_MN, int B_MN>
 __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
-    k_lora_skinny(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
-                  const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
-                  const SkParams p0, const SkParams p1, const int tiles0) {
+    k_lora_skinny(const __grid_constant__ SkMaps tm, const __grid_constant__ SkBatch bt) {
     using C = SkCfg;
-    const bool second = (int)blockIdx.x >= tiles0;
-    const SkParams &p = second ? p1 : p0;
-    const CUtensorMap *tm_a = second ? &tm_a1 : &tm_a0;
-    const CUtensorMap *tm_b = second ? &tm_b1 : &tm_b0;
-    const int64_t tile = second ? (int64_t)blockIdx.x - tiles0 : (int64_t)blockIdx.x;
+    int job = 0;
+    while (job + 1 < bt.n && (int)blockIdx.x >= bt.first[job + 1]) ++job;
+    const SkParams &p = bt.p[job];
+    const CUtensorMap *tm_a = &tm.a[job];
+    const CUtensorMap *tm_b = &tm.b[job];
+    const int64_t tile = (int64_t)blockIdx.x - bt.first[job];
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
@@ -239,8 +251,8 @@ __global__ void __launch_bounds__(SkCfg::THREADS, QLORA_SK_MIN_BLOCKS)
     // outputs are visible from here on; the next kernel may start its set-up
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (p0.zero && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
-        for (int i = threadIdx.x; i < p0.nzero; i += blockDim.x) p0.zero[i] = 0u;
+    if (bt.p[0].zero && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < bt.p[0].nzero; i += blockDim.x) bt.p[0].zero[i] = 0u;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----

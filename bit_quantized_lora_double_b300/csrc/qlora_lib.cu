@@ -651,31 +651,41 @@ int64_t skinny_chunks(int64_t clusters, int64_t steps) {
     return 1;
 }
 
-// Launches one skinny problem, or two (j1 != null) of the same kind and
-// contraction length in one grid.
+// Launches up to kSkMaxJobs skinny problems of one kind and rank-tile count
+// (rs[j]: problem j's rank) in one grid; the first launch's problem 0 zeroes
+// `zero` (the stream-K flags of the GEMM that follows).
 template <int A_MN, int B_MN>
-qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsigned id, uint32_t *zero = nullptr,
-                        int nzero = 0) {
+qlora_status run_skinny_jobs(const SkJob *jobs, const int *rs, int n, cudaStream_t s, unsigned id,
+                             uint32_t *zero = nullptr, int nzero = 0) {
+    if (n < 1 || n > kSkMaxJobs) return fail(QLORA_ERR_CUDA, "internal: %d skinny problems in one launch", n);
     const cudaError_t err = smem_attr(k_lora_skinny<A_MN, B_MN>, SkCfg::SMEM_BYTES);
     if (err != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(err));
-    SkJob j1v = j1p ? *j1p : j0;
-    const SkJob *j1 = j1p ? &j1v : nullptr;
-    if (j1 && (j1->pl.L != j0.pl.L || j1->pl.zt != j0.pl.zt))
-        return fail(QLORA_ERR_CUDA, "internal: grouped skinny problems differ in contraction or rank");
-    const int64_t steps = std::max<int64_t>(1, cdiv(j0.pl.L, 64));
-    const int64_t ch0 = skinny_chunks<A_MN, B_MN>((j0.pl.tiles + (j1 ? j1->pl.tiles : 0)) * j0.pl.zt, steps);
-    j0.pl.spc = cdiv(steps, ch0);
-    j0.pl.chunks = cdiv(steps, j0.pl.spc);
-    j1v.pl.spc = j0.pl.spc;
-    j1v.pl.chunks = j0.pl.chunks;
-    const SkJob &jb = j1 ? *j1 : j0;
-    SkParams p0 = sk_params(j0, r, id);
-    const SkParams p1 = sk_params(jb, r, id);
-    p0.zero = zero;
-    p0.nzero = nzero;
-    const int tiles0 = (int)j0.pl.tiles;
+    int64_t tiles = 0, max_steps = 1;
+    for (int j = 0; j < n; ++j) {
+        if (jobs[j].pl.zt != jobs[0].pl.zt)
+            return fail(QLORA_ERR_CUDA, "internal: batched skinny problems differ in rank tiles");
+        tiles += jobs[j].pl.tiles;
+        max_steps = std::max<int64_t>(max_steps, cdiv(jobs[j].pl.L, 64));
+    }
+    const int64_t chunks = skinny_chunks<A_MN, B_MN>(tiles * jobs[0].pl.zt, max_steps);
+    SkMaps tm;
+    memset(&tm, 0, sizeof tm);
+    SkBatch bt;
+    memset(&bt, 0, sizeof bt);
+    bt.n = n;
+    for (int j = 0; j < n; ++j) {
+        SkJob jb = jobs[j];
+        jb.pl.spc = std::max<int64_t>(1, cdiv(std::max<int64_t>(1, cdiv(jb.pl.L, 64)), chunks));
+        jb.pl.chunks = chunks;
+        tm.a[j] = *jb.ta;
+        tm.b[j] = *jb.tb;
+        bt.p[j] = sk_params(jb, rs[j], id);
+        bt.first[j + 1] = bt.first[j] + (int)jb.pl.tiles;
+    }
+    bt.p[0].zero = zero;
+    bt.p[0].nzero = nzero;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(j0.pl.tiles + (j1 ? j1->pl.tiles : 0)), (unsigned)j0.pl.chunks, (unsigned)j0.pl.zt);
+    cfg.gridDim = dim3((unsigned)tiles, (unsigned)chunks, (unsigned)jobs[0].pl.zt);
     cfg.blockDim = dim3(SkCfg::THREADS);
     cfg.dynamicSmemBytes = SkCfg::SMEM_BYTES;
     cfg.stream = s;
@@ -684,14 +694,14 @@ qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsig
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = (unsigned)j0.pl.chunks;
+    attr[1].val.clusterDim.y = (unsigned)chunks;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = j0.pl.chunks > 1 ? 2 : 1;
+    cfg.numAttrs = chunks > 1 ? 2 : 1;
     cudaError_t e;
     {
-        ProfScope ps(j0.mode >= kRedDA ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
-        e = cudaLaunchKernelEx(&cfg, k_lora_skinny<A_MN, B_MN>, *j0.ta, *j0.tb, *jb.ta, *jb.tb, p0, p1, tiles0);
+        ProfScope ps(jobs[0].mode >= kRedDA ? QLORA_KERNEL_GRADS : QLORA_KERNEL_LORA_PRE, s);
+        e = cudaLaunchKernelEx(&cfg, k_lora_skinny<A_MN, B_MN>, tm, bt);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -700,26 +710,13 @@ qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsig
     return launch_check("k_lora_skinny");
 }
 
-// Runs same-kind skinny problems, two per launch where their contraction
-// lengths agree; the first launch zeroes `zero` (the stream-K flags).
+// One skinny problem, or two (j1 != null) of the same kind and rank.
 template <int A_MN, int B_MN>
-qlora_status run_skinny_list(SkJob *jobs, int nj, int r, cudaStream_t s, unsigned id, uint32_t *zero,
-                                    int nzero) {
-    bool done[kMaxGroup] = {};
-    for (int i = 0; i < nj; ++i) {
-        if (done[i]) continue;
-        done[i] = true;
-        int mate = -1;
-        for (int j = i + 1; j < nj && mate < 0; ++j)
-            if (!done[j] && jobs[j].pl.L == jobs[i].pl.L && jobs[j].pl.zt == jobs[i].pl.zt) mate = j;
-        if (mate >= 0) done[mate] = true;
-        const qlora_status st =
-            run_skinny<A_MN, B_MN>(jobs[i], mate >= 0 ? &jobs[mate] : nullptr, r, s, id, zero, nzero);
-        if (st) return st;
-        zero = nullptr;
-        nzero = 0;
-    }
-    return QLORA_OK;
+qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsigned id, uint32_t *zero = nullptr,
+                        int nzero = 0) {
+    const SkJob jobs[2] = {j0, j1p ? *j1p : j0};
+    const int rs[2] = {r, r};
+    return run_skinny_jobs<A_MN, B_MN>(jobs, rs, j1p ? 2 : 1, s, id, zero, nzero);
 }
 
 }  // namespace
@@ -1739,7 +1736,10 @@ static qlora_status group_bwd_impl(const void *X, const void *U_saved, int64_t M
     prm.nk_main = prm.kg_first[n];
     prm.lora_steps = (int)cdiv(R, 64);
     prm.r = (int)R;
-    if ((st = run_skinny_list<0, 1>(vj, n, r, s, 4, gw.sk.flags, kSkFlagWords))) return st;
+    int rsv[kSkMaxJobs];
+    for (int g = 0; g < kSkMaxJobs; ++g) rsv[g] = r;
+    // every projection's V in one launch
+    if ((st = run_skinny_jobs<0, 1>(vj, rsv, n, s, 4, gw.sk.flags, kSkFlagWords))) return st;
     if (!U16) {
         // U recomputed for all projections in one pass as X A^T (A stacked)
         if ((st = run_skinny<0, 0>(SkJob{&tmXk, &gm.lw[0], sk_plan(M, K, (int)R), kRedV, 1.0f, nullptr, 0, gw.U,
@@ -1761,10 +1761,24 @@ static qlora_status group_bwd_impl(const void *X, const void *U_saved, int64_t M
         dA_contiguous = dA_contiguous &&
                         reinterpret_cast<char *>(proj[g].dA) == reinterpret_cast<char *>(proj[0].dA) + g * abytes;
     float *dAdst = dA_contiguous ? proj[0].dA : gw.dAcat;
-    if ((st = run_skinny<1, 1>(SkJob{&tmXmn, &tmVmn, sk_plan(K, M, (int)R), kRedDA, 1.0f, nullptr, 0, nullptr, 0, dAdst},
-                               nullptr, (int)R, s, 5)))
-        return st;
-    if ((st = run_skinny_list<1, 1>(bj, n, r, s, 5, nullptr, 0))) return st;
+    // dA of all projections (rank n r) and every projection's dB in one
+    // launch when their ranks take the same number of 64-wide tiles, else dA
+    // in one launch and the dB in another
+    SkJob gj[kSkMaxJobs];
+    int rsg[kSkMaxJobs];
+    gj[0] = SkJob{&tmXmn, &tmVmn, sk_plan(K, M, (int)R), kRedDA, 1.0f, nullptr, 0, nullptr, 0, dAdst};
+    rsg[0] = (int)R;
+    const bool together = gj[0].pl.zt == bj[0].pl.zt && n + 1 <= kSkMaxJobs;
+    if (together) {
+        for (int g = 0; g < n; ++g) {
+            gj[1 + g] = bj[g];
+            rsg[1 + g] = r;
+        }
+        if ((st = run_skinny_jobs<1, 1>(gj, rsg, n + 1, s, 5))) return st;
+    } else {
+        if ((st = run_skinny_jobs<1, 1>(gj, rsg, 1, s, 5))) return st;
+        if ((st = run_skinny_jobs<1, 1>(bj, rsv, n, s, 5))) return st;
+    }
     if (!dA_contiguous)
         for (int g = 0; g < n; ++g)
             if (cudaMemcpyAsync(proj[g].dA, reinterpret_cast<char *>(gw.dAcat) + g * abytes, abytes,
