@@ -6,7 +6,9 @@ projections) with the linear layer's bar: relative Frobenius error <= 5e-3
 per output tensor. Shapes cover the tensor-core paths (one fused GEMM over all
 projections' columns, or rows for dX), ragged N and M, groups of one to four,
 the few-token paths (projections one by one), U recomputed in the backward,
-and adapters given back to back or apart.
+adapters given back to back or apart, and the batched side-path launches (all
+V passes of a group in one launch; dA with every dB in one launch when their
+ranks take the same number of 64-wide tiles, up to five problems).
 """
 import numpy as np
 import pytest
@@ -83,6 +85,7 @@ def run_group(g, oracle, M, Ns, K, r, scale, seed, save_u=True, packed=False, ro
     (200, [2048, 2048], 512, 8, 1.0, False, False),         # gate/up-shaped, ragged M, U recomputed
     (130, [296, 136], 256, 16, 0.5, True, False),           # N not multiples of 64 or 256
     (256, [512, 384, 256, 128], 512, 64, 0.25, True, True), # four projections, r = 64
+    (200, [256, 128, 384, 128], 512, 16, 1.0, False, False),  # four, r = 16: dA and the four dB in one launch
     (96, [640], 768, 24, 2.0, True, False),                 # a group of one, r = 24
 ])
 def test_group_parity(g, oracle, M, Ns, K, r, scale, save_u, packed):
