@@ -36,8 +36,8 @@ __global__ void __launch_bounds__(kDownThreads) k_lora_down(const uint16_t *__re
                                                             uint16_t *__restrict__ U, int ldu,
                                                             uint16_t *__restrict__ sU, int lds,
                                                             uint32_t *__restrict__ zero = nullptr, int nzero = 0) {
-    // a forward launched as a programmatic dependent (the few-token kernel)
-    // may start streaming its weights now; it waits for U before using it
+    // a forward launched as a programmatic dependent may start now; it
+    // waits for U before using it
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (zero && blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;

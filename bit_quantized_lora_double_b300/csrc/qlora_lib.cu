@@ -284,37 +284,28 @@ SkArea take_sk_area(Carve &c) {
 }
 
 // The few-token forward (k_fwd_few) serves M <= 16 when K is a multiple of
-// its 1024-deep stages (and the block count fits 31 bits); other few-token
+// its 256-deep tasks (and the block count fits 31 bits); other few-token
 // shapes take k_fwd_small.
 inline bool few_path(int64_t M, int64_t N, int64_t K) {
-    return M <= 8 * FewCfg::MAX_NT && K % FewCfg::KSTAGE == 0 && N * (K / kBlock) < (int64_t(1) << 31);
+    return M <= 8 * FewCfg::MAX_NT && K % FewCfg::TK == 0 && N * (K / kBlock) < (int64_t(1) << 31);
 }
 
-// Its grid: one CTA per SM, more when a CTA's share of the slices would touch
-// more row groups than its shared memory holds sums (or rows of B) for.
+// Its split: tasks of 32 rows x 256 k over at most 16 warps on each of 148
+// CTAs, every warp at least one task.
 struct FewPlan {
-    int64_t grid, slices, spg, groups;
+    int64_t grid, warps, tasks, tpr, tiles;
 };
-FewPlan few_plan(int64_t N, int64_t K, int r) {
-    const int64_t max_groups = std::min<int64_t>(FewCfg::MAX_GROUPS, FewCfg::B_BYTES / (FewCfg::ROWS * 2 * r));
+FewPlan few_plan(int64_t N, int64_t K) {
     FewPlan f;
-    f.groups = cdiv(N, FewCfg::ROWS);
-    f.spg = K / FewCfg::KSTAGE;
-    f.slices = f.groups * f.spg * FewCfg::WARPS;
-    int64_t G = std::min<int64_t>(FewCfg::GRID, f.slices);
-    while (true) {
-        int64_t worst = 0;
-        for (int64_t c = 0; c < G; ++c) {
-            int64_t g0, ng;
-            few_groups(c, G, f.slices, f.spg, g0, ng);
-            worst = std::max(worst, ng);
-        }
-        if (worst <= max_groups || G >= f.slices) break;
-        G = std::min(f.slices, G + FewCfg::GRID);
-    }
-    f.grid = G;
+    f.tiles = cdiv(N, FewCfg::ROWS);
+    f.tpr = K / FewCfg::TK;
+    f.tasks = f.tiles * f.tpr;
+    f.warps = std::min<int64_t>(f.tasks, (int64_t)FewCfg::WARPS * FewCfg::GRID);
+    f.grid = cdiv(f.warps, FewCfg::WARPS);
     return f;
 }
+// fp32 slot floats per warp: two row tiles x 32 lanes x 8 per 8-token tile
+inline size_t few_slot_floats(int64_t M) { return (size_t)2 * 32 * 8 * (M <= 8 ? 1 : 2); }
 
 struct FwdWs {
     uint16_t *sU, *Bp;
@@ -327,10 +318,10 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     Carve c(ws);
     FwdWs f{};
     if (few_path(M, N, K)) {
-        const FewPlan fp = few_plan(N, K, r);
+        const FewPlan fp = few_plan(N, K);
         f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
-        f.few_slots = c.take<float>((size_t)fp.grid * 2 * FewCfg::SUM_FLOATS);
-        f.few_counters = c.take<uint32_t>((size_t)fp.groups);
+        f.few_slots = c.take<float>((size_t)fp.warps * few_slot_floats(M));
+        f.few_counters = c.take<uint32_t>((size_t)fp.tiles);
     } else if (!tc) {
         f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
     } else {
@@ -774,6 +765,11 @@ int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lo
 int qlora_debug_gemm_stamps(unsigned long long *host) {
     return cudaMemcpyFromSymbol(host, d_gemm_stamps, sizeof(d_gemm_stamps)) == cudaSuccess ? 0 : 1;
 }
+// The few-token forward's per-warp timeline of the last launch
+// (kFewStampWarps x 16 values, columns in fwd_few.cuh); 0 on success.
+int qlora_debug_few_stamps(unsigned long long *host) {
+    return cudaMemcpyFromSymbol(host, d_few_stamps, sizeof(d_few_stamps)) == cudaSuccess ? 0 : 1;
+}
 #endif
 
 const char *qlora_last_error(void) { return t_last_error.c_str(); }
@@ -1089,33 +1085,42 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         const cudaError_t aerr = smem_attr(kern, FewCfg::SMEM_BYTES);
         if (aerr != cudaSuccess)
             return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
-        const FewPlan fp = few_plan(N, K, r);
+        const FewPlan fp = few_plan(N, K);
         {
+            // a programmatic dependent of the preceding kernel (it waits for
+            // that grid before touching memory): its launch overlaps the
+            // preceding kernel's end
+            cudaLaunchConfig_t dc = {};
+            dc.gridDim = dim3((unsigned)M, (unsigned)r);
+            dc.blockDim = dim3(kFewDownThreads);
+            dc.stream = s;
+            cudaLaunchAttribute da[1];
+            da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            da[0].val.programmaticStreamSerializationAllowed = 1;
+            dc.attrs = da;
+            dc.numAttrs = 1;
             ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            k_lora_down<<<(unsigned)(M * rp), kDownThreads, 0, s>>>(X16, M, K, static_cast<const uint16_t *>(A), r,
-                                                                 scale, U16, ldu, f.sU, rp, f.few_counters,
-                                                                 (int)fp.groups);
+            const cudaError_t de = cudaLaunchKernelEx(&dc, k_few_down, X16, (int64_t)K, static_cast<const uint16_t *>(A),
+                                                      r, scale, U16, ldu, f.sU, rp, f.few_counters, (int)fp.tiles);
+            if (de != cudaSuccess) {
+                cudaGetLastError();
+                return fail(QLORA_ERR_CUDA, "k_few_down: launch failed: %s", cudaGetErrorString(de));
+            }
         }
-        if ((st = launch_check("k_lora_down"))) return st;
-        CUtensorMap tmC, tmQ;
-        // code boxes of 128 bytes x 32 rows (FewCfg::BOX_BYTES, what the kernel
-        // expects per box), 128-byte swizzle
-        static_assert(FewCfg::BOX_BYTES == 128 * FewCfg::ROWS, "code box");
+        if ((st = launch_check("k_few_down"))) return st;
+        CUtensorMap tmC;
+        // code boxes of 128 bytes x 32 rows (FewCfg::TASK_BYTES, one task),
+        // 128-byte swizzle
+        static_assert(FewCfg::TASK_BYTES == 128 * FewCfg::ROWS, "code box");
         if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 128, FewCfg::ROWS,
                            CU_TENSOR_MAP_SWIZZLE_128B, "codes")))
-            return st;
-        // fp32 absmax: the kernel issues no absmax-code boxes and the second
-        // map is never used
-        if (w.absmax)
-            tmQ = tmC;
-        else if ((st = make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.q, K / kBlock, N, K / kBlock, 16,
-                                FewCfg::ROWS, CU_TENSOR_MAP_SWIZZLE_NONE, "absmax codes")))
             return st;
         FewParams prm{};
         prm.X = X16;
         prm.M = M;
         prm.N = N;
         prm.K = K;
+        prm.q = w.q;
         prm.s2 = w.s2;
         prm.mean = w.mean;
         prm.sU = f.sU;
@@ -1125,9 +1130,14 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         prm.Y = static_cast<uint16_t *>(Y);
         prm.slots = f.few_slots;
         prm.counters = f.few_counters;
-        prm.slices = fp.slices;
-        prm.spg = fp.spg;
+        prm.tasks = fp.tasks;
+        prm.tpr = fp.tpr;
+        prm.warps = fp.warps;
         prm.wait_ns = wait_ns();
+        {
+            static const float kLevels[2][16] = {QLORA_NF4_LEVELS, QLORA_INT4_LEVELS};
+            memcpy(prm.levels, kLevels[w.tab], sizeof prm.levels);
+        }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)fp.grid);
         cfg.blockDim = dim3(FewCfg::THREADS);
@@ -1141,7 +1151,7 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         cudaError_t e;
         {
             ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
-            e = cudaLaunchKernelEx(&cfg, kern, tmC, tmQ, prm, (const float *)w.absmax, w.tab);
+            e = cudaLaunchKernelEx(&cfg, kern, tmC, prm, (const float *)w.absmax);
         }
         if (e != cudaSuccess) {
             cudaGetLastError();

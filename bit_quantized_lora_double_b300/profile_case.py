@@ -32,7 +32,7 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--codec", action="store_true")
-    ap.add_argument("--stamps", choices=["fwd", "dx"], default=None)
+    ap.add_argument("--stamps", choices=["fwd", "dx", "few"], default=None)
     args = ap.parse_args()
     if args.stamps:
         from bit_quantized_lora_double_b300 import _build
@@ -82,7 +82,11 @@ def main():
     torch.cuda.synchronize()
     ms, cnt, total = qlora.qlora_profile_stop()
     qlora.qlora_check_device_status()
-    if args.stamps:
+    if args.stamps == "few":
+        qlora.qlora_linear_fwd(Xd, M, w, Ad, Bd, r, s, Y, U, ws)
+        torch.cuda.synchronize()
+        print_few_timeline()
+    elif args.stamps:
         if args.stamps == "fwd":
             qlora.qlora_linear_fwd(Xd, M, w, Ad, Bd, r, s, Y, U, ws)
             seg = qlora.qlora_debug_gemm_segments(M, n, k // 64, (r + 63) // 64, 74)
@@ -125,6 +129,38 @@ def print_timeline(seg):
         "tile_drain_us": [float((h[6, t] - h[5, t]) / 1e3) for t in range(tiles) if h[6, t] > h[5, t]],
     }
     print(json.dumps({"gemm_timeline": out}))
+
+
+def print_few_timeline():
+    """Summary of the few-token forward's per-warp timeline (us from the
+    earliest warp's entry): percentiles over warps of each event."""
+    import ctypes
+    L = qlora.lib()
+    L.qlora_debug_few_stamps.argtypes = [ctypes.c_void_p]
+    L.qlora_debug_few_stamps.restype = ctypes.c_int
+    h = np.zeros(148 * 16 * 16, np.uint64)  # at least the device array
+    assert L.qlora_debug_few_stamps(h.ctypes.data) == 0
+    h = h.reshape(-1, 16).astype(np.int64)
+    last = h[:, 0].max()
+    h = h[(h[:, 0] > 0) & (h[:, 0] > last - 10**6) & (h[:, 14] >= h[:, 0])]
+    t0 = h[:, 0].min()
+    rel = lambda c: (h[:, c] - t0) / 1e3
+    pct = lambda a: {p: round(float(np.percentile(a, p)), 2) for p in (0, 10, 50, 90, 100)}
+    out = {"warps": int(len(h)), "entry": pct(rel(0)), "after_start_barrier": pct(rel(1))}
+    for i in range(4):
+        ok = h[:, 2 + 2 * i] >= h[:, 0]
+        if ok.sum() == 0:
+            break
+        out[f"task{i}_landed"] = pct(rel(2 + 2 * i)[ok])
+        out[f"task{i}_decode_us"] = pct(((h[:, 3 + 2 * i] - h[:, 2 + 2 * i]) / 1e3)[ok])
+    for e in range(2):
+        ok = h[:, 11 + 2 * e] >= h[:, 10 + 2 * e]
+        ok &= h[:, 10 + 2 * e] >= h[:, 0]
+        if ok.sum():
+            out[f"tile_end{e}_us"] = pct(((h[:, 11 + 2 * e] - h[:, 10 + 2 * e]) / 1e3)[ok])
+    out["stream_done"] = pct(rel(14))
+    out["warps_finishing_tiles"] = int((h[:, 15] > 0).sum())
+    print(json.dumps({"few_timeline": out}))
 
 
 if __name__ == "__main__":

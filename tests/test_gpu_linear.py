@@ -75,14 +75,17 @@ def run_and_check(g, oracle, M, N, K, r, scale, seed, **kw):
     (2048, 128, 9728, 16, 2.0),    # dX: the same split on the backward
     (2148, 4000, 192, 8, 1.0),     # stream-K over 80 tiles, 100-row last row tile, ragged N
     (4708, 2048, 128, 8, 1.0),     # ten row tiles: two bands of the tile order, the second partial
-    # persistent few-token forward (M <= 16, K a multiple of 1024):
-    (1, 4096, 1024, 16, 2.0),      # one token, 128 row groups of 32 over 148 CTAs
+    # few-token forward (M <= 16, K a multiple of 256; tasks of 32 rows x 256 k,
+    # one pipeline per warp, row tiles shared between warps finished by the last):
+    (1, 4096, 1024, 16, 2.0),      # one token, 512 tasks on 512 warps: four warps per row tile
     (16, 14336, 4096, 16, 2.0),    # the gate projection at 16 tokens
-    (5, 1000, 2048, 8, 2.0),       # ragged N (last row group of 8 rows), r % 8 == 0
-    (9, 96, 4096, 5, 2.0),         # 96 slices on 96 CTAs: every row group shared by 32 CTAs
-    (2, 33, 1024, 16, 2.0),        # a row group with one valid row
+    (5, 1000, 2048, 8, 2.0),       # ragged N (last row tile of 8 rows), r % 8 == 0
+    (9, 96, 4096, 5, 2.0),         # 48 tasks on 48 warps: every row tile shared by 16 warps, odd r
+    (2, 33, 1024, 16, 2.0),        # a row tile with one valid row
     (1, 1, 1024, 3, 2.0),          # a single weight row
-    (12, 520, 3072, 64, 0.25),     # rank 64, three stages per row group
+    (12, 520, 3072, 64, 0.25),     # rank 64: four LoRA steps in the finishing
+    (3, 700, 256, 16, 2.0),        # K = 256: one task per row tile, every tile finished by its own warp
+    (16, 4096, 14336, 16, 1.0),    # 8B down projection: ~20 warps per row tile (several slot chunks)
 ])
 def test_fwd_bwd_parity(g, oracle, M, N, K, r, scale):
     run_and_check(g, oracle, M, N, K, r, scale, seed=3000 + M + N + r)
