@@ -150,6 +150,14 @@ __device__ __forceinline__ uint32_t few_lut(uint32_t w, uint32_t lanebase) {
     return v;
 }
 
+// arrival on a row tile's counter: release of this warp's slot stores,
+// acquire of the other contributors' (whoever arrives last reads them)
+__device__ __forceinline__ uint32_t few_atom_add_acq_rel(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // D = A * B (+ D): mma.sync without side effects, so that the compiler may
 // interleave it with the table lookups
 __device__ __forceinline__ void few_mma_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -423,18 +431,19 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < NT; ++j)
                 __stcg(mine + rt * NT + j, make_float4(acc[rt][j][0], acc[rt][j][1], acc[rt][j][2], acc[rt][j][3]));
-        __threadfence();
+        // the warp barrier orders every lane's stores before lane 0's
+        // release (and its acquire before every lane's loads below)
         __syncwarp();
         uint32_t old = 0;
-        if (lane == 0) old = atomicAdd(p.counters + rtile, 1u);
+        if (lane == 0) old = few_atom_add_acq_rel(p.counters + rtile, 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
+        __syncwarp();
         const uint32_t wa = few_owner(a, W, T), wb = few_owner(b - 1, W, T);
         if (old != (uint32_t)(wb - wa)) return;
         // last to arrive: every contributor's slot. The first contributor's
         // range may start before the tile (then the tile is its last: slot
         // 1); every later one starts inside it (slot 0). Loads of a chunk
         // of contributors are in flight together; the sum runs in warp order.
-        __threadfence();
         ++n_fin;
         const int ea = few_begin(wa, W, T) == a ? 0 : 1;
         constexpr int CH = 4 / NT;
