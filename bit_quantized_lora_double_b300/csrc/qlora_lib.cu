@@ -716,6 +716,27 @@ extern "C" {
 
 const char *qlora_version(void) { return "qlora-b300 0.1 (sm_103a)"; }
 
+int64_t qlora_debug_few_split(int64_t N, int64_t K, int64_t *out, int64_t cap) {
+    if (N < 1 || K < FewCfg::TK || K % FewCfg::TK || !out || N * (K / kBlock) >= (int64_t(1) << 31)) return -2;
+    const FewPlan f = few_plan(N, K);
+    const int64_t need = 4 + 2 * f.warps + 2 * f.tiles;
+    if (cap < need) return -1;
+    const uint32_t T = (uint32_t)f.tasks, W = (uint32_t)f.warps, P = (uint32_t)f.tpr;
+    out[0] = f.tasks;
+    out[1] = f.warps;
+    out[2] = f.tpr;
+    out[3] = f.tiles;
+    for (uint32_t w = 0; w < W; ++w) {
+        out[4 + 2 * w] = few_begin(w, W, T);
+        out[5 + 2 * w] = few_begin(w + 1, W, T);
+    }
+    for (int64_t t = 0; t < f.tiles; ++t) {
+        out[4 + 2 * f.warps + 2 * t] = few_owner((uint32_t)t * P, W, T);
+        out[5 + 2 * f.warps + 2 * t] = few_owner((uint32_t)(t + 1) * P - 1, W, T);
+    }
+    return need;
+}
+
 int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lora_steps, int pairs_resident,
                                   int64_t *out, int64_t cap) {
     if (M < 1 || Nd < 1 || nk_main < 0 || lora_steps < 0 || nk_main + lora_steps < 1 || pairs_resident < 1 ||

@@ -31,7 +31,7 @@ EXPORTS = [
     "qlora_nf4_dequantize",
     "qlora_linear_fwd_workspace", "qlora_linear_bwd_workspace", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_last_error", "qlora_check_device_status", "qlora_set_wait_limit", "qlora_version",
-    "qlora_profile_start", "qlora_profile_stop", "qlora_debug_gemm_segments",
+    "qlora_profile_start", "qlora_profile_stop", "qlora_debug_gemm_segments", "qlora_debug_few_split",
     "qlora_lora_merge_workspace", "qlora_lora_merge_requantize", "qlora_adamw_step",
     "qlora_q4_table", "qlora_q4_quantize", "qlora_q4_dequantize", "qlora_q4_linear_fwd_workspace",
     "qlora_q4_linear_bwd_workspace", "qlora_q4_linear_fwd", "qlora_q4_linear_bwd",
@@ -140,6 +140,8 @@ def lib():
         L.qlora_group_bwd.argtypes = [vp, vp, i64, P, i32, i32, f32, vp, vp, sz, vp]
         L.qlora_debug_gemm_segments.restype = i64
         L.qlora_debug_gemm_segments.argtypes = [i64, i64, i64, i32, i32, vp, i64]
+        L.qlora_debug_few_split.restype = i64
+        L.qlora_debug_few_split.argtypes = [i64, i64, vp, i64]
         _lib = L
     return _lib
 
@@ -437,6 +439,23 @@ def qlora_debug_gemm_segments(M: int, Nd: int, nk_main: int, lora_steps: int, pa
         if n != -1:
             raise QloraError(2, "qlora_debug_gemm_segments: invalid arguments")
         cap *= 4
+
+
+def qlora_debug_few_split(N: int, K: int):
+    """The few-token forward's split of an N x K weight (host computation, no
+    GPU): returns (tasks, warps, P, tiles, ranges, tile_warps), ranges an
+    int64 array [warps, 2] of each warp's task range [first, end) and
+    tile_warps [tiles, 2] each row tile's first and last contributing warp.
+    Raises QloraError(QLORA_ERR_SHAPE) on bad input."""
+    import numpy as np
+    cap = 4 + 2 * 16 * 148 + 2 * ((int(N) + 31) // 32)
+    out = np.zeros(cap, np.int64)
+    n = lib().qlora_debug_few_split(int(N), int(K), out.ctypes.data, cap)
+    if n < 0:
+        raise QloraError(2, "qlora_debug_few_split: invalid arguments")
+    T, W, P, tiles = (int(v) for v in out[:4])
+    return (T, W, P, tiles, out[4:4 + 2 * W].reshape(W, 2).copy(),
+            out[4 + 2 * W:4 + 2 * W + 2 * tiles].reshape(tiles, 2).copy())
 
 
 def qlora_profile_start():
