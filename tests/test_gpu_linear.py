@@ -85,6 +85,8 @@ def run_and_check(g, oracle, M, N, K, r, scale, seed, **kw):
     (1, 1, 1024, 3, 2.0),          # a single weight row
     (12, 520, 3072, 64, 0.25),     # rank 64: four LoRA steps in the finishing
     (3, 700, 256, 16, 2.0),        # K = 256: one task per row tile, every tile finished by its own warp
+    (4, 256, 1024, 128, 0.5),      # largest rank: eight LoRA steps in the finishing, 128 sU CTAs a token
+    (16, 64, 512, 128, 0.5),       # sixteen tokens at the largest rank
     (16, 4096, 14336, 16, 1.0),    # 8B down projection: ~20 warps per row tile (several slot chunks)
 ])
 def test_fwd_bwd_parity(g, oracle, M, N, K, r, scale):

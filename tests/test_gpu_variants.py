@@ -106,7 +106,7 @@ def _linear(g, oracle, table, dq, M, N, K, r, scale, seed, bwd=True):
 @pytest.mark.parametrize("M,N,K,r,scale", [
     (5, 1000, 2048, 8, 2.0),      # few-token kernel, one 8-token tile; CUDA-core backward
     (13, 520, 1024, 16, 1.0),     # few-token kernel, two tiles
-    (24, 300, 320, 5, 2.0),       # small-M kernel (K not a multiple of 1024)
+    (24, 300, 320, 5, 2.0),       # small-M kernel (M > 16, K not a multiple of 256)
     (200, 384, 512, 16, 2.0),     # tensor-core GEMM forward and backward
 ])
 def test_linear_parity(g, oracle, table, dq, M, N, K, r, scale):
