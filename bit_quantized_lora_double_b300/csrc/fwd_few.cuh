@@ -489,6 +489,24 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     uint32_t rt = t0 / P, kc = t0 - rt * P;
     Scales cur, nxt;
     load_scales(t0, cur);
+    // X^T fragments of one block (k-chunk kc2, block b2). With one 8-token
+    // tile they are requested one block ahead of their use, so that a read
+    // from L2 overlaps a block's decode (with two, the registers are short).
+    auto load_x = [&](uint32_t kc2, int b2, uint4 (&xv)[NT][2]) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            if (xb[j]) {
+                const uint4 *xp = reinterpret_cast<const uint4 *>(xb[j] + kc2 * C::TK + b2 * kBlock);
+                xv[j][0] = __ldg(xp);
+                xv[j][1] = __ldg(xp + 1);
+            } else {
+                xv[j][0] = xv[j][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    };
+    constexpr bool kXpf = NT == 1;
+    uint4 xcur[NT][2];
+    if (kXpf) load_x(kc, 0, xcur);
     for (int i = 0; i < n; ++i) {
         const int s = i % S;
         const uint32_t par = (uint32_t)(i / S) & 1u;
@@ -507,16 +525,21 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
         const uint8_t *sl = sp(slot_of(s));
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            uint4 xv[NT][2];
+            uint4 xv[NT][2], xn[NT][2];
+            if (kXpf) {
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                if (xb[j]) {
-                    const uint4 *xp = reinterpret_cast<const uint4 *>(xb[j] + kc * C::TK + b * kBlock);
-                    xv[j][0] = __ldg(xp);
-                    xv[j][1] = __ldg(xp + 1);
-                } else {
-                    xv[j][0] = xv[j][1] = make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < NT; ++j) {
+                    xv[j][0] = xcur[j][0];
+                    xv[j][1] = xcur[j][1];
                 }
+                // the next block's fragments: this task's block b + 1, or the
+                // next task's first block (k-chunk kc + 1, or 0 in a new tile)
+                if (b < 3)
+                    load_x(kc, b + 1, xn);
+                else if (i + 1 < n)
+                    load_x(kc + 1 == P ? 0u : kc + 1, 0, xn);
+            } else {
+                load_x(kc, b, xv);
             }
             uint2 cw[4];
 #pragma unroll
@@ -574,6 +597,12 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
                     acc[r2][j][1] = fmaf(ap[2 * r2], blk[r2][j][1], acc[r2][j][1]);
                     acc[r2][j][2] = fmaf(ap[2 * r2 + 1], blk[r2][j][2], acc[r2][j][2]);
                     acc[r2][j][3] = fmaf(ap[2 * r2 + 1], blk[r2][j][3], acc[r2][j][3]);
+                }
+            if (kXpf)
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    xcur[j][0] = xn[j][0];
+                    xcur[j][1] = xn[j][1];
                 }
         }
         if (i < 4) QLORA_FEW_STAMP(gw, 3 + 2 * i);
