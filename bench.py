@@ -334,11 +334,48 @@ def roofline_of(kind_ms, kind_n, graph_ms, M, projections, r, pk, clocks):
                       "that the kinds sum to the graph-timed ms_per_step"}
 
 
+def pcie_rates(torch, dev, nbytes=512 << 20):
+    """Pinned host <-> device copy rates of this machine (GB/s): each direction
+    alone and both at once on two streams (best of three), the roofline of
+    the end-to-end leg."""
+    import time
+    n = nbytes // 2
+    h1 = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    h2 = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    d1 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    d2 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d1.copy_(h1, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    def best(*fns):
+        for f in fns:
+            f()
+        torch.cuda.synchronize()
+        t = 1e9
+        for _ in range(3):
+            a = time.perf_counter()
+            for f in fns:
+                f()
+            torch.cuda.synchronize()
+            t = min(t, time.perf_counter() - a)
+        return t
+    th, td, tb = best(h2d), best(d2h), best(h2d, d2h)
+    del h1, h2, d1, d2
+    return {"h2d_gbs": nbytes / th / 1e9, "d2h_gbs": nbytes / td / 1e9, "both_gbs": 2 * nbytes / tb / 1e9}
+
+
 def e2e_leg(qlora, torch, dev, P, G, M, r, world, steps, flops):
     """Same step through the C ABI with pinned host buffers: per step the H2D
-    copy of every group's X and every projection's dY, and the D2H copy of
-    every Y, dA, dB and every group's dX, on two copy streams overlapping the
-    compute stream."""
+    copy of every group's X and every projection's dY (in the order the step
+    uses them), and the D2H copy of every Y, dA, dB and every group's dX, on
+    two copy streams overlapping the compute stream."""
     hY = [torch.empty(d["Y"].shape, dtype=torch.bfloat16, pin_memory=True) for d in P]
     hdA = [torch.empty(d["dA"].shape, dtype=torch.float32, pin_memory=True) for d in P]
     hdB = [torch.empty(d["dB"].shape, dtype=torch.float32, pin_memory=True) for d in P]
@@ -355,20 +392,23 @@ def e2e_leg(qlora, torch, dev, P, G, M, r, world, steps, flops):
         stream_to.wait_event(ev)
 
     def e2e_step():
-        ev_x, ev_dy = [], []
+        # inputs in the order the step consumes them: every X (forward, first
+        # group first), then every dY in backward order (last group first),
+        # so that each backward starts as soon as its own dY has arrived
+        ev_x, ev_dy = [], [None] * len(G)
         for g in G:
             with torch.cuda.stream(s_h2d):
                 g["X"].copy_(P[g["idx"][0]]["hX"], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(s_h2d)
                 ev_x.append(e)
-        for g in G:
+        for gi in reversed(range(len(G))):
             with torch.cuda.stream(s_h2d):
-                for i in g["idx"]:
+                for i in G[gi]["idx"]:
                     P[i]["dY"].copy_(P[i]["hdY"], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(s_h2d)
-                ev_dy.append(e)
+                ev_dy[gi] = e
         for gi, g in enumerate(G):
             comp.wait_event(ev_x[gi])
             qlora.qlora_group_fwd(g["X"], M, g["w"], g["A"], g["B"], r, g["s"], g["Y"], g["U"], g["ws"])
@@ -400,8 +440,13 @@ def e2e_leg(qlora, torch, dev, P, G, M, r, world, steps, flops):
     b.record(comp)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    pc = pcie_rates(torch, dev)
+    copy_ms = max(h2d / pc["h2d_gbs"], d2h / pc["d2h_gbs"], (h2d + d2h) / pc["both_gbs"]) / 1e6
     return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "pcie": {**pc, "copy_bound_ms_per_step": copy_ms, "frac": copy_ms / ms,
+                     "note": "pinned copies of 512 MiB measured on this box; the step's host traffic at these "
+                             "rates is its lower bound"},
             "note": "pinned host buffers; H2D of every group's X and every dY, D2H of every Y, dA, dB and every "
                     "group's dX, on two copy streams overlapping the compute stream; grouped calls"}
 
