@@ -354,9 +354,10 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
         for (int j = 0; j < NT; ++j) {
             const int tok = 8 * j + g;
             if (tok < p.M) {
+                // written by the preceding kernel: read through L2
                 const uint16_t *ur = p.sU + (int64_t)tok * p.ldu + 16 * kk + 2 * t;
-                bu[j][0] = *reinterpret_cast<const uint32_t *>(ur);
-                bu[j][1] = *reinterpret_cast<const uint32_t *>(ur + 8);
+                bu[j][0] = __ldcg(reinterpret_cast<const unsigned int *>(ur));
+                bu[j][1] = __ldcg(reinterpret_cast<const unsigned int *>(ur + 8));
             } else {
                 bu[j][0] = bu[j][1] = 0u;
             }
