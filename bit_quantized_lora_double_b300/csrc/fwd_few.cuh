@@ -6,9 +6,10 @@
 // Work: the weight is cut into tasks of 32 rows x 256 k (four blocks of 64;
 // the codes of a task are one TMA box of 32 rows x 128 bytes), numbered row
 // tile by row tile: tile t holds tasks [t P, (t + 1) P), P = K / 256. The
-// line of T tasks is split evenly over the W warps of the grid (warp
-// w = 16 * block + warp index takes [w T / W, (w + 1) T / W), at least one
-// task each), so the SMs stream the same number of bytes to within a task.
+// line of T tasks is split evenly over the W warps of the grid (16 warps a
+// CTA with one 8-token tile, 12 with two; warp w = warps a CTA * block +
+// warp index takes [w T / W, (w + 1) T / W), at least one task each), so the
+// SMs stream the same number of bytes to within a task.
 //
 // Every warp is its own pipeline: its lane 0 keeps two of its tasks in flight
 // (two 4 KB slots, one mbarrier each), the warp decodes a landed task while
@@ -47,7 +48,7 @@ namespace qlora {
 struct FewCfg {
     static constexpr int ROWS = 32;                     // weight rows per task (two m16 tiles)
     static constexpr int TK = 256;                      // k per task: four blocks
-    static constexpr int WARPS = 16;                    // warps per CTA, one pipeline each
+    static constexpr int WARPS = 16;                    // warps per CTA at most, one pipeline each
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int TASK_BYTES = ROWS * 128;       // a task's codes: one 32-row x 128-byte box
     static constexpr int SLOTS = 2;                     // tasks in flight per warp
@@ -69,6 +70,15 @@ static_assert(FewCfg::TABLE_ADDR + FewCfg::TABLE_BYTES + (FewCfg::NSLOT - 15) * 
                   0x400 + FewCfg::SMEM_BYTES,
               "layout when the allocation starts 1 KB into the window (15 slots below the table)");
 static_assert(FewCfg::SMEM_BYTES <= 232448, "shared memory per CTA");
+
+// Warps per CTA for NT 8-token tiles: sixteen with one tile; twelve with two
+// (their accumulators and the X fragments requested a block ahead need the
+// registers of a 384-thread CTA).
+template <int NT>
+__host__ __device__ constexpr int few_warps() {
+    return NT == 1 ? 16 : 12;
+}
+static_assert(few_warps<1>() <= FewCfg::WARPS && few_warps<2>() <= FewCfg::WARPS, "slots of the layout");
 
 // Diagnostic timeline (built only with -DQLORA_GEMM_STAMPS, into a separate
 // library): globaltimer stamps per warp of the last launch. Columns: 0 entry,
@@ -227,7 +237,7 @@ __global__ void __launch_bounds__(kFewDownThreads) k_few_down(const uint16_t *__
 // F32A: the block absmax is stored as fp32 (`absmax`, one per block) instead
 // of double-quantized; tab selects the level table (kTableNF4 / kTableINT4).
 template <int NT, bool F32A>
-__global__ void __launch_bounds__(FewCfg::THREADS, 1)
+__global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
     k_fwd_few(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ FewParams p,
               const float *__restrict__ absmax) {
     using C = FewCfg;
@@ -245,7 +255,8 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t T = (uint32_t)p.tasks, W = (uint32_t)p.warps, P = (uint32_t)p.tpr;
-    const uint32_t gw = blockIdx.x * C::WARPS + warp;
+    constexpr int WPC = few_warps<NT>();  // warps of this CTA
+    const uint32_t gw = blockIdx.x * WPC + warp;
     const bool active = gw < W;
     if (active) QLORA_FEW_STAMP(gw, 0);
     const uint32_t t0 = active ? few_begin(gw, W, T) : 0, t1 = active ? few_begin(gw + 1, W, T) : 0;
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     }
     // the byte table, while the first tasks stream in: word (e, lane) at
     // TABLE_ADDR + 256 e + 4 lane = bf16 pair (L[e >> 4] low, L[e & 15] high)
-    for (int i = threadIdx.x; i < 256 * 32; i += C::THREADS) {
+    for (int i = threadIdx.x; i < 256 * 32; i += 32 * WPC) {
         const int e = i >> 5, l = i & 31;
         *reinterpret_cast<uint32_t *>(sp(C::TABLE_ADDR + (uint32_t)(e * 256 + l * 4))) =
             pack_bf16x2(p.levels[e >> 4], p.levels[e & 15]);
@@ -490,9 +501,8 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
     uint32_t rt = t0 / P, kc = t0 - rt * P;
     Scales cur, nxt;
     load_scales(t0, cur);
-    // X^T fragments of one block (k-chunk kc2, block b2). With one 8-token
-    // tile they are requested one block ahead of their use, so that a read
-    // from L2 overlaps a block's decode (with two, the registers are short).
+    // X^T fragments of one block (k-chunk kc2, block b2), requested one block
+    // ahead of their use, so that a read from L2 overlaps a block's decode
     auto load_x = [&](uint32_t kc2, int b2, uint4 (&xv)[NT][2]) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
@@ -505,7 +515,7 @@ __global__ void __launch_bounds__(FewCfg::THREADS, 1)
             }
         }
     };
-    constexpr bool kXpf = NT == 1;
+    constexpr bool kXpf = true;
     uint4 xcur[NT][2];
     if (kXpf) load_x(kc, 0, xcur);
     for (int i = 0; i < n; ++i) {

@@ -290,18 +290,20 @@ inline bool few_path(int64_t M, int64_t N, int64_t K) {
     return M <= 8 * FewCfg::MAX_NT && K % FewCfg::TK == 0 && N * (K / kBlock) < (int64_t(1) << 31);
 }
 
-// Its split: tasks of 32 rows x 256 k over at most 16 warps on each of 148
-// CTAs, every warp at least one task.
+// Its split: tasks of 32 rows x 256 k over the warps of at most 148 CTAs
+// (16 warps a CTA for M <= 8, 12 for two 8-token tiles), every warp at least
+// one task.
 struct FewPlan {
-    int64_t grid, warps, tasks, tpr, tiles;
+    int64_t grid, warps, tasks, tpr, tiles, wpc;
 };
-FewPlan few_plan(int64_t N, int64_t K) {
+FewPlan few_plan(int64_t M, int64_t N, int64_t K) {
     FewPlan f;
+    f.wpc = M <= 8 ? few_warps<1>() : few_warps<2>();
     f.tiles = cdiv(N, FewCfg::ROWS);
     f.tpr = K / FewCfg::TK;
     f.tasks = f.tiles * f.tpr;
-    f.warps = std::min<int64_t>(f.tasks, (int64_t)FewCfg::WARPS * FewCfg::GRID);
-    f.grid = cdiv(f.warps, FewCfg::WARPS);
+    f.warps = std::min<int64_t>(f.tasks, f.wpc * FewCfg::GRID);
+    f.grid = cdiv(f.warps, f.wpc);
     return f;
 }
 // fp32 slot floats per warp: two row tiles x 32 lanes x 8 per 8-token tile
@@ -318,7 +320,7 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r, void *ws, FwdWs *out) {
     Carve c(ws);
     FwdWs f{};
     if (few_path(M, N, K)) {
-        const FewPlan fp = few_plan(N, K);
+        const FewPlan fp = few_plan(M, N, K);
         f.sU = c.take<uint16_t>((size_t)M * lora_pad(r));
         f.few_slots = c.take<float>((size_t)fp.warps * few_slot_floats(M));
         f.few_counters = c.take<uint32_t>((size_t)fp.tiles);
@@ -716,9 +718,11 @@ extern "C" {
 
 const char *qlora_version(void) { return "qlora-b300 0.1 (sm_103a)"; }
 
-int64_t qlora_debug_few_split(int64_t N, int64_t K, int64_t *out, int64_t cap) {
-    if (N < 1 || K < FewCfg::TK || K % FewCfg::TK || !out || N * (K / kBlock) >= (int64_t(1) << 31)) return -2;
-    const FewPlan f = few_plan(N, K);
+int64_t qlora_debug_few_split(int64_t M, int64_t N, int64_t K, int64_t *out, int64_t cap) {
+    if (M < 1 || M > 8 * FewCfg::MAX_NT || N < 1 || K < FewCfg::TK || K % FewCfg::TK || !out ||
+        N * (K / kBlock) >= (int64_t(1) << 31))
+        return -2;
+    const FewPlan f = few_plan(M, N, K);
     const int64_t need = 4 + 2 * f.warps + 2 * f.tiles;
     if (cap < need) return -1;
     const uint32_t T = (uint32_t)f.tasks, W = (uint32_t)f.warps, P = (uint32_t)f.tpr;
@@ -1106,7 +1110,7 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         const cudaError_t aerr = smem_attr(kern, FewCfg::SMEM_BYTES);
         if (aerr != cudaSuccess)
             return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
-        const FewPlan fp = few_plan(N, K);
+        const FewPlan fp = few_plan(M, N, K);
         {
             // a programmatic dependent of the preceding kernel (it waits for
             // that grid before touching memory): its launch overlaps the
@@ -1161,7 +1165,7 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)fp.grid);
-        cfg.blockDim = dim3(FewCfg::THREADS);
+        cfg.blockDim = dim3((unsigned)(32 * fp.wpc));
         cfg.dynamicSmemBytes = FewCfg::SMEM_BYTES;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];

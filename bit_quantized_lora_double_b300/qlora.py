@@ -141,7 +141,7 @@ def lib():
         L.qlora_debug_gemm_segments.restype = i64
         L.qlora_debug_gemm_segments.argtypes = [i64, i64, i64, i32, i32, vp, i64]
         L.qlora_debug_few_split.restype = i64
-        L.qlora_debug_few_split.argtypes = [i64, i64, vp, i64]
+        L.qlora_debug_few_split.argtypes = [i64, i64, i64, vp, i64]
         _lib = L
     return _lib
 
@@ -441,16 +441,16 @@ def qlora_debug_gemm_segments(M: int, Nd: int, nk_main: int, lora_steps: int, pa
         cap *= 4
 
 
-def qlora_debug_few_split(N: int, K: int):
-    """The few-token forward's split of an N x K weight (host computation, no
-    GPU): returns (tasks, warps, P, tiles, ranges, tile_warps), ranges an
+def qlora_debug_few_split(M: int, N: int, K: int):
+    """The few-token forward's split of an N x K weight for M tokens (host
+    computation, no GPU): returns (tasks, warps, P, tiles, ranges, tile_warps), ranges an
     int64 array [warps, 2] of each warp's task range [first, end) and
     tile_warps [tiles, 2] each row tile's first and last contributing warp.
     Raises QloraError(QLORA_ERR_SHAPE) on bad input."""
     import numpy as np
     cap = 4 + 2 * 16 * 148 + 2 * ((int(N) + 31) // 32)
     out = np.zeros(cap, np.int64)
-    n = lib().qlora_debug_few_split(int(N), int(K), out.ctypes.data, cap)
+    n = lib().qlora_debug_few_split(int(M), int(N), int(K), out.ctypes.data, cap)
     if n < 0:
         raise QloraError(2, "qlora_debug_few_split: invalid arguments")
     T, W, P, tiles = (int(v) for v in out[:4])

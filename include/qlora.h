@@ -414,15 +414,16 @@ int64_t qlora_debug_gemm_segments(int64_t M, int64_t Nd, int64_t nk_main, int lo
                                   int64_t *out, int64_t cap);
 
 /* Diagnostic, host only (no device access): the split the few-token forward
- * (M <= 16, K a multiple of 256) uses for an N x K weight. Tasks of 32 rows x
- * 256 k are numbered row tile by row tile (tile t holds tasks t P .. t P + P -
- * 1, P = K / 256) and split evenly over W warps. Writes out[0..3] = T tasks,
+ * (M <= 16, K a multiple of 256) uses for M tokens and an N x K weight. Tasks
+ * of 32 rows x 256 k are numbered row tile by row tile (tile t holds tasks t P
+ * .. t P + P - 1, P = K / 256) and split evenly over W warps (16 per CTA for
+ * M <= 8, 12 for M > 8, at most 148 CTAs). Writes out[0..3] = T tasks,
  * W warps, P, row tiles; then each warp's first task and one past its last
  * (2 W values); then each row tile's first and last contributing warp (2 x
  * tiles values). A tile whose two warps are equal is finished by that warp;
  * otherwise the last of its warps to arrive finishes it. Returns the number of
  * values written, -1 when `cap` is too small, -2 for invalid arguments. */
-int64_t qlora_debug_few_split(int64_t N, int64_t K, int64_t *out, int64_t cap);
+int64_t qlora_debug_few_split(int64_t M, int64_t N, int64_t K, int64_t *out, int64_t cap);
 
 #ifdef __cplusplus
 }

@@ -25,11 +25,12 @@ _rng = np.random.default_rng(11)
 SHAPES += [(int(_rng.integers(1, 40000)), 256 * int(_rng.integers(1, 120))) for _ in range(40)]
 
 
+@pytest.mark.parametrize("M", [1, 16])
 @pytest.mark.parametrize("N,K", SHAPES)
-def test_few_split(N, K):
-    T, W, P, tiles, rng, tw = qlora.qlora_debug_few_split(N, K)
+def test_few_split(M, N, K):
+    T, W, P, tiles, rng, tw = qlora.qlora_debug_few_split(M, N, K)
     assert P == K // 256 and tiles == (N + 31) // 32 and T == tiles * P
-    assert W == min(T, 16 * 148)
+    assert W == min(T, (16 if M <= 8 else 12) * 148)
     # even split: warp w starts at floor(w T / W); ranges tile [0, T), none empty
     w = np.arange(W, dtype=np.int64)
     assert np.array_equal(rng[:, 0], w * T // W)
@@ -62,6 +63,6 @@ def test_few_split(N, K):
 
 
 def test_few_split_rejects():
-    for N, K in [(0, 256), (10, 100), (10, 0), (1 << 20, 1 << 20)]:
+    for M, N, K in [(1, 0, 256), (1, 10, 100), (1, 10, 0), (1, 1 << 20, 1 << 20), (0, 10, 256), (17, 10, 256)]:
         with pytest.raises(qlora.QloraError):
-            qlora.qlora_debug_few_split(N, K)
+            qlora.qlora_debug_few_split(M, N, K)
