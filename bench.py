@@ -611,6 +611,66 @@ def bench_sweep(qlora, torch, dev, pk):
     return {"workload": wl["name"] + ": gate 4096->14336 NF4+DQ, LoRA r=16 alpha=32", "rows": rows}
 
 
+def bench_decode(qlora, torch, dev, pk, Ms=(1, 16)):
+    """The 8B-shaped layer's forward at decode sizes (M = 1 and 16): the seven
+    projections as grouped calls (q/k/v, o, gate/up, down) and as single
+    calls, two copies of the layer's weights alternating (224 MB > L2),
+    graph-replayed; GB/s counts the packed weights read (codes, absmax codes,
+    scales) against the HBM roofline."""
+    wl = synth.WORKLOADS[LAYER8B]
+    r, scale = wl["r"], wl["scale"]
+    projs = wl["projections"]
+    groups = groups_of([{"name": nm} for nm, _, _ in projs])
+    dv = lambda h: torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
+    layers = []
+    for copy in range(2):
+        P = []
+        for p, (nm, n, k) in enumerate(projs):
+            _, W, A, B, _, _ = synth.layer_inputs(LAYER8B, p, M=1)
+            w = qlora.alloc_nf4_weight(n, k, dev)
+            qlora.qlora_nf4_quantize(dv(W), w, qlora.workspace(qlora.qlora_nf4_quantize_workspace(n, k), dev))
+            P.append(dict(n=n, k=k, w=w, A=dv(A), B=dv(B)))
+        layers.append(P)
+    wbytes = sum(n * k // 2 + n * k // 64 + 4 * ((n * k // 64 + 255) // 256) + 4 for _, n, k in projs)
+    rows = []
+    for M in Ms:
+        Xs = {k: torch.randn(M, k, device=dev).to(torch.bfloat16) for _, _, k in projs}
+        for P in layers:
+            for d in P:
+                d["Y"] = torch.empty((M, d["n"]), dtype=torch.bfloat16, device=dev)
+        U = torch.empty((M, 3 * r), dtype=torch.bfloat16, device=dev)
+        U1 = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+        size = 0
+        for P in layers:
+            for d in P:
+                size = max(size, qlora.qlora_linear_fwd_workspace(M, d["w"], r))
+            for idx in groups:
+                size = max(size, qlora.qlora_group_fwd_workspace(M, [P[i]["w"] for i in idx],
+                                                                 [P[i]["A"] for i in idx], [P[i]["B"] for i in idx], r))
+        ws = qlora.workspace(size, dev)
+
+        def grouped():
+            for P in layers:
+                for idx in groups:
+                    qlora.qlora_group_fwd(Xs[P[idx[0]]["k"]], M, [P[i]["w"] for i in idx], [P[i]["A"] for i in idx],
+                                          [P[i]["B"] for i in idx], r, scale, [P[i]["Y"] for i in idx], U, ws)
+
+        def single():
+            for P in layers:
+                for d in P:
+                    qlora.qlora_linear_fwd(Xs[d["k"]], M, d["w"], d["A"], d["B"], r, scale, d["Y"], U1, ws)
+        tg = graph_time(torch, grouped, 50, 3) / 2
+        ts = graph_time(torch, single, 50, 3) / 2
+        rows.append({"M": M, "layer_fwd_us_grouped": tg * 1e3, "layer_fwd_us_single": ts * 1e3,
+                     "grouped_gbs": wbytes / (tg * 1e-3) / 1e9, "grouped_pct_hbm": wbytes / (tg * 1e-3) / 1e9 / pk["hbm"],
+                     "single_gbs": wbytes / (ts * 1e-3) / 1e9})
+        del ws, Xs
+    del layers
+    torch.cuda.empty_cache()
+    return {"workload": wl["name"] + ": the seven projections' forward at decode sizes", "weight_bytes": wbytes,
+            "rows": rows}
+
+
 def host_cores():
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
@@ -842,6 +902,7 @@ def main():
         extra["single_layer"] = bench_layer(qlora, torch, dev, pk, SINGLE, 200)
         extra["codec"] = bench_codec(qlora, torch, dev, pk)
         extra["gate_sweep"] = bench_sweep(qlora, torch, dev, pk)
+        extra["decode_layer"] = bench_decode(qlora, torch, dev, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

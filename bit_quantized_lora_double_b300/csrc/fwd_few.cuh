@@ -98,22 +98,40 @@ __device__ unsigned long long d_few_stamps[kFewStampWarps][16];
     } while (0)
 #endif
 
-struct FewParams {
-    const uint16_t *X;
-    int64_t M, N, K;
+// One projection of a launch (up to kMaxGroup projections that share X and
+// K): its weight's constants, its adapter's B and its output, and where its
+// row tiles start in the launch's line of tiles.
+struct FewProj {
     const int8_t *q;       // int8 absmax codes [N, K / 64] (null with fp32 absmax)
     const float *s2;       // second-level scales, one per 256 blocks
     const float *mean;
-    const uint16_t *sU;    // bf16(s * U) [M, ldu], zero beyond r
-    int ldu;
+    const float *absmax;   // fp32 block absmax (variant without double quantization)
     const uint16_t *B;     // [N, r]
+    uint16_t *Y;           // [M, N]
+    int64_t N;
+    uint32_t tile0;        // first row tile of this projection in the launch
+    int sucol;             // first column of its bf16(s * U) slice in sU
+};
+// NP: projections a launch carries room for (1, or kMaxGroup for groups), so
+// that a single projection's kernel parameters stay small.
+template <int NP>
+struct FewMaps {
+    CUtensorMap codes[NP];  // the packed codes of each projection
+};
+template <int NP>
+struct FewParams {
+    const uint16_t *X;
+    int64_t M, K;
+    const uint16_t *sU;    // bf16(s * U) [M, ldu]: one slice of 64-column multiples per projection, zero beyond r
+    int ldu;
     int r;
-    uint16_t *Y;
+    int nproj;
+    FewProj proj[NP];
     float *slots;          // [warps][2][32 lanes][8 NT]: fragments of shared row tiles
-    uint32_t *counters;    // [ceil(N / 32)], zeroed by the preceding kernel
+    uint32_t *counters;    // [row tiles of all projections], zeroed by the preceding kernel
     int64_t tasks;         // T = row tiles x P
     int64_t tpr;           // P = K / 256 tasks per row tile
-    int64_t warps;         // W = min(T, 16 x grid)
+    int64_t warps;         // W = min(T, warps a CTA x grid)
     uint64_t wait_ns;
     float levels[16];      // the 4-bit level table (a kernel parameter: no cold constant-cache read)
 };
@@ -183,17 +201,23 @@ __device__ __forceinline__ void few_mma(float (&d)[4], const uint32_t (&a)[4], u
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// sU for the few-token forward: CTA (m, j) computes U[m, j] = sum_k
-// X[m, k] A[j, k] (threads striding over K in 8-element chunks, eight loads
-// of each operand in flight, then a warp and a block reduction in fixed
-// order), writes U (bf16, stride ldu, may be null) and sU = bf16(s * U)
-// (stride lds); CTA (m, 0) also writes the zeros of sU for r <= j < lds, and
-// CTA (0, 0) zeroes the forward's arrival counters. K % 8 == 0.
+// sU for the few-token forward over n projections (A_g [r, K] each): CTA
+// (m, jj, g) computes U[m, j] = sum_k X[m, k] A_g[jj, k], j = g r + jj (threads
+// striding over K in 8-element chunks, eight loads of each operand in
+// flight, then a warp and a block reduction in fixed order) and writes U
+// (bf16, stride ldu, may be null) and sU = bf16(s * U) at column g rp + jj
+// (stride lds: one slice of rp columns per projection); CTA (m, 0, g) also
+// writes the zeros of slice g beyond r, and CTA (0, 0) zeroes the forward's
+// arrival counters. A0..A3: A_g (unused ones may be null). K % 8 == 0.
+// Grid: (M, r, n).
 constexpr int kFewDownThreads = 256;
 __global__ void __launch_bounds__(kFewDownThreads) k_few_down(const uint16_t *__restrict__ X, int64_t K,
-                                                              const uint16_t *__restrict__ A, int r, float s,
+                                                              const uint16_t *__restrict__ A0,
+                                                              const uint16_t *__restrict__ A1,
+                                                              const uint16_t *__restrict__ A2,
+                                                              const uint16_t *__restrict__ A3, int r, float s,
                                                               uint16_t *__restrict__ U, int ldu,
-                                                              uint16_t *__restrict__ sU, int lds,
+                                                              uint16_t *__restrict__ sU, int lds, int rp,
                                                               uint32_t *__restrict__ zero, int nzero) {
     // launched as a programmatic dependent of whatever precedes it: wait for
     // that grid before touching memory (X or the workspace may be its output)
@@ -202,13 +226,15 @@ __global__ void __launch_bounds__(kFewDownThreads) k_few_down(const uint16_t *__
     // its weights now; it waits for this grid before it reads sU or counts
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float wsum[kFewDownThreads / 32];
-    const int m = blockIdx.x, j = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m = blockIdx.x, jj = blockIdx.y, pj = blockIdx.z, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = pj * r + jj;
     if (m == 0 && j == 0)
         for (int i = threadIdx.x; i < nzero; i += kFewDownThreads) zero[i] = 0u;
-    if (j == 0)
-        for (int i = r + threadIdx.x; i < lds; i += kFewDownThreads) sU[(int64_t)m * lds + i] = 0;
+    if (jj == 0)  // the zero columns of this projection's slice
+        for (int i = r + threadIdx.x; i < rp; i += kFewDownThreads) sU[(int64_t)m * lds + pj * rp + i] = 0;
+    const uint16_t *Ap = pj == 0 ? A0 : (pj == 1 ? A1 : (pj == 2 ? A2 : A3));
     const uint4 *xr = reinterpret_cast<const uint4 *>(X + (int64_t)m * K);
-    const uint4 *ar = reinterpret_cast<const uint4 *>(A + (int64_t)j * K);
+    const uint4 *ar = reinterpret_cast<const uint4 *>(Ap + (int64_t)jj * K);
     float acc = 0.0f;
 #pragma unroll 8
     for (int64_t c = threadIdx.x; c < K / 8; c += kFewDownThreads) {
@@ -229,17 +255,19 @@ __global__ void __launch_bounds__(kFewDownThreads) k_few_down(const uint16_t *__
 #pragma unroll
         for (int w = 1; w < kFewDownThreads / 32; ++w) t += wsum[w];
         if (U) U[(int64_t)m * ldu + j] = __bfloat16_as_ushort(__float2bfloat16_rn(t));
-        sU[(int64_t)m * lds + j] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, t)));
+        sU[(int64_t)m * lds + pj * rp + jj] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(s, t)));
     }
 }
 
 // NT = number of 8-token tiles (M <= 8 * NT <= 16).
 // F32A: the block absmax is stored as fp32 (`absmax`, one per block) instead
-// of double-quantized; tab selects the level table (kTableNF4 / kTableINT4).
-template <int NT, bool F32A>
+// of double-quantized; the level table comes in p.levels.
+// MULTI: more than one projection (p.nproj > 1); with one, every projection
+// lookup folds to projection 0.
+template <int NT, bool F32A, bool MULTI>
 __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
-    k_fwd_few(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ FewParams p,
-              const float *__restrict__ absmax) {
+    k_fwd_few(const __grid_constant__ FewMaps<MULTI ? kMaxGroup : 1> tm,
+              const __grid_constant__ FewParams<MULTI ? kMaxGroup : 1> p) {
     using C = FewCfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
@@ -267,15 +295,25 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
     // this warp's slot s (1024-byte aligned; the table may sit between two)
     auto slot_of = [&](int s) { return few_slot(L, C::SLOTS * warp + s); };
 
-    // lane 0: task x into slot s (rows 32 (x / P) .., bytes 128 (x % P) ..)
+    // the projection whose row tiles hold the launch's tile gt
+    auto proj_of = [&](uint32_t gt) {
+        int pj = 0;
+#pragma unroll
+        for (int k = 1; k < (MULTI ? kMaxGroup : 1); ++k) pj += (k < p.nproj && gt >= p.proj[k].tile0) ? 1 : 0;
+        return pj;
+    };
+    // lane 0: task x into slot s (tile x / P: rows 32 (tile - its
+    // projection's first) .., bytes 128 (x % P) .. of that projection's codes)
     auto issue = [&](int s, uint32_t x) {
-        const uint32_t rt = x / P, kc = x - rt * P;
+        const uint32_t gt = x / P, kc = x - gt * P;
+        const int pj = proj_of(gt);
         mbar_arrive_expect_tx(&full[s], (uint32_t)C::TASK_BYTES);
-        tma_load_2d(sp(slot_of(s)), &tm_codes, &full[s], (int32_t)(kc * 128u), (int32_t)(rt * C::ROWS));
+        tma_load_2d(sp(slot_of(s)), &tm.codes[pj], &full[s], (int32_t)(kc * 128u),
+                    (int32_t)((gt - p.proj[pj].tile0) * C::ROWS));
     };
     if (threadIdx.x == 0) *abort_flag = 0;
     if (lane == 0 && active) {
-        prefetch_tmap(&tm_codes);
+        for (int k = 0; k < p.nproj; ++k) prefetch_tmap(&tm.codes[k]);
         for (int q = 0; q < S; ++q) mbar_init(&full[q], 1);
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -295,8 +333,8 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
 
     const int g = lane >> 2, t = lane & 3;
     const uint32_t lanebase = C::TABLE_ADDR | (uint32_t)(lane << 2);
-    const float mean = F32A ? 0.0f : *p.mean;
     const uint32_t KB = (uint32_t)(p.K / kBlock);
+    const float mean0 = F32A ? 0.0f : __ldg(p.proj[0].mean);  // (one projection)
     // X^T fragments: token 8 j + g, k = 64 kb + 16 t .. + 15
     const uint16_t *xb[NT];
 #pragma unroll
@@ -315,18 +353,24 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
         uint32_t q[4];
         float s2[4];
         float4 a[4];
+        float mean;
     };
     auto load_scales = [&](uint32_t x, Scales &sc) {
-        const uint32_t rt = x / P, kc = x - rt * P;
+        const uint32_t gt = x / P, kc = x - gt * P;
+        // (the parameters are read by index, never through a reference: a
+        // constant-bank load, folded to an immediate with one projection)
+        const int pj = proj_of(gt);
+        const uint32_t row0 = (gt - p.proj[pj].tile0) * C::ROWS;
+        if (MULTI && !F32A) sc.mean = __ldg(p.proj[pj].mean);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t nrow = rt * C::ROWS + g + 8 * i;
-            const uint32_t idx = (nrow < (uint32_t)p.N ? nrow : 0u) * KB + 4u * kc;
+            const uint32_t nrow = row0 + g + 8 * i;
+            const uint32_t idx = (nrow < (uint32_t)p.proj[pj].N ? nrow : 0u) * KB + 4u * kc;
             if (F32A) {
-                sc.a[i] = __ldg(reinterpret_cast<const float4 *>(absmax + idx));
+                sc.a[i] = __ldg(reinterpret_cast<const float4 *>(p.proj[pj].absmax + idx));
             } else {
-                sc.q[i] = __ldg(reinterpret_cast<const uint32_t *>(p.q + idx));
-                sc.s2[i] = __ldg(p.s2 + (idx >> 8));
+                sc.q[i] = __ldg(reinterpret_cast<const uint32_t *>(p.proj[pj].q + idx));
+                sc.s2[i] = __ldg(p.proj[pj].s2 + (idx >> 8));
             }
         }
     };
@@ -340,33 +384,35 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
             pdl_done = true;
         }
     };
-    // B pair (B[n, jj], B[n, jj + 1]) as bf16x2, zero beyond N rows or r ranks
-    auto b_pair = [&](int64_t nrow, int jj) -> uint32_t {
-        if (nrow >= p.N || jj >= p.r) return 0u;
-        const uint16_t *br = p.B + nrow * p.r + jj;
+    // B pair (B[n, jj], B[n, jj + 1]) of projection pr as bf16x2, zero
+    // beyond its N rows or r ranks
+    auto b_pair = [&](int pj, int64_t nrow, int jj) -> uint32_t {
+        if (nrow >= p.proj[pj].N || jj >= p.r) return 0u;
+        const uint16_t *br = p.proj[pj].B + nrow * p.r + jj;
         if ((p.r & 1) == 0) return __ldg(reinterpret_cast<const uint32_t *>(br));  // 4-byte aligned
         const uint32_t hi = jj + 1 < p.r ? (uint32_t)__ldg(br + 1) : 0u;
         return (uint32_t)__ldg(br) | (hi << 16);
     };
-    // LoRA operands of ranks [16 kk, 16 kk + 16): rows of B as A fragments,
-    // sU^T as B fragments (sU is zero beyond r)
-    auto lora_a = [&](uint32_t rtile, int kk, uint32_t (&ba)[2][4]) {
+    // LoRA operands of ranks [16 kk, 16 kk + 16) for the projection's row
+    // tile lt: rows of B as A fragments, sU^T as B fragments (its slice of sU
+    // is zero beyond r)
+    auto lora_a = [&](int pj, uint32_t lt, int kk, uint32_t (&ba)[2][4]) {
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt) {
-            const int64_t ra = (int64_t)rtile * C::ROWS + 16 * rt + g;
-            ba[rt][0] = b_pair(ra, 16 * kk + 2 * t);
-            ba[rt][1] = b_pair(ra + 8, 16 * kk + 2 * t);
-            ba[rt][2] = b_pair(ra, 16 * kk + 2 * t + 8);
-            ba[rt][3] = b_pair(ra + 8, 16 * kk + 2 * t + 8);
+            const int64_t ra = (int64_t)lt * C::ROWS + 16 * rt + g;
+            ba[rt][0] = b_pair(pj, ra, 16 * kk + 2 * t);
+            ba[rt][1] = b_pair(pj, ra + 8, 16 * kk + 2 * t);
+            ba[rt][2] = b_pair(pj, ra, 16 * kk + 2 * t + 8);
+            ba[rt][3] = b_pair(pj, ra + 8, 16 * kk + 2 * t + 8);
         }
     };
-    auto lora_b = [&](int kk, uint32_t (&bu)[NT][2]) {
+    auto lora_b = [&](int pj, int kk, uint32_t (&bu)[NT][2]) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int tok = 8 * j + g;
             if (tok < p.M) {
                 // written by the preceding kernel: read through L2
-                const uint16_t *ur = p.sU + (int64_t)tok * p.ldu + 16 * kk + 2 * t;
+                const uint16_t *ur = p.sU + (int64_t)tok * p.ldu + p.proj[pj].sucol + 16 * kk + 2 * t;
                 bu[j][0] = __ldcg(reinterpret_cast<const unsigned int *>(ur));
                 bu[j][1] = __ldcg(reinterpret_cast<const unsigned int *>(ur + 8));
             } else {
@@ -377,7 +423,7 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
     // Finishes row tile rtile from its full fp32 sums v (fragment layout):
     // adds the LoRA term with mma.sync (ranks 0..15 from ba0 / bu0, loaded
     // by the caller) and writes the valid outputs as bf16.
-    auto finish = [&](float (&v)[2][NT][4], uint32_t rtile, const uint32_t (&ba0)[2][4],
+    auto finish = [&](float (&v)[2][NT][4], int pj, uint32_t lt, const uint32_t (&ba0)[2][4],
                       const uint32_t (&bu0)[NT][2]) {
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt)
@@ -385,27 +431,27 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
             for (int j = 0; j < NT; ++j) few_mma(v[rt][j], ba0[rt], bu0[j][0], bu0[j][1]);
         for (int kk = 1; kk * 16 < p.r; ++kk) {
             uint32_t ba[2][4], bu[NT][2];
-            lora_a(rtile, kk, ba);
-            lora_b(kk, bu);
+            lora_a(pj, lt, kk, ba);
+            lora_b(pj, kk, bu);
 #pragma unroll
             for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
                 for (int j = 0; j < NT; ++j) few_mma(v[rt][j], ba[rt], bu[j][0], bu[j][1]);
         }
-        const int64_t row0 = (int64_t)rtile * C::ROWS;
+        const int64_t row0 = (int64_t)lt * C::ROWS;
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int64_t nrow = row0 + 16 * rt + 8 * h + g;
-                if (nrow >= p.N) continue;
+                if (nrow >= p.proj[pj].N) continue;
 #pragma unroll
                 for (int j = 0; j < NT; ++j)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int tok = 8 * j + 2 * t + e;
                         if (tok < p.M)
-                            p.Y[(int64_t)tok * p.N + nrow] =
+                            p.proj[pj].Y[(int64_t)tok * p.proj[pj].N + nrow] =
                                 __bfloat16_as_ushort(__float2bfloat16_rn(v[rt][j][2 * h + e]));
                     }
             }
@@ -425,13 +471,15 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
         // the first 16 ranks of the LoRA term come in while the tile is
         // handed over (B is an input; sU and the zeroed counters come from
         // the preceding kernel)
+        const int pj = proj_of(rtile);
+        const uint32_t lt = rtile - p.proj[pj].tile0;
         uint32_t ba0[2][4], bu0[NT][2];
-        lora_a(rtile, 0, ba0);
+        lora_a(pj, lt, 0, ba0);
         pdl_wait_once();
-        lora_b(0, bu0);
+        lora_b(pj, 0, bu0);
         const uint32_t a = rtile * P, b = a + P;
         if (a >= t0 && b <= t1) {
-            finish(acc, rtile, ba0, bu0);
+            finish(acc, pj, lt, ba0, bu0);
             ++n_fin;
             return;
         }
@@ -493,7 +541,7 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
                 }
             }
         }
-        finish(v, rtile, ba0, bu0);
+        finish(v, pj, lt, ba0, bu0);
     };
 
     // ------------------------------------------------ the stream ----------
@@ -597,7 +645,7 @@ __global__ void __launch_bounds__(32 * few_warps<NT>(), 1)
                 if (F32A) {
                     ap[q] = b == 0 ? cur.a[q].x : (b == 1 ? cur.a[q].y : (b == 2 ? cur.a[q].z : cur.a[q].w));
                 } else {
-                    ap[q] = dq_absmax((int8_t)((cur.q[q] >> (8 * b)) & 0xFFu), cur.s2[q], mean);
+                    ap[q] = dq_absmax((int8_t)((cur.q[q] >> (8 * b)) & 0xFFu), cur.s2[q], MULTI ? cur.mean : mean0);
                 }
             }
 #pragma unroll

@@ -296,16 +296,18 @@ inline bool few_path(int64_t M, int64_t N, int64_t K) {
 struct FewPlan {
     int64_t grid, warps, tasks, tpr, tiles, wpc;
 };
-FewPlan few_plan(int64_t M, int64_t N, int64_t K) {
+// tiles: the 32-row tiles of all the launch's projections
+FewPlan few_plan_tiles(int64_t M, int64_t tiles, int64_t K) {
     FewPlan f;
     f.wpc = M <= 8 ? few_warps<1>() : few_warps<2>();
-    f.tiles = cdiv(N, FewCfg::ROWS);
+    f.tiles = tiles;
     f.tpr = K / FewCfg::TK;
     f.tasks = f.tiles * f.tpr;
     f.warps = std::min<int64_t>(f.tasks, f.wpc * FewCfg::GRID);
     f.grid = cdiv(f.warps, f.wpc);
     return f;
 }
+FewPlan few_plan(int64_t M, int64_t N, int64_t K) { return few_plan_tiles(M, cdiv(N, FewCfg::ROWS), K); }
 // fp32 slot floats per warp: two row tiles x 32 lanes x 8 per 8-token tile
 inline size_t few_slot_floats(int64_t M) { return (size_t)2 * 32 * 8 * (M <= 8 ? 1 : 2); }
 
@@ -714,6 +716,104 @@ qlora_status run_skinny(SkJob j0, const SkJob *j1p, int r, cudaStream_t s, unsig
 
 }  // namespace
 
+// One few-token forward launch pair with parameters for NP projections.
+template <int NP, class Kern>
+static qlora_status few_fwd_launch_np(Kern kern, const uint16_t *X16, int64_t M, const Wt *const *w,
+                                      const void *const *A, const void *const *B, void *const *Y, int n, int r,
+                                      float scale, uint16_t *U16, int ldu, uint16_t *sU, int rp, float *slots,
+                                      uint32_t *counters, cudaStream_t s) {
+    qlora_status st;
+    const int64_t K = w[0]->cols;
+    const cudaError_t aerr = smem_attr(kern, FewCfg::SMEM_BYTES);
+    if (aerr != cudaSuccess) return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
+    FewParams<NP> prm{};
+    FewMaps<NP> maps;
+    memset(&maps, 0, sizeof maps);
+    const uint16_t *da[kMaxGroup] = {nullptr, nullptr, nullptr, nullptr};
+    int64_t tiles = 0;
+    // code boxes of 128 bytes x 32 rows (FewCfg::TASK_BYTES, one task),
+    // 128-byte swizzle
+    static_assert(FewCfg::TASK_BYTES == 128 * FewCfg::ROWS, "code box");
+    for (int g = 0; g < n; ++g) {
+        const Wt &wg = *w[g];
+        if ((st = make_map(&maps.codes[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, wg.codes, K / 2, wg.rows, K / 2, 128,
+                           FewCfg::ROWS, CU_TENSOR_MAP_SWIZZLE_128B, "codes")))
+            return st;
+        FewProj &pr = prm.proj[g];
+        pr.q = wg.q;
+        pr.s2 = wg.s2;
+        pr.mean = wg.mean;
+        pr.absmax = wg.absmax;
+        pr.B = static_cast<const uint16_t *>(B[g]);
+        pr.Y = static_cast<uint16_t *>(Y[g]);
+        pr.N = wg.rows;
+        pr.tile0 = (uint32_t)tiles;
+        pr.sucol = g * rp;
+        tiles += cdiv(wg.rows, FewCfg::ROWS);
+        da[g] = static_cast<const uint16_t *>(A[g]);
+    }
+    const FewPlan fp = few_plan_tiles(M, tiles, K);
+    {
+        // a programmatic dependent of the preceding kernel (it waits for
+        // that grid before touching memory): its launch overlaps the
+        // preceding kernel's end
+        cudaLaunchConfig_t dc = {};
+        dc.gridDim = dim3((unsigned)M, (unsigned)r, (unsigned)n);
+        dc.blockDim = dim3(kFewDownThreads);
+        dc.stream = s;
+        cudaLaunchAttribute dattr[1];
+        dattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        dattr[0].val.programmaticStreamSerializationAllowed = 1;
+        dc.attrs = dattr;
+        dc.numAttrs = 1;
+        ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
+        const cudaError_t de = cudaLaunchKernelEx(&dc, k_few_down, X16, (int64_t)K, da[0], da[1], da[2], da[3], r,
+                                                  scale, U16, ldu, sU, n * rp, rp, counters, (int)tiles);
+        if (de != cudaSuccess) {
+            cudaGetLastError();
+            return fail(QLORA_ERR_CUDA, "k_few_down: launch failed: %s", cudaGetErrorString(de));
+        }
+    }
+    if ((st = launch_check("k_few_down"))) return st;
+    prm.X = X16;
+    prm.M = M;
+    prm.K = K;
+    prm.sU = sU;
+    prm.ldu = n * rp;
+    prm.r = r;
+    prm.nproj = n;
+    prm.slots = slots;
+    prm.counters = counters;
+    prm.tasks = fp.tasks;
+    prm.tpr = fp.tpr;
+    prm.warps = fp.warps;
+    prm.wait_ns = wait_ns();
+    {
+        static const float kLevels[2][16] = {QLORA_NF4_LEVELS, QLORA_INT4_LEVELS};
+        memcpy(prm.levels, kLevels[w[0]->tab], sizeof prm.levels);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)fp.grid);
+    cfg.blockDim = dim3((unsigned)(32 * fp.wpc));
+    cfg.dynamicSmemBytes = FewCfg::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    {
+        ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
+        e = cudaLaunchKernelEx(&cfg, kern, maps, prm);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(QLORA_ERR_CUDA, "k_fwd_few: launch failed: %s", cudaGetErrorString(e));
+    }
+    return launch_check("k_fwd_few");
+}
+
 extern "C" {
 
 const char *qlora_version(void) { return "qlora-b300 0.1 (sm_103a)"; }
@@ -1082,6 +1182,24 @@ static qlora_status check_linear_common(int64_t M, const Wt &w, const void *A, c
     return QLORA_OK;
 }
 
+// The few-token forward of n projections (1..kMaxGroup) sharing X and K:
+// k_few_down (sU of all of them, slices of rp columns, lds = n rp) then one
+// k_fwd_few over the row tiles of all of them. Workspace: sU [M, n rp],
+// slots (few_slot_floats(M) per warp of the plan), one counter per row tile.
+static qlora_status few_fwd_launch(const uint16_t *X16, int64_t M, const Wt *const *w, const void *const *A,
+                                   const void *const *B, void *const *Y, int n, int r, float scale, uint16_t *U16,
+                                   int ldu, uint16_t *sU, int rp, float *slots, uint32_t *counters, cudaStream_t s) {
+    qlora_status st;
+    if ((st = tc_device_ok())) return st;
+    if (n > 1)  // several projections: NF4 with double quantization only (the group calls)
+        return few_fwd_launch_np<kMaxGroup>(M <= 8 ? k_fwd_few<1, false, true> : k_fwd_few<2, false, true>, X16, M,
+                                            w, A, B, Y, n, r, scale, U16, ldu, sU, rp, slots, counters, s);
+    const bool f32a = w[0]->absmax != nullptr;
+    auto kern = M <= 8 ? (f32a ? k_fwd_few<1, true, false> : k_fwd_few<1, false, false>)
+                       : (f32a ? k_fwd_few<2, true, false> : k_fwd_few<2, false, false>);
+    return few_fwd_launch_np<1>(kern, X16, M, w, A, B, Y, n, r, scale, U16, ldu, sU, rp, slots, counters, s);
+}
+
 // ldu: row pitch (elements) of U_save; r for the single-layer entry points.
 static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const void *A, const void *B, int r,
                                     float scale, void *Y, void *U_save, void *ws, size_t ws_bytes,
@@ -1103,87 +1221,10 @@ static qlora_status linear_fwd_impl(const void *X, int64_t M, const Wt &w, const
     uint16_t *U16 = static_cast<uint16_t *>(U_save);
 
     if (few_path(M, N, K)) {
-        // few tokens, K a multiple of 1024: persistent HBM-bound kernel
-        if ((st = tc_device_ok())) return st;
-        auto kern = M <= 8 ? (w.absmax ? k_fwd_few<1, true> : k_fwd_few<1, false>)
-                           : (w.absmax ? k_fwd_few<2, true> : k_fwd_few<2, false>);
-        const cudaError_t aerr = smem_attr(kern, FewCfg::SMEM_BYTES);
-        if (aerr != cudaSuccess)
-            return fail(QLORA_ERR_CUDA, "setting shared memory size: %s", cudaGetErrorString(aerr));
-        const FewPlan fp = few_plan(M, N, K);
-        {
-            // a programmatic dependent of the preceding kernel (it waits for
-            // that grid before touching memory): its launch overlaps the
-            // preceding kernel's end
-            cudaLaunchConfig_t dc = {};
-            dc.gridDim = dim3((unsigned)M, (unsigned)r);
-            dc.blockDim = dim3(kFewDownThreads);
-            dc.stream = s;
-            cudaLaunchAttribute da[1];
-            da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            da[0].val.programmaticStreamSerializationAllowed = 1;
-            dc.attrs = da;
-            dc.numAttrs = 1;
-            ProfScope ps(QLORA_KERNEL_LORA_PRE, s);
-            const cudaError_t de = cudaLaunchKernelEx(&dc, k_few_down, X16, (int64_t)K, static_cast<const uint16_t *>(A),
-                                                      r, scale, U16, ldu, f.sU, rp, f.few_counters, (int)fp.tiles);
-            if (de != cudaSuccess) {
-                cudaGetLastError();
-                return fail(QLORA_ERR_CUDA, "k_few_down: launch failed: %s", cudaGetErrorString(de));
-            }
-        }
-        if ((st = launch_check("k_few_down"))) return st;
-        CUtensorMap tmC;
-        // code boxes of 128 bytes x 32 rows (FewCfg::TASK_BYTES, one task),
-        // 128-byte swizzle
-        static_assert(FewCfg::TASK_BYTES == 128 * FewCfg::ROWS, "code box");
-        if ((st = make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 128, FewCfg::ROWS,
-                           CU_TENSOR_MAP_SWIZZLE_128B, "codes")))
-            return st;
-        FewParams prm{};
-        prm.X = X16;
-        prm.M = M;
-        prm.N = N;
-        prm.K = K;
-        prm.q = w.q;
-        prm.s2 = w.s2;
-        prm.mean = w.mean;
-        prm.sU = f.sU;
-        prm.ldu = rp;
-        prm.B = static_cast<const uint16_t *>(B);
-        prm.r = r;
-        prm.Y = static_cast<uint16_t *>(Y);
-        prm.slots = f.few_slots;
-        prm.counters = f.few_counters;
-        prm.tasks = fp.tasks;
-        prm.tpr = fp.tpr;
-        prm.warps = fp.warps;
-        prm.wait_ns = wait_ns();
-        {
-            static const float kLevels[2][16] = {QLORA_NF4_LEVELS, QLORA_INT4_LEVELS};
-            memcpy(prm.levels, kLevels[w.tab], sizeof prm.levels);
-        }
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)fp.grid);
-        cfg.blockDim = dim3((unsigned)(32 * fp.wpc));
-        cfg.dynamicSmemBytes = FewCfg::SMEM_BYTES;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e;
-        {
-            ProfScope ps(QLORA_KERNEL_FWD_SIMT, s);
-            e = cudaLaunchKernelEx(&cfg, kern, tmC, prm, (const float *)w.absmax);
-        }
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return fail(QLORA_ERR_CUDA, "k_fwd_few: launch failed: %s", cudaGetErrorString(e));
-        }
-        if ((st = launch_check("k_fwd_few"))) return st;
-        return ok();
+        // few tokens, K a multiple of 256: persistent HBM-bound kernel
+        const Wt *wp = &w;
+        return few_fwd_launch(X16, M, &wp, &A, &B, &Y, 1, r, scale, U16, ldu, f.sU, rp, f.few_slots, f.few_counters,
+                              s);
     }
 
     if (M <= kSmallMaxM && K <= kSmallMaxK) {
@@ -1556,10 +1597,24 @@ static bool group_tc_bwd(int64_t M, const GroupView &gv) {
 struct GroupWs {
     uint16_t *Acat, *sU, *sV, *U, *parts;
     float *dAcat;
+    float *few_slots;
+    uint32_t *few_counters;
     SkArea sk;
     char *rest;  // per-projection workspace of the one-by-one paths
     size_t rest_bytes;
 };
+// A group's few-token forward runs as one launch over all its projections
+// when each of them takes the few-token kernel.
+static bool group_few_fwd(int64_t M, const GroupView &gv) {
+    for (int g = 0; g < gv.n; ++g)
+        if (!few_path(M, gv.w[g].rows, gv.K)) return false;
+    return true;
+}
+static int64_t group_tiles(const GroupView &gv) {
+    int64_t t = 0;
+    for (int g = 0; g < gv.n; ++g) t += cdiv(gv.w[g].rows, FewCfg::ROWS);
+    return t;
+}
 static size_t group_ws(int64_t M, const GroupView &gv, int r, bool bwd, void *ws, size_t ws_bytes, GroupWs *out) {
     const int n = gv.n;
     const int64_t K = gv.K, R = (int64_t)n * r;
@@ -1570,6 +1625,11 @@ static size_t group_ws(int64_t M, const GroupView &gv, int r, bool bwd, void *ws
         w.Acat = c.take<uint16_t>((size_t)(R * K));
         w.sU = c.take<uint16_t>((size_t)(M * R));
         w.sk = take_sk_area(c);
+    } else if (!bwd && group_few_fwd(M, gv)) {
+        const FewPlan fp = few_plan_tiles(M, group_tiles(gv), K);
+        w.sU = c.take<uint16_t>((size_t)M * n * lora_pad(r));
+        w.few_slots = c.take<float>((size_t)fp.warps * few_slot_floats(M));
+        w.few_counters = c.take<uint32_t>((size_t)fp.tiles);
     } else if (bwd && group_tc_bwd(M, gv)) {
         w.Acat = c.take<uint16_t>((size_t)(R * K));
         w.sV = c.take<uint16_t>((size_t)(M * R));
@@ -1625,6 +1685,21 @@ static qlora_status group_fwd_impl(const void *X, int64_t M, const qlora_proj *p
     if (ws_bytes < need) return fail(QLORA_ERR_WORKSPACE, "group forward workspace %zu < %zu bytes", ws_bytes, need);
     const int64_t K = gv.K, R = (int64_t)n * r;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (group_few_fwd(M, gv)) {
+        // few tokens: one HBM-bound launch over the row tiles of every projection
+        const Wt *wp[kMaxGroup];
+        const void *Ap[kMaxGroup], *Bp[kMaxGroup];
+        void *Yp[kMaxGroup];
+        for (int g = 0; g < n; ++g) {
+            wp[g] = &gv.w[g];
+            Ap[g] = proj[g].A;
+            Bp[g] = proj[g].B;
+            Yp[g] = proj[g].Y;
+        }
+        return few_fwd_launch(static_cast<const uint16_t *>(X), M, wp, Ap, Bp, Yp, n, r, scale,
+                              static_cast<uint16_t *>(U_save), (int)R, gw.sU, lora_pad(r), gw.few_slots,
+                              gw.few_counters, s);
+    }
     if (!group_tc_fwd(M)) {
         // few tokens: the projections one by one (HBM-bound kernels)
         for (int g = 0; g < n; ++g)

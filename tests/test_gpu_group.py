@@ -5,7 +5,8 @@ functions (each projection's Y_g, U_g, dA_g, dB_g, and dX summed over the
 projections) with the linear layer's bar: relative Frobenius error <= 5e-3
 per output tensor. Shapes cover the tensor-core paths (one fused GEMM over all
 projections' columns, or rows for dX), ragged N and M, groups of one to four,
-the few-token paths (projections one by one), U recomputed in the backward,
+the few-token paths (the forward as one launch over the group's row tiles, the
+backward projection by projection), U recomputed in the backward,
 adapters given back to back or apart, and the batched side-path launches (all
 V passes of a group in one launch; dA with every dB in one launch when their
 ranks take the same number of 64-wide tiles, up to five problems).
@@ -93,8 +94,10 @@ def test_group_parity(g, oracle, M, Ns, K, r, scale, save_u, packed):
 
 
 @pytest.mark.parametrize("M,Ns,K,r,save_u", [
-    (5, [1024, 256, 256], 1024, 16, True),    # few-token forward, CUDA-core backward
+    (5, [1024, 256, 256], 1024, 16, True),    # few-token forward (one launch over the group), CUDA-core backward
     (16, [512, 512], 2048, 8, False),         # two 8-token tiles, U recomputed
+    (3, [100, 36, 520, 64], 512, 16, True),   # four projections, row tiles ragged at every projection's end
+    (1, [4096, 1024, 1024], 4096, 16, True),  # the 8B layer's q/k/v at one token
     (24, [300, 100], 320, 8, True),           # small-M forward; N % 8 != 0
     (70, [300, 96], 256, 16, True),           # tensor-core forward, CUDA-core backward (N % 8)
 ])
