@@ -290,6 +290,9 @@ qlora_status qlora_linear_bwd(const void *dY, const void *X, const void *U_saved
  * group runs as one fused GEMM launch over all projections' output columns
  * (forward) or over all their rows (dX), one LoRA down-projection over the
  * stacked A_g, and reads X once per pass instead of once per projection.
+ * With few tokens (M <= 16, K a multiple of 256) the forward is one
+ * weight-streaming launch over all projections' rows; smaller backwards run
+ * projection by projection.
  * Requirements: every weight has the same cols K; one rank r for all,
  * r % 8 == 0 and 8 <= r <= 128; one scale. All pointers are device
  * pointers, 16-byte aligned, owned by the caller. A QLORA_ERR_* status is
