@@ -3,6 +3,10 @@
 //
 //   Y [M, N] = X [M, K] . W'^T + (sU) [M, r] . B^T          (K % 256 == 0)
 //
+// One launch serves one projection or a group of up to four sharing X and K
+// (their row tiles one after the other in a single line of tiles, each with
+// its own tensor map, constants, B, Y and slice of sU).
+//
 // Work: the weight is cut into tasks of 32 rows x 256 k (four blocks of 64;
 // the codes of a task are one TMA box of 32 rows x 128 bytes), numbered row
 // tile by row tile: tile t holds tasks [t P, (t + 1) P), P = K / 256. The
